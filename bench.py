@@ -1,0 +1,454 @@
+"""Benchmark of the KDA hot path on one GB300 (or N, one process per GPU).
+
+One step = the whole path over one batch of the varlen workload: a packed
+prefill of 64 sequences (lengths uniform in [128, 8192], H = 16, d_k = 128,
+d_v = 256, chunk 64, bf16 q/k/v, fp32 alpha/beta/state) through kda_prefill
+(planner + chunkwise kernel), then 32 kda_decode_step calls continuing every
+sequence from its returned state.  Inputs are seeded synthetic data, resident
+in HBM before timing; they exceed L2 (about 11 GB per step), so no flush is
+needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on the host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gated_delta_rule_45_gb300 import synth  # noqa: E402
+
+METRIC = "KDA prefill tokens/s & decode state-updates/s at 1 GB300; % of TC/HBM roofline"
+UNIT = "tokens/s"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel from one ncu capture, scaled to this workload (see profiles/);
+# None until a capture of the current kernel exists.
+NCU_TRAFFIC_BYTES_PER_LAUNCH = None
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    ws, rank, _ = dist_env()
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend, rank=rank, world_size=ws)
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def reduce_max_sum(elapsed_s: float, units: float, device=None):
+    """Max of elapsed time and sum of units over ranks (identity when single-process)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workload
+def workload_bytes(spec, T: int, decode_steps: int):
+    """Algorithmic HBM bytes of one prefill launch and of one decode step."""
+    esz = 2 if spec.dtype == "bf16" else 4
+    per_token_head = 2 * spec.d_k * esz + spec.d_v * esz + spec.d_v * 4 + 4 + spec.d_v * esz
+    state = spec.num_seqs * spec.H * spec.d_v * spec.d_k * 4
+    prefill = T * spec.H * per_token_head + 2 * state + 4 * (spec.num_seqs + 1)
+    bh = spec.num_seqs * spec.H
+    decode = bh * (2 * spec.d_k * esz + spec.d_v * esz + spec.d_v * 4 + 4 + spec.d_v * esz) \
+        + 2 * state
+    return prefill, decode
+
+
+def make_workload(seed: int):
+    spec = synth.VARLEN
+    if seed != spec.seed:
+        import dataclasses
+        spec = dataclasses.replace(spec, seed=seed)
+    d = synth.prefill_inputs(spec)
+    steps = synth.decode_sequence_inputs(synth.VARLEN_DECODE_STEPS, spec.num_seqs, spec.H,
+                                         spec.d_k, spec.d_v, spec.dtype, spec.alpha_mu,
+                                         d["generator"])
+    return spec, d, steps
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle
+def time_oracle_sample(d, steps, pairs_wanted: int, budget_s: float, seed: int = 0):
+    """Time the oracle on sampled (sequence, head) pairs of the workload (prefill
+    over the whole sequence, then the 32 decode tokens).  Returns (tokens/s,
+    cores, description).  A token is counted per head, divided by H to give
+    tokens (all heads) per second, the unit of the GPU figure."""
+    import oracle
+    spec = d["spec"]
+    rng = np.random.default_rng(seed)
+    cu = d["cu_seqlens"].numpy()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    order = rng.permutation(spec.num_seqs * spec.H)
+    chosen = []
+    token_heads = 0
+    # pick pairs until about the budget's worth of work (≈ 8 d_k d_v flop per token-head,
+    # ~2 Gflop/s per core fp64 for this loop nest)
+    per_core_rate = 2.0e9
+    target = budget_s * per_core_rate * cores / (8.0 * spec.d_k * spec.d_v)
+    for idx in order[:pairs_wanted]:
+        n, h = divmod(int(idx), spec.H)
+        chosen.append((n, h))
+        token_heads += int(cu[n + 1] - cu[n]) + len(steps)
+        if token_heads >= target:
+            break
+    # gather packed inputs: prefill tokens followed by the decode tokens of each pair
+    qs, ks, vs, als, bes, lens, s0s = [], [], [], [], [], [], []
+    for n, h in chosen:
+        a, b = int(cu[n]), int(cu[n + 1])
+        qs.append(torch.cat([d["q"][a:b, h]] + [st["q"][n, h][None] for st in steps]))
+        ks.append(torch.cat([d["k"][a:b, h]] + [st["k"][n, h][None] for st in steps]))
+        vs.append(torch.cat([d["v"][a:b, h]] + [st["v"][n, h][None] for st in steps]))
+        als.append(torch.cat([d["alpha"][a:b, h]] + [st["alpha"][n, h][None] for st in steps]))
+        bes.append(torch.cat([d["beta"][a:b, h]] + [st["beta"][n, h][None] for st in steps]))
+        lens.append(b - a + len(steps))
+        s0s.append(d["S0"][n, h].double().numpy())
+    q = synth.bf16_bits(torch.cat(qs)[:, None])
+    k = synth.bf16_bits(torch.cat(ks)[:, None])
+    v = synth.bf16_bits(torch.cat(vs)[:, None])
+    al = torch.cat(als)[:, None].numpy()
+    be = torch.cat(bes)[:, None].numpy()
+    pcu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    S0 = np.stack(s0s)[:, None]
+    t0 = time.perf_counter()
+    oracle.prefill(q, k, v, al, be, S0, pcu, nthreads=cores)
+    dt = time.perf_counter() - t0
+    th = int(pcu[-1])
+    desc = (f"{len(chosen)} (sequence, head) pairs of the varlen workload, each over its "
+            f"whole prefill plus its 32 decode tokens: {th} token-heads, fp64, "
+            f"{dt:.1f} s on {cores} threads; tokens/s = token-heads/s / H")
+    return th / dt / spec.H, cores, desc, dt
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        init_dist("gloo")
+        if rank != 0:
+            barrier()
+            return
+    spec, d, steps = make_workload(synth.VARLEN.seed)
+    for _ in range(args.warmup):
+        time_oracle_sample(d, steps, pairs_wanted=4, budget_s=1.0, seed=99)
+    vals, times = [], []
+    desc = cores = None
+    for i in range(args.steps):
+        v, cores, desc, dt = time_oracle_sample(d, steps, pairs_wanted=64,
+                                                budget_s=args.ref_budget, seed=i)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same recipe as the GPU arm)",
+        "config": {"workload": "varlen: 64 seqs, lengths U[128,8192], H=16, d_k=128, d_v=256, "
+                               "+32 decode steps (bounded sample per step)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        barrier()
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args):
+    from gated_delta_rule_45_gb300 import kda
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist("nccl")
+    dev = torch.device("cuda", local)
+    kda.load()
+
+    spec, d, steps = make_workload(synth.VARLEN.seed + rank)
+    T = int(d["cu_seqlens"][-1])
+    N, H, d_k, d_v = spec.num_seqs, spec.H, spec.d_k, spec.d_v
+    n_dec = len(steps)
+    stream = torch.cuda.Stream(device=dev)
+
+    # device-resident inputs and outputs
+    g = {key: d[key].to(dev) for key in ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")}
+    dec = [{key: st[key].to(dev) for key in ("q", "k", "v", "alpha", "beta")} for st in steps]
+    o = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev)
+    S = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
+    o_dec = [torch.empty((N, H, d_v), dtype=torch.bfloat16, device=dev) for _ in range(n_dec)]
+    wsp = torch.empty(kda.workspace_size(N, H, d_k, d_v, spec.chunk), dtype=torch.uint8,
+                      device=dev)
+    torch.cuda.synchronize()
+
+    ev_pf = []
+
+    def step(record=False):
+        with torch.cuda.stream(stream):
+            if record:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e2 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                             g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
+            if record:
+                e1.record(stream)
+            for i in range(n_dec):
+                x = dec[i]
+                kda.decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S, o_dec[i],
+                                stream=stream)
+            if record:
+                e2.record(stream)
+                ev_pf.append((e0, e1, e2))
+
+    for _ in range(args.warmup):
+        step()
+    kda.device_status(wsp, stream=stream)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    pf_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev_pf]
+    dec_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev_pf]
+
+    tokens_per_step = T + n_dec * N
+    elapsed_max, units = reduce_max_sum(elapsed, float(tokens_per_step * args.steps), dev)
+    value = units / elapsed_max
+
+    prefill_bytes, decode_bytes = workload_bytes(spec, T, n_dec)
+    hbm_peak, peak_src = peaks()
+    pf_avg_s = statistics.mean(pf_ms) / 1e3
+    achieved = prefill_bytes / pf_avg_s / 1e9
+    dec_step_s = statistics.mean(dec_ms) / 1e3 / n_dec
+
+    # end to end: host buffers, copies inside the timed region
+    e2e = run_e2e(args, kda, d, steps, spec, dev, stream)
+
+    if rank == 0:
+        ours_launches = 2 + n_dec  # planner + prefill kernel + one kernel per decode step
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 in/out; bf16 hi/lo MMA + fp32 accumulate; fp32 state",
+            "data": "synthetic (seeded: torch.Generator seed 0 + rank)",
+            "config": {"workload": "varlen: 64 seqs, lengths U[128,8192], H=16, d_k=128, "
+                                   "d_v=256, chunk=64, S0~N(0,0.1^2), then 32 decode steps",
+                       "prefill_tokens": T, "decode_tokens": n_dec * N,
+                       "tokens_per_step": tokens_per_step,
+                       "l2": "no flush: inputs exceed L2 (%.1f GB per step)"
+                             % ((prefill_bytes + n_dec * decode_bytes) / 1e9)},
+            "components": {
+                "prefill_ms": statistics.mean(pf_ms),
+                "prefill_tokens_per_s": T / pf_avg_s,
+                "prefill_token_heads_per_s": T * H / pf_avg_s,
+                "decode_step_us": dec_step_s * 1e6,
+                "decode_state_updates_per_s": N * H / dec_step_s,
+                "decode_hbm_gbs": decode_bytes / dec_step_s / 1e9,
+                "decode_hbm_frac": decode_bytes / dec_step_s / 1e9 / hbm_peak,
+            },
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC_BYTES_PER_LAUNCH,
+                         "kernel": "kda_prefill (planner + chunk kernel)",
+                         "algorithmic_bytes_per_launch": prefill_bytes,
+                         "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"},
+            "clocks": clock_info,
+            "gpu_launches": ours_launches * args.steps,
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline:
+            v, cores, desc, _ = time_oracle_sample(d, steps, pairs_wanted=64,
+                                                   budget_s=args.ref_budget)
+            line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": desc}
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, kda, d, steps, spec, dev, stream):
+    """Same step through the public API with pinned host buffers; H2D of inputs and
+    D2H of outputs inside the timed region."""
+    keys = ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")
+    host = {key: d[key].pin_memory() for key in keys}
+    host_dec = [{key: st[key].pin_memory() for key in ("q", "k", "v", "alpha", "beta")}
+                for st in steps]
+    T = int(d["cu_seqlens"][-1])
+    N, H, d_k, d_v = spec.num_seqs, spec.H, spec.d_k, spec.d_v
+    g = {key: torch.empty_like(host[key], device=dev) for key in keys}
+    gd = [{key: torch.empty_like(x[key], device=dev) for key in x} for x in host_dec]
+    o = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev)
+    S = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
+    o_dec = torch.empty((len(steps), N, H, d_v), dtype=torch.bfloat16, device=dev)
+    wsp = torch.empty(kda.workspace_size(N), dtype=torch.uint8, device=dev)
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    od_h = torch.empty(o_dec.shape, dtype=o_dec.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values()) + \
+        sum(x.numel() * x.element_size() for hd in host_dec for x in hd.values())
+    d2h = sum(x.numel() * x.element_size() for x in (o_h, S_h, od_h))
+
+    def step():
+        with torch.cuda.stream(stream):
+            for key in keys:
+                g[key].copy_(host[key], non_blocking=True)
+            for i, hd in enumerate(host_dec):
+                for key in hd:
+                    gd[i][key].copy_(hd[key], non_blocking=True)
+            kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                             g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
+            for i, x in enumerate(gd):
+                kda.decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S, o_dec[i],
+                                stream=stream)
+            o_h.copy_(o, non_blocking=True)
+            S_h.copy_(S, non_blocking=True)
+            od_h.copy_(o_dec, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 3))
+    step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(e2e_steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    el, units = reduce_max_sum(t0.elapsed_time(t1) / 1e3,
+                               float((T + len(steps) * N) * e2e_steps), dev)
+    return {"value": units / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--ref-budget", type=float, default=None,
+                   help="seconds of CPU work per reference step / cpu_baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    # at least 3 untimed warm-up steps; the JSON line reports the number used
+    args.warmup = max(3, args.warmup)
+    if args.ref_budget is None:
+        args.ref_budget = max(1.0, min(8.0, 120.0 / max(1, args.steps)))
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

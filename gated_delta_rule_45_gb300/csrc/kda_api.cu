@@ -1,0 +1,202 @@
+// C ABI of libkda: argument validation, workspace layout and kernel dispatch.
+// Every entry point is declared and documented in include/kda.h.
+#include "kda_internal.h"
+
+#include <mutex>
+
+namespace kda {
+
+int sm_count() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev >= 64) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace kda
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+kda_status prefill_impl(const void* q, const void* k, const void* v, const float* alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens,
+                        int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                        int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
+                        void* workspace, size_t workspace_bytes, kda_prefill_kernel kernel,
+                        kda_stream_t stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_CHUNK_SIMT &&
+        kernel != KDA_KERNEL_CHUNK_TC)
+        return KDA_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * H > (int64_t)INT32_MAX / 64) return KDA_ERR_UNSUPPORTED;
+    if (!cu_seqlens || !S_T || !workspace) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !alpha || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < kda::WorkspaceLayout::bytes(num_seqs)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, alpha, beta, S0, o, S_T, workspace, cu_seqlens};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+    const size_t n_o = (size_t)total_tokens * H * d_v * esz;
+    const size_t n_s = (size_t)num_seqs * H * d_v * d_k * sizeof(float);
+    // outputs may not overlap inputs, except S_T == S0 exactly
+    if (S0 && S_T != S0 && overlaps(S_T, n_s, S0, n_s)) return KDA_ERR_INVALID_ARG;
+    const size_t n_qk = (size_t)total_tokens * H * d_k * esz;
+    const size_t n_v = (size_t)total_tokens * H * d_v * esz;
+    const size_t n_a = (size_t)total_tokens * H * d_v * sizeof(float);
+    const void* ins[] = {q, k, v, alpha, beta};
+    const size_t in_n[] = {n_qk, n_qk, n_v, n_a, (size_t)total_tokens * H * sizeof(float)};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(o, n_o, ins[i], in_n[i]) || overlaps(S_T, n_s, ins[i], in_n[i]))
+            return KDA_ERR_INVALID_ARG;
+    if (overlaps(o, n_o, S_T, n_s) || overlaps(o, n_o, S0, n_s)) return KDA_ERR_INVALID_ARG;
+
+    kda::PrefillArgs a;
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S0 = S0;
+    a.cu_seqlens = cu_seqlens; a.num_seqs = num_seqs; a.total_tokens = total_tokens;
+    a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.chunk = chunk; a.o = o; a.S_T = S_T;
+    char* ws = static_cast<char*>(workspace);
+    a.status = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kStatus);
+    a.counter = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kCounter);
+    a.order = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kOrder);
+
+    const bool tc_ok = kda::prefill_tc_supports(a);
+    if (kernel == KDA_KERNEL_CHUNK_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
+    const bool use_tc = kernel == KDA_KERNEL_CHUNK_TC || (kernel == KDA_KERNEL_AUTO && tc_ok);
+
+    if (kda::launch_planner(a, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (num_seqs == 0) return KDA_OK;
+    const cudaError_t err = use_tc ? kda::launch_prefill_tc(a, stream)
+                                   : kda::launch_prefill_simt(a, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
+                                  int32_t chunk) {
+    (void)H; (void)d_k; (void)d_v; (void)chunk;
+    if (num_seqs < 0) return 0;
+    return kda::WorkspaceLayout::bytes(num_seqs);
+}
+
+kda_status kda_prefill(const void* q, const void* k, const void* v, const float* alpha,
+                       const float* beta, const float* S0, const int32_t* cu_seqlens,
+                       int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                       int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
+                       void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    return prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
+                        d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, KDA_KERNEL_AUTO,
+                        stream);
+}
+
+kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const float* alpha,
+                          const float* beta, const float* S0, const int32_t* cu_seqlens,
+                          int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                          int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
+                          void* workspace, size_t workspace_bytes, kda_prefill_kernel kernel,
+                          kda_stream_t stream) {
+    return prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
+                        d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, kernel, stream);
+}
+
+kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d_k, int32_t d_v,
+                                 kda_dtype dtype, int32_t chunk) {
+    if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_CHUNK_SIMT &&
+        kernel != KDA_KERNEL_CHUNK_TC)
+        return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
+    if (kernel != KDA_KERNEL_CHUNK_TC) return KDA_OK;
+    kda::PrefillArgs a = {};
+    a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.chunk = chunk;
+    return kda::prefill_tc_supports(a) ? KDA_OK : KDA_ERR_UNSUPPORTED;
+}
+
+kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream) {
+    if (!workspace) return KDA_ERR_INVALID_ARG;
+    int32_t st = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&st, static_cast<const char*>(workspace) + kda::WorkspaceLayout::kStatus,
+                        sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    return st == 0 ? KDA_OK : KDA_ERR_DEVICE_INPUT;
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* alpha,
+                           const float* beta, float* S, int32_t B, int32_t H, int32_t d_k,
+                           int32_t d_v, kda_dtype dtype, void* o, kda_stream_t stream) {
+    if (B < 0 || H < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (d_k != 16 && d_k != 32 && d_k != 64 && d_k != 128 && d_k != 256)
+        return KDA_ERR_UNSUPPORTED;
+    if (d_v > 4096) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !alpha || !beta || !S || !o) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, alpha, beta, S, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+    const size_t n_s = (size_t)B * H * d_v * d_k * sizeof(float);
+    const size_t n_o = (size_t)B * H * d_v * esz;
+    const void* ins[] = {q, k, v, alpha, beta};
+    const size_t in_n[] = {(size_t)B * H * d_k * esz, (size_t)B * H * d_k * esz,
+                           (size_t)B * H * d_v * esz, (size_t)B * H * d_v * sizeof(float),
+                           (size_t)B * H * sizeof(float)};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(S, n_s, ins[i], in_n[i]) || overlaps(o, n_o, ins[i], in_n[i]))
+            return KDA_ERR_INVALID_ARG;
+    if (overlaps(o, n_o, S, n_s)) return KDA_ERR_INVALID_ARG;
+
+    kda::DecodeArgs a;
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S = S;
+    a.B = B; a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.o = o;
+    return kda::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported size or option";
+        case KDA_ERR_CUDA: return "CUDA error";
+        case KDA_ERR_DEVICE_INPUT: return "invalid device input (cu_seqlens)";
+        default: return "unknown status";
+    }
+}
+
+int32_t kda_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

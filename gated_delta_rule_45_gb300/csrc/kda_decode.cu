@@ -1,0 +1,140 @@
+// KDA decode step: one token per (sequence, head), state updated in place.
+//
+// Per row r of S (one value channel; "Kimi (AI)", section "Kimi Delta
+// Attention (KDA)", forget gating / predict / memory updating):
+//     a   = s_r . k          b = s_r . q          kappa = k . q
+//     v~  = alpha_r a
+//     s'  = alpha_r s_r + beta (v_r - v~) k
+//     o_r = s' . q = alpha_r b + beta (v_r - v~) kappa
+// so each fp32 state row is read once and written once: the kernel is a
+// single streaming pass over S (HBM-bound, ~1 flop per byte).
+//
+// Mapping: a row of d_k floats is split over LPR lanes (float4 per lane per
+// step); a warp covers 32/LPR rows per step and UNROLL steps, all loads issued
+// before any reduction so that each warp keeps UNROLL x 512 B in flight.
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeUnroll = 8;
+
+template <int DK>
+struct DecodeShape {
+    static constexpr int LPR = DK / 4 < 32 ? DK / 4 : 32;       // lanes per row
+    static constexpr int VEC = DK / (4 * LPR);                   // float4 per lane per row
+    static constexpr int RPW = 32 / LPR;                         // rows per warp step
+    static constexpr int ROWS_PER_CTA = kDecodeWarps * RPW * kDecodeUnroll;
+};
+
+template <int LPR>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+template <int DK, typename T>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                  const float* __restrict__ alpha, const float* __restrict__ beta,
+                  float* __restrict__ S, int32_t H, int32_t d_v, T* __restrict__ o) {
+    using Sh = DecodeShape<DK>;
+    const int bh = blockIdx.x;                  // b * H + h
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int sub = lane % Sh::LPR;             // lane within its row group
+    const int grp = lane / Sh::LPR;             // row group within the warp
+
+    // this lane's slice of k and q: columns (j * LPR + sub) * 4 .. +3
+    float kr[Sh::VEC][4], qr[Sh::VEC][4];
+    float kq = 0.f;
+#pragma unroll
+    for (int j = 0; j < Sh::VEC; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = (j * Sh::LPR + sub) * 4 + e;
+            kr[j][e] = Elem<T>::load(k + (size_t)bh * DK + c);
+            qr[j][e] = Elem<T>::load(q + (size_t)bh * DK + c);
+            kq = fmaf(kr[j][e], qr[j][e], kq);
+        }
+    }
+    kq = group_sum<Sh::LPR>(kq);
+    const float bt = beta[bh];
+
+    const int row0 = blockIdx.y * Sh::ROWS_PER_CTA + warp * (Sh::RPW * kDecodeUnroll);
+    float4 s[kDecodeUnroll][Sh::VEC];
+#pragma unroll
+    for (int u = 0; u < kDecodeUnroll; ++u) {
+        const int r = row0 + u * Sh::RPW + grp;
+        if (r < d_v) {
+            const float4* src = reinterpret_cast<const float4*>(S + ((size_t)bh * d_v + r) * DK);
+#pragma unroll
+            for (int j = 0; j < Sh::VEC; ++j) s[u][j] = __ldcs(src + j * Sh::LPR + sub);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kDecodeUnroll; ++u) {
+        const int r = row0 + u * Sh::RPW + grp;
+        float pa = 0.f, pb = 0.f;
+        if (r < d_v) {
+#pragma unroll
+            for (int j = 0; j < Sh::VEC; ++j) {
+                pa = fmaf(s[u][j].x, kr[j][0], pa); pb = fmaf(s[u][j].x, qr[j][0], pb);
+                pa = fmaf(s[u][j].y, kr[j][1], pa); pb = fmaf(s[u][j].y, qr[j][1], pb);
+                pa = fmaf(s[u][j].z, kr[j][2], pa); pb = fmaf(s[u][j].z, qr[j][2], pb);
+                pa = fmaf(s[u][j].w, kr[j][3], pa); pb = fmaf(s[u][j].w, qr[j][3], pb);
+            }
+        }
+        pa = group_sum<Sh::LPR>(pa);   // every lane takes part in the shuffles
+        pb = group_sum<Sh::LPR>(pb);
+        if (r < d_v) {
+            const size_t vi = (size_t)bh * d_v + r;
+            const float al = alpha[vi];
+            const float err = bt * (Elem<T>::load(v + vi) - al * pa);
+            float4* dst = reinterpret_cast<float4*>(S + vi * DK);
+#pragma unroll
+            for (int j = 0; j < Sh::VEC; ++j) {
+                float4 n;
+                n.x = fmaf(al, s[u][j].x, err * kr[j][0]);
+                n.y = fmaf(al, s[u][j].y, err * kr[j][1]);
+                n.z = fmaf(al, s[u][j].z, err * kr[j][2]);
+                n.w = fmaf(al, s[u][j].w, err * kr[j][3]);
+                __stcs(dst + j * Sh::LPR + sub, n);
+            }
+            if (sub == 0) Elem<T>::store(o + vi, fmaf(al, pb, err * kq));
+        }
+    }
+}
+
+template <int DK, typename T>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+    using Sh = DecodeShape<DK>;
+    dim3 grid(a.B * a.H, (a.d_v + Sh::ROWS_PER_CTA - 1) / Sh::ROWS_PER_CTA);
+    kda_decode_kernel<DK, T><<<grid, kDecodeWarps * 32, 0, stream>>>(
+        static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
+        a.alpha, a.beta, a.S, a.H, a.d_v, static_cast<T*>(a.o));
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_decode_dk(const DecodeArgs& a, cudaStream_t stream) {
+    switch (a.d_k) {
+        case 16: return launch_decode_t<16, T>(a, stream);
+        case 32: return launch_decode_t<32, T>(a, stream);
+        case 64: return launch_decode_t<64, T>(a, stream);
+        case 128: return launch_decode_t<128, T>(a, stream);
+        case 256: return launch_decode_t<256, T>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.dtype == KDA_BF16) return launch_decode_dk<__nv_bfloat16>(a, stream);
+    return launch_decode_dk<float>(a, stream);
+}
+
+}  // namespace kda

@@ -1,0 +1,88 @@
+// Internal declarations shared by the libkda translation units (CUDA path only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Layout of the prefill workspace (all offsets in bytes from its start).
+//   [0, 4)    int32 device status (0 = ok, KDA_ERR_DEVICE_INPUT)
+//   [4, 8)    int32 work counter of the persistent tensor-core kernel
+//   [16, ...) int32 order[num_seqs]: sequence indices, longest first
+struct WorkspaceLayout {
+    static constexpr size_t kStatus = 0;
+    static constexpr size_t kCounter = 4;
+    static constexpr size_t kOrder = 16;
+    static size_t bytes(int32_t num_seqs) {
+        size_t b = kOrder + sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 0);
+        return (b + 255) & ~(size_t)255;
+    }
+};
+
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    const float* S0;
+    const int32_t* cu_seqlens;
+    int32_t num_seqs;
+    int64_t total_tokens;
+    int32_t H, d_k, d_v;
+    kda_dtype dtype;
+    int32_t chunk;
+    void* o;
+    float* S_T;
+    int32_t* status;    // device
+    int32_t* counter;   // device
+    int32_t* order;     // device, [num_seqs]
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    float* S;
+    int32_t B, H, d_k, d_v;
+    kda_dtype dtype;
+    void* o;
+};
+
+// Launchers; each returns the CUDA error of its launch.
+cudaError_t launch_planner(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+bool prefill_tc_supports(const PrefillArgs& a);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+int sm_count();   // of the current device, cached per device
+
+// ---- small device helpers ------------------------------------------------
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static __device__ __forceinline__ float load(const float* p) { return *p; }
+    static __device__ __forceinline__ void store(float* p, float x) { *p = x; }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+};
+
+}  // namespace kda

@@ -1,0 +1,302 @@
+// Portable chunkwise KDA prefill on CUDA cores, all arithmetic in fp32.
+//
+// Chunk form of the recurrence ("Kimi (AI)", section "Kimi Delta Attention
+// (KDA)"; chunking: "grouping multiple steps" in the Kimi K3 architecture
+// walkthrough).  With D_t = diag(alpha_t) the update is
+// S_t = D_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T; D_t acts on rows
+// and the projector on columns, so each row of S is a scalar-gated delta rule.
+// For a chunk of C tokens, gamma_t = prod_{j<=t} alpha_j (per value channel):
+//
+//   A = I + diag(beta) strict_lower(K K^T),  T = A^{-1}     (C x C, shared by all rows)
+//   X = diag(beta) (V / Gamma - K S^T)                       (C x d_v)
+//   U = T X
+//   O = Gamma * (Q S^T + tril_incl(Q K^T) U)
+//   S <- diag(gamma_C) (S + U^T K)
+//
+// Rows past the end of a sequence are padded with k = q = v = 0, alpha = 1,
+// beta = 0; they leave S unchanged and their o is not stored.
+//
+// One CTA per (sequence, head, block of 64 value channels); CTAs are issued
+// in the planner's longest-first order.  This kernel covers every supported
+// shape (d_k <= 128, chunk 16/32/64, bf16 or fp32 storage) and is the path for
+// shapes the tensor-core kernel does not take.
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kDVB = 64;           // value channels per CTA
+constexpr int kDVP = kDVB + 1;     // padded row stride of [C][d_v-block] tiles
+constexpr int kMaxDK = 128;
+
+struct SimtSmem {
+    int KP, CP;
+    float *Ks, *Qs, *Ss, *Xs, *Us, *Gs, *Ls, *Ts, *Ps, *bs;
+};
+
+__host__ __device__ inline size_t simt_smem_floats(int C, int d_k) {
+    const int KP = d_k + 1, CP = C + 1;
+    return (size_t)2 * C * KP + (size_t)kDVB * KP + (size_t)3 * C * kDVP + (size_t)3 * C * CP + C;
+}
+
+__device__ inline SimtSmem carve(float* base, int C, int d_k) {
+    SimtSmem s;
+    s.KP = d_k + 1;
+    s.CP = C + 1;
+    float* p = base;
+    s.Ks = p; p += C * s.KP;
+    s.Qs = p; p += C * s.KP;
+    s.Ss = p; p += kDVB * s.KP;
+    s.Xs = p; p += C * kDVP;
+    s.Us = p; p += C * kDVP;
+    s.Gs = p; p += C * kDVP;
+    s.Ls = p; p += C * s.CP;
+    s.Ts = p; p += C * s.CP;
+    s.Ps = p; p += C * s.CP;
+    s.bs = p;
+    return s;
+}
+
+// acc[i][j] += sum_k A(m_i, k) B(n_j, k) for m_i = ty + 16 i < M, n_j = n0 + tx + 16 j < N,
+// with A(m, k) = A[m * sam + k * sak] and B(n, k) = B[n * sbn + k * sbk].
+__device__ __forceinline__ void mm_acc(float (&acc)[4][4], const float* A, int sam, int sak,
+                                       const float* B, int sbn, int sbk, int M, int N, int K,
+                                       int n0, int ty, int tx) {
+    for (int k = 0; k < K; ++k) {
+        float a[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = ty + 16 * i;
+            a[i] = m < M ? A[m * sam + k * sak] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx + 16 * j;
+            b[j] = n < N ? B[n * sbn + k * sbk] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+}
+
+__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+}
+
+template <typename T, int C>
+__global__ void __launch_bounds__(kThreads)
+kda_prefill_simt_kernel(PrefillArgs a) {
+    if (*a.status != 0) return;               // planner rejected cu_seqlens
+    extern __shared__ float smem[];
+    const int d_k = a.d_k, d_v = a.d_v, H = a.H;
+    SimtSmem s = carve(smem, C, d_k);
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+
+    const int nvb = (d_v + kDVB - 1) / kDVB;
+    const int item = blockIdx.x;
+    const int rank = item / (H * nvb);
+    const int h = (item / nvb) % H;
+    const int vb = item % nvb;
+    const int n = a.order[rank];
+    const int64_t t_begin = a.cu_seqlens[n], t_end = a.cu_seqlens[n + 1];
+    const int r0 = vb * kDVB;
+    const int rows = min(kDVB, d_v - r0);
+
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    const T* v = static_cast<const T*>(a.v);
+    T* o = static_cast<T*>(a.o);
+    const size_t state_off = ((size_t)n * H + h) * (size_t)d_v * d_k + (size_t)r0 * d_k;
+
+    for (int idx = tid; idx < kDVB * d_k; idx += kThreads) {
+        const int r = idx / d_k, c = idx % d_k;
+        float x = 0.f;
+        if (r < rows && a.S0) x = a.S0[state_off + (size_t)r * d_k + c];
+        s.Ss[r * s.KP + c] = x;
+    }
+    __syncthreads();
+
+    for (int64_t c0 = t_begin; c0 < t_end; c0 += C) {
+        const int nvalid = (int)min((int64_t)C, t_end - c0);
+        // load the chunk; padded tokens: k = q = v = 0, alpha = 1, beta = 0
+        for (int idx = tid; idx < C * d_k; idx += kThreads) {
+            const int t = idx / d_k, c = idx % d_k;
+            float kx = 0.f, qx = 0.f;
+            if (t < nvalid) {
+                const size_t gi = ((size_t)(c0 + t) * H + h) * d_k + c;
+                kx = Elem<T>::load(k + gi);
+                qx = Elem<T>::load(q + gi);
+            }
+            s.Ks[t * s.KP + c] = kx;
+            s.Qs[t * s.KP + c] = qx;
+        }
+        for (int idx = tid; idx < C * kDVB; idx += kThreads) {
+            const int t = idx / kDVB, r = idx % kDVB;
+            float vx = 0.f, ax = 1.f;
+            if (t < nvalid && r < rows) {
+                const size_t gi = ((size_t)(c0 + t) * H + h) * d_v + r0 + r;
+                vx = Elem<T>::load(v + gi);
+                ax = a.alpha[gi];
+            }
+            s.Xs[t * kDVP + r] = vx;
+            s.Gs[t * kDVP + r] = ax;
+        }
+        if (tid < C) s.bs[tid] = tid < nvalid ? a.beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        __syncthreads();
+
+        // Gamma: running product of alpha over the chunk, per value channel
+        if (tid < kDVB) {
+            float g = 1.f;
+            for (int t = 0; t < C; ++t) {
+                g *= s.Gs[t * kDVP + tid];
+                s.Gs[t * kDVP + tid] = g;
+            }
+        }
+        // L = diag(beta) strict_lower(K K^T);  P = tril_incl(Q K^T)
+        {
+            float acc[4][4], accp[4][4];
+            zero(acc);
+            zero(accp);
+            mm_acc(acc, s.Ks, s.KP, 1, s.Ks, s.KP, 1, C, C, d_k, 0, ty, tx);
+            mm_acc(accp, s.Qs, s.KP, 1, s.Ks, s.KP, 1, C, C, d_k, 0, ty, tx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int m = ty + 16 * i, nn = tx + 16 * j;
+                    if (m < C && nn < C) {
+                        s.Ls[m * s.CP + nn] = nn < m ? s.bs[m] * acc[i][j] : 0.f;
+                        s.Ps[m * s.CP + nn] = nn <= m ? accp[i][j] : 0.f;
+                    }
+                }
+        }
+        __syncthreads();
+
+        // T = (I + L)^{-1}, unit lower triangular; one thread per column,
+        // forward substitution T[i][c] = delta_ic - sum_{j<i} L[i][j] T[j][c]
+        if (tid < C) {
+            const int c = tid;
+            for (int i = 0; i < C; ++i) {
+                float x = (i == c) ? 1.f : 0.f;
+                if (i > c) {
+                    for (int j = c; j < i; ++j) x = fmaf(-s.Ls[i * s.CP + j], s.Ts[j * s.CP + c], x);
+                }
+                s.Ts[i * s.CP + c] = x;
+            }
+        }
+        // X = diag(beta) (V / Gamma - K S^T), written over V
+        {
+            float acc[4][4];
+            zero(acc);
+            mm_acc(acc, s.Ks, s.KP, 1, s.Ss, s.KP, 1, C, kDVB, d_k, 0, ty, tx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = ty + 16 * i, r = tx + 16 * j;
+                    if (t < C) {
+                        const float vg = s.Xs[t * kDVP + r] / s.Gs[t * kDVP + r];
+                        s.Xs[t * kDVP + r] = s.bs[t] * (vg - acc[i][j]);
+                    }
+                }
+        }
+        __syncthreads();
+
+        // U = T X
+        {
+            float acc[4][4];
+            zero(acc);
+            mm_acc(acc, s.Ts, s.CP, 1, s.Xs, 1, kDVP, C, kDVB, C, 0, ty, tx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = ty + 16 * i, r = tx + 16 * j;
+                    if (t < C) s.Us[t * kDVP + r] = acc[i][j];
+                }
+        }
+        __syncthreads();
+
+        // O = Gamma * (Q S^T + P U)
+        {
+            float acc[4][4];
+            zero(acc);
+            mm_acc(acc, s.Qs, s.KP, 1, s.Ss, s.KP, 1, C, kDVB, d_k, 0, ty, tx);
+            mm_acc(acc, s.Ps, s.CP, 1, s.Us, 1, kDVP, C, kDVB, C, 0, ty, tx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = ty + 16 * i, r = tx + 16 * j;
+                    if (t < nvalid && r < rows) {
+                        const float y = s.Gs[t * kDVP + r] * acc[i][j];
+                        Elem<T>::store(o + ((size_t)(c0 + t) * H + h) * d_v + r0 + r, y);
+                    }
+                }
+        }
+        __syncthreads();
+
+        // S <- diag(gamma_C) (S + U^T K)
+        for (int n0 = 0; n0 < d_k; n0 += 64) {
+            float acc[4][4];
+            zero(acc);
+            mm_acc(acc, s.Us, 1, kDVP, s.Ks, 1, s.KP, kDVB, d_k, C, n0, ty, tx);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = ty + 16 * i, c = n0 + tx + 16 * j;
+                    if (c < d_k) {
+                        const float gC = s.Gs[(C - 1) * kDVP + r];
+                        s.Ss[r * s.KP + c] = gC * (s.Ss[r * s.KP + c] + acc[i][j]);
+                    }
+                }
+        }
+        __syncthreads();
+    }
+
+    for (int idx = tid; idx < rows * d_k; idx += kThreads) {
+        const int r = idx / d_k, c = idx % d_k;
+        a.S_T[state_off + (size_t)r * d_k + c] = s.Ss[r * s.KP + c];
+    }
+}
+
+template <typename T, int C>
+cudaError_t launch_simt_t(const PrefillArgs& a, cudaStream_t stream) {
+    const size_t smem = simt_smem_floats(C, kMaxDK) * sizeof(float);
+    cudaError_t err = cudaFuncSetAttribute(kda_prefill_simt_kernel<T, C>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const int nvb = (a.d_v + kDVB - 1) / kDVB;
+    const int64_t blocks = (int64_t)a.num_seqs * a.H * nvb;
+    if (blocks == 0) return cudaSuccess;
+    kda_prefill_simt_kernel<T, C><<<(unsigned)blocks, kThreads,
+                                    simt_smem_floats(C, a.d_k) * sizeof(float), stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_simt_c(const PrefillArgs& a, cudaStream_t stream) {
+    switch (a.chunk) {
+        case 16: return launch_simt_t<T, 16>(a, stream);
+        case 32: return launch_simt_t<T, 32>(a, stream);
+        case 64: return launch_simt_t<T, 64>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream) {
+    if (a.d_k > kMaxDK) return cudaErrorInvalidValue;
+    if (a.dtype == KDA_BF16) return launch_simt_c<__nv_bfloat16>(a, stream);
+    return launch_simt_c<float>(a, stream);
+}
+
+}  // namespace kda

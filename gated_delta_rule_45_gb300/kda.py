@@ -1,0 +1,178 @@
+"""Python binding of libkda (ctypes).  Argument marshalling only.
+
+Every step of the recurrence runs in the CUDA kernels behind the C ABI in
+``include/kda.h``.  PyTorch supplies device memory and the stream; nothing
+here computes any part of the method, and there is no CPU fallback: if the
+library is missing or a call fails, an exception is raised.
+
+The names follow the C ABI: ``prefill`` / ``prefill_into`` wrap
+``kda_prefill`` / ``kda_prefill_ex``, ``decode_step`` wraps
+``kda_decode_step``, ``workspace_size`` wraps ``kda_prefill_workspace_size``
+and ``device_status`` wraps ``kda_prefill_device_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_INPUT = 0, 1, 2, 3, 4
+BF16, FP32 = 0, 1
+KERNEL_AUTO, KERNEL_CHUNK_SIMT, KERNEL_CHUNK_TC = 0, 1, 2
+_KERNELS = {"auto": KERNEL_AUTO, "simt": KERNEL_CHUNK_SIMT, "tc": KERNEL_CHUNK_TC}
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def load(path: str | None = None):
+    """Load libkda.so (built by ``gated_delta_rule_45_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libkda.so not found at {p}: build it with "
+                           "`python -m gated_delta_rule_45_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.kda_prefill_workspace_size.restype = sz
+    lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    prefill_args = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, ctypes.c_int, i32,
+                    vp, vp, vp, sz]
+    lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill.argtypes = prefill_args + [vp]
+    lib.kda_prefill_ex.restype = ctypes.c_int
+    lib.kda_prefill_ex.argtypes = prefill_args + [ctypes.c_int, vp]
+    lib.kda_prefill_supported.restype = ctypes.c_int
+    lib.kda_prefill_supported.argtypes = [ctypes.c_int, i32, i32, i32, ctypes.c_int, i32]
+    lib.kda_prefill_device_status.restype = ctypes.c_int
+    lib.kda_prefill_device_status.argtypes = [vp, vp]
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
+                                    vp, vp]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_version.restype = i32
+    lib.kda_version.argtypes = []
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"q, k, v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+
+
+def supported(kernel: str, H: int, d_k: int, d_v: int, dtype: torch.dtype, chunk: int) -> bool:
+    """Whether kda_prefill_ex with this kernel choice accepts the shape (host-only query)."""
+    code = BF16 if dtype == torch.bfloat16 else FP32
+    return load().kda_prefill_supported(_KERNELS[kernel], H, d_k, d_v, code, chunk) == OK
+
+
+def workspace_size(num_seqs: int, H: int = 1, d_k: int = 128, d_v: int = 128,
+                   chunk: int = 64) -> int:
+    return int(load().kda_prefill_workspace_size(num_seqs, H, d_k, d_v, chunk))
+
+
+def prefill_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace, *, chunk: int = 64,
+                 kernel: str = "auto", stream=None) -> None:
+    """Enqueue kda_prefill_ex on `stream` (default: current stream) into preallocated outputs.
+
+    q, k: [T, H, d_k]; v, o: [T, H, d_v] (bf16 or fp32, all the same); alpha:
+    [T, H, d_v] fp32; beta: [T, H] fp32; S0: [N, H, d_v, d_k] fp32 or None;
+    cu_seqlens: int32 [N+1] on the device; S_T: [N, H, d_v, d_k] fp32 (may be S0);
+    workspace: a uint8 device tensor of at least ``workspace_size(N)`` bytes.
+    """
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace)
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if alpha.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("alpha and beta must be float32")
+    if S_T.dtype != torch.float32 or (S0 is not None and S0.dtype != torch.float32):
+        raise TypeError("states must be float32")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype:
+        raise TypeError("q, k, v and o must share one dtype")
+    st = load().kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                               _ptr(cu_seqlens), N, T, H, d_k, d_v, dt, chunk, _ptr(o),
+                               _ptr(S_T), _ptr(workspace), workspace.numel(), _KERNELS[kernel],
+                               _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_prefill")
+
+
+def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64, kernel: str = "auto",
+            stream=None, check_device_status: bool = False):
+    """Allocate outputs with PyTorch and run kda_prefill; returns (o, S_T)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
+    S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=q.device)
+    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk), dtype=torch.uint8, device=q.device)
+    prefill_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, ws, chunk=chunk, kernel=kernel,
+                 stream=stream)
+    if check_device_status:
+        device_status(ws, stream=stream)
+    return o, S_T
+
+
+def device_status(workspace, stream=None) -> None:
+    """Synchronise `stream` and raise KdaError if the device rejected the last prefill's input."""
+    st = load().kda_prefill_device_status(_ptr(workspace), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_prefill (device check)")
+
+
+def decode_step(q, k, v, alpha, beta, S, o=None, *, stream=None):
+    """Enqueue kda_decode_step: S [B, H, d_v, d_k] fp32 updated in place; returns o [B, H, d_v]."""
+    B, H, d_k = q.shape
+    d_v = v.shape[2]
+    if o is None:
+        o = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
+    _check_cuda(q, k, v, alpha, beta, S, o)
+    if S.dtype != torch.float32 or alpha.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("S, alpha and beta must be float32")
+    dt = _dtype_code(q)
+    st = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S),
+                                B, H, d_k, d_v, dt, _ptr(o), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_decode_step")
+    return o

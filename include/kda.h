@@ -1,0 +1,172 @@
+/*
+ * kda.h -- C ABI of libkda, a GB300 (sm_103a) implementation of the Kimi
+ * Delta Attention (KDA) recurrence.
+ *
+ * The operation ("Kimi (AI)", Wikipedia mirror, section "Kimi Delta
+ * Attention (KDA)": the forget gating / predict / memory updating block, with
+ * the output o_t = S_t q_t of the naive linear attention line before it):
+ *
+ *     S~_t = diag(alpha_t) S_{t-1}
+ *     v~_t = S~_t k_t
+ *     S_t  = S~_t + beta_t (v_t - v~_t) k_t^T
+ *     o_t  = S_t q_t
+ *
+ * per (sequence, head).  S is d_v x d_k (a sum of v k^T outer products), so
+ * alpha_t has d_v entries and scales the rows of S (value channels); beta_t
+ * is one scalar per token and head.  No scale or normalisation is applied to
+ * q or k and there is no output gate: the page has none.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Memory: every tensor argument is a DEVICE pointer owned by the caller.
+ *   The library never allocates device memory, never frees caller memory and
+ *   keeps no state between calls except a per-device cache of the SM count
+ *   and the driver's tensor-map encoder entry point.
+ * - Layouts are dense, row-major, last index fastest, no padding:
+ *     q, k   [T][H][d_k]      v, o   [T][H][d_v]      (dtype: KDA_BF16 or KDA_FP32)
+ *     alpha  [T][H][d_v] fp32, each in (0, 1]         beta   [T][H] fp32
+ *     state  [N][H][d_v][d_k] fp32
+ *   Every pointer must be 16-byte aligned.
+ * - Stream: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream).  No call synchronises the host except
+ *   kda_prefill_device_status, which says so.
+ * - Errors: argument errors are returned synchronously and enqueue nothing.
+ *   A failed kernel launch returns KDA_ERR_CUDA.  Errors that depend on device
+ *   data (a malformed cu_seqlens) are detected on the device: the kernels then
+ *   write no output, and kda_prefill_device_status reports the error.
+ *   No C++ exception crosses this interface.
+ * - Alias rules: outputs must not overlap inputs, except that S_T may equal
+ *   S0 exactly (in-place state update).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misalignment, bad alias */
+    KDA_ERR_UNSUPPORTED = 2,   /* sizes outside what the kernels implement (see each call) */
+    KDA_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+    KDA_ERR_DEVICE_INPUT = 4   /* device data invalid: cu_seqlens not 0-based, decreasing or past T */
+} kda_status;
+
+typedef enum {
+    KDA_BF16 = 0,   /* q, k, v, o stored as bfloat16 */
+    KDA_FP32 = 1    /* q, k, v, o stored as float32 */
+} kda_dtype;
+
+/* Which prefill kernel runs.  AUTO picks the tensor-core kernel whenever the
+ * shape qualifies (dtype KDA_BF16, d_k == 128, d_v a multiple of 128,
+ * chunk == 64) and the portable chunk kernel otherwise. */
+typedef enum {
+    KDA_KERNEL_AUTO = 0,
+    KDA_KERNEL_CHUNK_SIMT = 1,   /* fp32 CUDA-core chunk kernel: any supported shape */
+    KDA_KERNEL_CHUNK_TC = 2      /* tcgen05 / TMEM / TMA chunk kernel */
+} kda_prefill_kernel;
+
+typedef void* kda_stream_t;   /* a cudaStream_t */
+
+/*
+ * Bytes of device workspace kda_prefill needs for `num_seqs` sequences (the
+ * other sizes are accepted for forward compatibility and do not change the
+ * result today).  Returns 0 for num_seqs < 0.  The workspace holds the
+ * varlen schedule (sequence order, work counter, device error word); its
+ * contents need no initialisation and are overwritten by every call.
+ */
+size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
+                                  int32_t chunk);
+
+/*
+ * Chunkwise-parallel prefill over a packed (varlen) batch.  Runs the
+ * recurrence above for every sequence n (tokens cu_seqlens[n] ..
+ * cu_seqlens[n+1]-1) and head h, starting from S0[n][h] (zeros when S0 is
+ * NULL); writes o for every token of every sequence and the final state S_T.
+ * A zero-length sequence gives S_T[n] = S0[n] (zeros when S0 is NULL).
+ * Tokens at or beyond cu_seqlens[num_seqs] are not read and their o is not
+ * written.
+ *
+ *   q, k, v, alpha, beta  inputs, layouts above, T = total_tokens
+ *   S0                    [N][H][d_v][d_k] fp32 or NULL
+ *   cu_seqlens            device int32 [num_seqs+1]: cu[0] == 0,
+ *                         non-decreasing, cu[num_seqs] <= total_tokens
+ *                         (checked on the device -> KDA_ERR_DEVICE_INPUT)
+ *   dtype                 storage type of q, k, v and o
+ *   chunk                 tokens per chunk: 16, 32 or 64
+ *   o                     output [T][H][d_v] (dtype)
+ *   S_T                   output [N][H][d_v][d_k] fp32; may equal S0
+ *   workspace             device memory of kda_prefill_workspace_size bytes,
+ *                         16-byte aligned; must not be shared by calls that
+ *                         may run concurrently
+ *
+ * Supported: 1 <= H, 16 <= d_k <= 128 and d_k % 16 == 0, 1 <= d_v <= 1024
+ * and d_v % 16 == 0, alpha in (0, 1] with every product of alpha over one
+ * chunk of one channel >= 1e-30 (the chunk form divides by it).
+ * num_seqs == 0 or total_tokens == 0 is a valid no-op apart from S_T = S0.
+ */
+kda_status kda_prefill(const void* q, const void* k, const void* v,
+                       const float* alpha, const float* beta, const float* S0,
+                       const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                       int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype, int32_t chunk,
+                       void* o, float* S_T, void* workspace, size_t workspace_bytes,
+                       kda_stream_t stream);
+
+/* kda_prefill with an explicit kernel choice (for testing both kernels on
+ * one shape).  Requesting KDA_KERNEL_CHUNK_TC for a shape it does not cover
+ * returns KDA_ERR_UNSUPPORTED. */
+kda_status kda_prefill_ex(const void* q, const void* k, const void* v,
+                          const float* alpha, const float* beta, const float* S0,
+                          const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                          int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype, int32_t chunk,
+                          void* o, float* S_T, void* workspace, size_t workspace_bytes,
+                          kda_prefill_kernel kernel, kda_stream_t stream);
+
+/*
+ * Whether `kernel` covers a prefill of this shape: KDA_OK if kda_prefill_ex
+ * would accept it, KDA_ERR_UNSUPPORTED if not, KDA_ERR_INVALID_ARG for an
+ * unknown enum value.  Host only; makes no CUDA call.
+ */
+kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d_k, int32_t d_v,
+                                 kda_dtype dtype, int32_t chunk);
+
+/*
+ * Blocks until `stream` has finished the work enqueued so far, then returns
+ * the device-side status a kda_prefill call on `workspace` recorded
+ * (KDA_OK or KDA_ERR_DEVICE_INPUT), or KDA_ERR_CUDA if the copy fails.
+ * This is the only call that synchronises the host.
+ */
+kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream);
+
+/*
+ * One decode step for B sequences with one new token each, state updated in
+ * place: for every (b, h), S[b][h] <- S_1 and o[b][h] <- S_1 q for the single
+ * token (q[b][h], k[b][h], v[b][h], alpha[b][h], beta[b][h]).
+ *
+ *   q, k   [B][H][d_k] (dtype)     v, o  [B][H][d_v] (dtype)
+ *   alpha  [B][H][d_v] fp32        beta  [B][H] fp32
+ *   S      [B][H][d_v][d_k] fp32, read and overwritten
+ *
+ * Supported: d_k in {16, 32, 64, 128, 256}; 1 <= d_v <= 4096; B, H >= 1
+ * (B == 0 is a valid no-op).
+ */
+kda_status kda_decode_step(const void* q, const void* k, const void* v,
+                           const float* alpha, const float* beta, float* S,
+                           int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                           void* o, kda_stream_t stream);
+
+/* Static description of a status code.  Never NULL. */
+const char* kda_status_string(kda_status s);
+
+/* Library ABI version, (major << 16) | minor. */
+int32_t kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

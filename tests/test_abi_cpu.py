@@ -1,0 +1,146 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/kda.h declares, and rejects bad arguments on the host before any
+CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_45_gb300 import build, kda
+    build.build()
+    return kda.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("kda_prefill", "kda_decode_step", "kda_prefill_workspace_size",
+                     "kda_status_string", "kda_prefill_device_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in kda.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    from gated_delta_rule_45_gb300 import kda
+    for code in range(6):
+        assert isinstance(kda.status_string(code), str)
+    assert kda.status_string(0) == "ok"
+    assert lib.kda_version() >> 16 == 1
+
+
+def test_workspace_size(lib):
+    from gated_delta_rule_45_gb300 import kda
+    assert kda.workspace_size(0) >= 16
+    assert kda.workspace_size(1000) >= 16 + 4 * 1000
+    assert kda.workspace_size(1000) % 256 == 0
+    assert lib.kda_prefill_workspace_size(-1, 1, 128, 128, 64) == 0
+
+
+P = ctypes.c_void_p
+
+
+def _fake(addr):
+    # never dereferenced: each call below must return before any CUDA work
+    return P(addr)
+
+
+def _prefill(lib, **kw):
+    args = dict(q=_fake(0x10000), k=_fake(0x20000), v=_fake(0x30000), alpha=_fake(0x40000),
+                beta=_fake(0x50000), S0=None, cu=_fake(0x60000), N=2, T=64, H=2, d_k=64,
+                d_v=64, dtype=0, chunk=64, o=_fake(0x70000), S_T=_fake(0x80000),
+                ws=_fake(0x90000), ws_bytes=4096, kernel=0)
+    args.update(kw)
+    return lib.kda_prefill_ex(args["q"], args["k"], args["v"], args["alpha"], args["beta"],
+                              args["S0"], args["cu"], args["N"], args["T"], args["H"],
+                              args["d_k"], args["d_v"], args["dtype"], args["chunk"], args["o"],
+                              args["S_T"], args["ws"], args["ws_bytes"], args["kernel"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(chunk=48), 2),
+    (dict(chunk=128), 2),
+    (dict(d_k=130), 2),
+    (dict(d_k=256), 2),
+    (dict(d_v=2048), 2),
+    (dict(d_v=40), 2),
+    (dict(H=0), 1),
+    (dict(N=-1), 1),
+    (dict(T=-5), 1),
+    (dict(dtype=7), 1),
+    (dict(kernel=9), 1),
+    (dict(cu=None), 1),
+    (dict(S_T=None), 1),
+    (dict(ws=None), 1),
+    (dict(q=None), 1),
+    (dict(ws_bytes=8), 1),
+    (dict(q=_fake(0x10004)), 1),            # misaligned
+    (dict(o=_fake(0x10000)), 1),            # o overlaps q
+    (dict(S0=_fake(0x80000 + 64)), 1),      # S_T partially overlaps S0
+    (dict(kernel=2, d_k=64), 2),            # tensor-core kernel needs d_k == 128
+])
+def test_prefill_rejects_on_host(lib, kw, expect):
+    assert _prefill(lib, **kw) == expect
+
+
+def _decode(lib, **kw):
+    args = dict(q=_fake(0x10000), k=_fake(0x20000), v=_fake(0x30000), alpha=_fake(0x40000),
+                beta=_fake(0x50000), S=_fake(0x100000), B=2, H=2, d_k=128, d_v=128, dtype=0,
+                o=_fake(0x90000))
+    args.update(kw)
+    return lib.kda_decode_step(args["q"], args["k"], args["v"], args["alpha"], args["beta"],
+                               args["S"], args["B"], args["H"], args["d_k"], args["d_v"],
+                               args["dtype"], args["o"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d_k=96), 2),
+    (dict(d_k=512), 2),
+    (dict(d_v=5000), 2),
+    (dict(H=0), 1),
+    (dict(B=-1), 1),
+    (dict(dtype=3), 1),
+    (dict(S=None), 1),
+    (dict(o=None), 1),
+    (dict(v=_fake(0x30002)), 1),
+    (dict(o=_fake(0x100000)), 1),           # o overlaps S
+])
+def test_decode_rejects_on_host(lib, kw, expect):
+    assert _decode(lib, **kw) == expect
+
+
+def test_supported_query(lib):
+    from gated_delta_rule_45_gb300 import kda
+    import torch
+    assert kda.supported("simt", 2, 64, 64, torch.float32, 16)
+    assert kda.supported("auto", 2, 128, 256, torch.bfloat16, 64)
+    assert not kda.supported("simt", 2, 130, 64, torch.float32, 16)
+    assert not kda.supported("tc", 2, 64, 128, torch.bfloat16, 64)
+    assert not kda.supported("tc", 2, 128, 128, torch.float32, 64)
+    assert lib.kda_prefill_supported(7, 1, 128, 128, 0, 64) == 1
+
+
+def test_decode_empty_batch_is_noop(lib):
+    assert _decode(lib, B=0, q=None, k=None, v=None, alpha=None, beta=None, S=None, o=None) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from gated_delta_rule_45_gb300 import kda
+    with pytest.raises(RuntimeError, match="libkda.so not found"):
+        kda.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,155 @@
+"""kda_prefill against the oracle on small and ragged problems (GPU).
+
+Sizes are chosen so the oracle finishes in seconds while still spanning
+several chunks, several value-channel blocks and partial last chunks.
+Both kernels run where the shape allows it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from gated_delta_rule_45_gb300 import kda, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _kernels_for(spec):
+    ks = ["simt"]
+    dt = torch.bfloat16 if spec.dtype == "bf16" else torch.float32
+    if kda.supported("tc", spec.H, spec.d_k, spec.d_v, dt, spec.chunk):
+        ks.append("tc")
+    return ks
+
+
+def _check(spec, kernel, S0_override="keep", tol=None):
+    d = synth.prefill_inputs(spec)
+    if S0_override is None:
+        d["S0"] = None
+    dev = parity.to_device(d)
+    o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], chunk=spec.chunk, kernel=kernel,
+                         check_device_status=True)
+    torch.cuda.synchronize()
+    pairs = [(n, h) for n in range(spec.num_seqs) for h in range(spec.H)]
+    ref = parity.oracle_pairs(d, pairs)
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    if tol is None:
+        tol = parity.TOL_BF16 if spec.dtype == "bf16" else parity.TOL_FP32
+    assert wo <= tol and ws <= tol, (kernel, wo, ws)
+    return o, S_T, d
+
+
+SMALL = [
+    synth.PrefillSpec(num_seqs=3, len_lo=1, len_hi=200, H=2, d_k=32, d_v=48, dtype="bf16",
+                      chunk=16, s0_std=0.1, seed=1),
+    synth.PrefillSpec(num_seqs=2, len_lo=100, len_hi=300, H=3, d_k=64, d_v=64, dtype="fp32",
+                      chunk=32, s0_std=0.1, seed=2),
+    synth.PrefillSpec(num_seqs=4, len_lo=1, len_hi=400, H=2, d_k=128, d_v=128, dtype="bf16",
+                      chunk=64, s0_std=0.1, seed=3),
+    synth.PrefillSpec(num_seqs=3, len_lo=60, len_hi=300, H=2, d_k=128, d_v=256, dtype="bf16",
+                      chunk=64, s0_std=0.1, seed=4),
+    synth.PrefillSpec(num_seqs=2, len_lo=129, len_hi=129, H=1, d_k=16, d_v=208, dtype="bf16",
+                      chunk=64, s0_std=0.0, seed=5),
+    synth.PrefillSpec(num_seqs=5, len_lo=64, len_hi=64, H=2, d_k=128, d_v=128, dtype="bf16",
+                      chunk=64, alpha_mu=5.0, s0_std=0.1, seed=6),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)))
+def test_prefill_small(idx):
+    spec = SMALL[idx]
+    for kernel in _kernels_for(spec):
+        _check(spec, kernel)
+
+
+def test_tiny_workload_fp32_chunk16():
+    """B = 1, H = 2, T = 64, d = 32, fp32, chunk 16 (the tiny oracle workload)."""
+    _check(synth.TINY, "auto")
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_chunk_size_invariance(chunk):
+    """The chunk size is an implementation choice: every chunk gives the oracle's answer."""
+    spec = synth.PrefillSpec(num_seqs=2, len_lo=150, len_hi=250, H=2, d_k=64, d_v=64,
+                             dtype="fp32", chunk=chunk, s0_std=0.2, seed=7)
+    _check(spec, "simt")
+
+
+def test_without_initial_state():
+    spec = synth.PrefillSpec(num_seqs=3, len_lo=10, len_hi=200, H=2, d_k=128, d_v=128,
+                             s0_std=0.1, seed=8)
+    for kernel in _kernels_for(spec):
+        _check(spec, kernel, S0_override=None)
+
+
+def test_in_place_state_and_zero_length():
+    """S_T may alias S0; zero-length sequences return S0 unchanged."""
+    spec = synth.PrefillSpec(num_seqs=4, len_lo=50, len_hi=150, H=2, d_k=128, d_v=128,
+                             s0_std=0.1, seed=9)
+    d = synth.prefill_inputs(spec)
+    # make sequences 1 and 3 empty
+    lengths = [d["lengths"][0], 0, d["lengths"][2], 0]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    T = int(cu[-1])
+    for key in ("q", "k", "v", "alpha", "beta"):
+        d[key] = d[key][:T].contiguous()
+    d["cu_seqlens"] = cu
+    dev = parity.to_device(d)
+    for kernel in _kernels_for(spec):
+        S = dev["S0"].clone()
+        o = torch.empty((T, spec.H, spec.d_v), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(kda.workspace_size(4), dtype=torch.uint8, device="cuda")
+        kda.prefill_into(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], S,
+                         dev["cu_seqlens"], o, S, ws, kernel=kernel)
+        kda.device_status(ws)
+        ref = parity.oracle_pairs(d, [(n, h) for n in range(4) for h in range(spec.H)])
+        wo, wsr = parity.compare_pairs(d, o, S, ref)
+        assert wo <= parity.TOL_BF16 and wsr <= parity.TOL_BF16, (kernel, wo, wsr)
+        assert torch.equal(S[1], dev["S0"][1]) and torch.equal(S[3], dev["S0"][3])
+
+
+def test_empty_batch_and_all_empty_sequences():
+    H, d_k, d_v = 2, 128, 128
+    z = lambda *s, dt=torch.bfloat16: torch.zeros(*s, dtype=dt, device="cuda")
+    # all sequences empty: S_T = S0
+    S0 = torch.randn(3, H, d_v, d_k, device="cuda")
+    S_T = torch.empty_like(S0)
+    cu = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kda.workspace_size(3), dtype=torch.uint8, device="cuda")
+    kda.prefill_into(z(0, H, d_k), z(0, H, d_k), z(0, H, d_v), z(0, H, d_v, dt=torch.float32),
+                     z(0, H, dt=torch.float32), S0, cu, z(0, H, d_v), S_T, ws)
+    kda.device_status(ws)
+    assert torch.equal(S_T, S0)
+    # no sequences at all
+    cu0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.prefill_into(z(0, H, d_k), z(0, H, d_k), z(0, H, d_v), z(0, H, d_v, dt=torch.float32),
+                     z(0, H, dt=torch.float32), None, cu0, z(0, H, d_v),
+                     torch.empty(0, H, d_v, d_k, device="cuda"), ws)
+    kda.device_status(ws)
+
+
+@pytest.mark.parametrize("bad", [[1, 5, 9], [0, 6, 4], [0, 4, 12]])
+def test_bad_cu_seqlens_reported_and_nothing_written(bad):
+    """A malformed cu_seqlens is caught on the device: status reported, outputs untouched."""
+    H, d_k, d_v, T = 2, 128, 128, 9
+    g = torch.Generator(device="cpu").manual_seed(0)
+    q = torch.randn(T, H, d_k, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(T, H, d_v, generator=g).to(torch.bfloat16).cuda()
+    al = torch.full((T, H, d_v), 0.9, device="cuda")
+    be = torch.full((T, H), 0.5, device="cuda")
+    cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+    o = torch.full((T, H, d_v), 5.0, dtype=torch.bfloat16, device="cuda")
+    S_T = torch.full((2, H, d_v, d_k), 5.0, device="cuda")
+    ws = torch.empty(kda.workspace_size(2), dtype=torch.uint8, device="cuda")
+    for kernel in ("simt", "tc"):
+        try:
+            kda.prefill_into(q, q, v, al, be, None, cu, o, S_T, ws, kernel=kernel)
+        except kda.KdaError as e:
+            assert e.status == kda.ERR_UNSUPPORTED and kernel == "tc"
+            continue
+        with pytest.raises(kda.KdaError) as ei:
+            kda.device_status(ws)
+        assert ei.value.status == kda.ERR_DEVICE_INPUT
+        assert torch.all(o == 5.0) and torch.all(S_T == 5.0)
