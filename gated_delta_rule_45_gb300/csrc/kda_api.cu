@@ -54,7 +54,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
     if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * H > (int64_t)INT32_MAX / 64) return KDA_ERR_UNSUPPORTED;
-    if (!cu_seqlens || !S_T || !workspace) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !workspace || (num_seqs > 0 && !S_T)) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !alpha || !beta || !o)) return KDA_ERR_INVALID_ARG;
     if (workspace_bytes < kda::WorkspaceLayout::bytes(num_seqs)) return KDA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, alpha, beta, S0, o, S_T, workspace, cu_seqlens};
@@ -149,7 +149,8 @@ kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream)
                         sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
-    return st == 0 ? KDA_OK : KDA_ERR_DEVICE_INPUT;
+    if (st == 0) return KDA_OK;
+    return st == KDA_ERR_DEVICE_TIMEOUT ? KDA_ERR_DEVICE_TIMEOUT : KDA_ERR_DEVICE_INPUT;
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* alpha,
@@ -193,6 +194,7 @@ const char* kda_status_string(kda_status s) {
         case KDA_ERR_UNSUPPORTED: return "unsupported size or option";
         case KDA_ERR_CUDA: return "CUDA error";
         case KDA_ERR_DEVICE_INPUT: return "invalid device input (cu_seqlens)";
+        case KDA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         default: return "unknown status";
     }
 }

@@ -53,7 +53,8 @@ typedef enum {
     KDA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misalignment, bad alias */
     KDA_ERR_UNSUPPORTED = 2,   /* sizes outside what the kernels implement (see each call) */
     KDA_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
-    KDA_ERR_DEVICE_INPUT = 4   /* device data invalid: cu_seqlens not 0-based, decreasing or past T */
+    KDA_ERR_DEVICE_INPUT = 4,  /* device data invalid: cu_seqlens not 0-based, decreasing or past T */
+    KDA_ERR_DEVICE_TIMEOUT = 5 /* a device-side wait hit its time limit; outputs are incomplete */
 } kda_status;
 
 typedef enum {
@@ -99,7 +100,8 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int3
  *   dtype                 storage type of q, k, v and o
  *   chunk                 tokens per chunk: 16, 32 or 64
  *   o                     output [T][H][d_v] (dtype)
- *   S_T                   output [N][H][d_v][d_k] fp32; may equal S0
+ *   S_T                   output [N][H][d_v][d_k] fp32; may equal S0; may be
+ *                         NULL only when num_seqs == 0
  *   workspace             device memory of kda_prefill_workspace_size bytes,
  *                         16-byte aligned; must not be shared by calls that
  *                         may run concurrently
@@ -137,7 +139,8 @@ kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d
 /*
  * Blocks until `stream` has finished the work enqueued so far, then returns
  * the device-side status a kda_prefill call on `workspace` recorded
- * (KDA_OK or KDA_ERR_DEVICE_INPUT), or KDA_ERR_CUDA if the copy fails.
+ * (KDA_OK, KDA_ERR_DEVICE_INPUT or KDA_ERR_DEVICE_TIMEOUT), or KDA_ERR_CUDA
+ * if the copy fails.
  * This is the only call that synchronises the host.
  */
 kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream);
