@@ -1,11 +1,781 @@
-// Tensor-core (tcgen05 / TMEM / TMA) chunkwise KDA prefill: placeholder until
-// the kernel lands; reports every shape as not covered.
+// Tensor-core chunkwise KDA prefill for GB300: tcgen05 MMAs with fp32
+// accumulators in TMEM, operands staged by TMA, persistent CTAs.
+//
+// Chunk form of the recurrence ("Kimi (AI)", section "Kimi Delta Attention
+// (KDA)"; chunk-wise parallelism as in the Kimi K3 architecture walkthrough):
+// per chunk of C = 64 tokens, gamma_t = prod_{j<=t} alpha_j per value channel,
+//
+//   T  = (I + diag(beta) strict_lower(K K^T))^{-1}          (64 x 64, shared by all rows)
+//   X  = diag(beta) (V / Gamma - K S^T)
+//   U  = T X
+//   O  = Gamma * (Q S^T + tril_incl(Q K^T) U)
+//   S <- diag(gamma_C) (S + U^T K)
+//
+// Everything is computed value-channel-major (the M = 128 dimension of every
+// MMA is a block of 128 rows of S), so each MMA result lands with one value
+// channel per TMEM lane:
+//   SKQ  = S [K;Q]^T        M128 N128 K128   (A = S from TMEM, B = [K;Q] tile)
+//   KQK  = [K;Q] K^T        M128 N64  K128   (rows 0-63: K K^T, rows 64-127: Q K^T)
+//   U^T  = X^T T^T          M128 N64  K64    (A = X^T from TMEM, B = T)
+//   O^T += U^T P^T          M128 N64  K64    (accumulates onto the Q S^T half of SKQ)
+//   S   += U^T K            M128 N128 K64    (B = the K tile read MN-major)
+// Operands that are not exact bf16 inputs (S, X, U, T, P) are split into
+// bf16 hi + lo parts, giving ~16 significant bits: products with exact bf16
+// data take two MMAs, products of two split operands three (hi*hi, hi*lo,
+// lo*hi).  Plain bf16 rounding of these intermediates would cost ~1e-3
+// relative error on its own.
+//
+// Roles (384 threads, one CTA per SM, items (sequence, head, 128-channel
+// block) assigned round-robin in the planner's longest-first order):
+//   warp 0      TMA producer: K, Q (128B-swizzled) and alpha, V tiles, beta
+//   warp 1      MMA issuer (one thread)
+//   warps 4-7   token group: T by forward substitution, P = tril_incl(Q K^T)
+//   warps 8-11  row group: one thread per value channel: Gamma, X, U staging,
+//               output, state decay and hi/lo staging of S
+// Every wait is bounded; on a timeout the CTA records KDA_ERR_DEVICE_TIMEOUT,
+// stops issuing work, drains what it issued, frees TMEM and exits.
 #include "kda_internal.h"
+#include "kda_tc.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 namespace kda {
+namespace {
 
-bool prefill_tc_supports(const PrefillArgs&) { return false; }
+using namespace tc;
 
-cudaError_t launch_prefill_tc(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int C = 64;        // tokens per chunk
+constexpr int DK = 128;      // key channels
+constexpr int DVB = 128;     // value channels per work item
+constexpr int kThreads = 384;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+// TMEM columns (512 allocated)
+constexpr uint32_t TM_S = 0;       // S, fp32, 128 columns
+constexpr uint32_t TM_SKQ = 128;   // S K^T | S Q^T (+ U P^T), then U^T in the first half
+constexpr uint32_t TM_KQK = 256;   // [K;Q] K^T, 64 columns
+constexpr uint32_t TM_SHI = 320;   // S hi, bf16 pairs, 64 columns
+constexpr uint32_t TM_SLO = 384;   // S lo
+constexpr uint32_t TM_XHI = 448;   // X^T then U^T hi, 32 columns
+constexpr uint32_t TM_XLO = 480;   // X^T then U^T lo
+constexpr uint32_t TM_COLS = 512;
+
+// Shared memory (offsets from a 1024-byte aligned base)
+constexpr uint32_t SM_KQ = 0;            // 2 stages: [k-block 2][128 rows: 64 K, 64 Q][128 B]
+constexpr uint32_t KQ_STAGE = 32768;
+constexpr uint32_t KQ_KBLOCK = 16384;
+constexpr uint32_t SM_ALPHA = 65536;     // [64 tokens][128 channels] fp32
+constexpr uint32_t SM_V = 98304;         // [64][128] bf16
+constexpr uint32_t SM_T = 114688;        // 2 buffers x (hi, lo) x [64][64] bf16, swizzled
+constexpr uint32_t SM_P = 147456;        // same for P
+constexpr uint32_t TP_BUF = 16384;
+constexpr uint32_t TP_LO = 8192;
+constexpr uint32_t SM_BETA = 180224;     // 2 stages x 64 fp32
+constexpr uint32_t SM_L = 180736;        // [64][LSTR] fp32: diag(beta) strict_lower(K K^T)
+constexpr uint32_t LSTR = 68;
+constexpr uint32_t SM_BAR = 198144;
+constexpr uint32_t SM_MISC = SM_BAR + 256;
+constexpr uint32_t SMEM_BYTES = SM_MISC + 64 + 1024;
+
+// mbarrier indices
+enum {
+    B_KQ_FULL = 0,     // [2] producer -> K/Q/beta stage loaded
+    B_KQ_EMPTY = 2,    // [2] MMA commit -> stage free
+    B_AV_FULL = 4,     // producer -> alpha/V loaded
+    B_AV_EMPTY = 5,    // row group (128) -> alpha/V consumed
+    B_KQK_DONE = 6,    // MMA commit -> [K;Q]K^T ready
+    B_KQK_FREE = 7,    // token group (128) -> KQK read
+    B_TP_READY = 8,    // [2] token group (128) -> T, P written
+    B_TP_FREE = 10,    // [2] MMA commit -> T, P buffer consumed
+    B_S_READY = 12,    // row group (128) -> S and S hi/lo staged
+    B_SKQ_DONE = 13,   // MMA commit
+    B_X_READY = 14,    // row group (128)
+    B_U_DONE = 15,     // MMA commit
+    B_U_READY = 16,    // row group (128)
+    B_SO_DONE = 17,    // MMA commit
+    B_COUNT = 18
+};
+
+struct TcParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_a;
+    const float* beta;
+    const float* S0;
+    float* S_T;
+    __nv_bfloat16* o;
+    const int32_t* cu;
+    const int32_t* order;
+    int32_t* status;
+    int32_t H, d_v, nvb, num_items;
+};
+
+struct ItemInfo {
+    int n, h, vb, len, nc;
+    int64_t t0;
+};
+
+__device__ __forceinline__ ItemInfo item_info(const TcParams& p, int item) {
+    ItemInfo it;
+    const int per_rank = p.H * p.nvb;
+    const int rank = item / per_rank, rem = item % per_rank;
+    it.h = rem / p.nvb;
+    it.vb = rem % p.nvb;
+    it.n = p.order[rank];
+    it.t0 = p.cu[it.n];
+    it.len = p.cu[it.n + 1] - p.cu[it.n];
+    it.nc = (it.len + C - 1) / C;
+    return it;
+}
+
+// Walks the chunks of this CTA's items in order, skipping empty items.
+struct ChunkCursor {
+    int item, c;
+    bool valid;
+    ItemInfo info;
+    __device__ void init(const TcParams& p) {
+        item = blockIdx.x;
+        c = 0;
+        seek(p);
+    }
+    __device__ void seek(const TcParams& p) {
+        valid = false;
+        while (item < p.num_items) {
+            info = item_info(p, item);
+            if (info.nc > 0) {
+                valid = true;
+                return;
+            }
+            item += gridDim.x;
+        }
+    }
+    __device__ void next(const TcParams& p) {
+        if (++c >= info.nc) {
+            c = 0;
+            item += gridDim.x;
+            seek(p);
+        }
+    }
+};
+
+struct Ctx {
+    uint8_t* smem;
+    uint64_t* bars;
+    volatile int* abort;
+    volatile int* slots;   // [2 groups][2] broadcast slots
+    volatile int* never;   // always 0: lets drain waits ignore the abort flag
+    uint32_t tmem;
+    int32_t* status;
+};
+
+__device__ __forceinline__ void fail(const Ctx& cx) {
+    *cx.abort = 1;
+    atomicExch(cx.status, (int32_t)KDA_ERR_DEVICE_TIMEOUT);
+}
+
+__device__ __forceinline__ bool wait1(const Ctx& cx, int b, uint32_t parity) {
+    if (mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs)) return true;
+    fail(cx);
+    return false;
+}
+
+// One thread of a 128-thread group waits; the outcome is shared through a
+// named barrier, so the whole group continues or stops together.  Each
+// thread then takes its own acquire on the (already completed) phase.
+struct Group {
+    int tid, bar_id, flip;
+    volatile int* slot;
+    __device__ bool wait(const Ctx& cx, int b, uint32_t parity) {
+        volatile int* s = slot + flip;
+        flip ^= 1;
+        if (tid == 0) *s = wait1(cx, b, parity) ? 1 : 0;
+        __syncwarp();   // bar.sync is warp-aligned: reconverge after the elected wait
+        named_bar_sync(bar_id, 128);
+        if (*s == 0) return false;
+        if (!mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs)) {
+            fail(cx);
+            return false;
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ uint32_t kq_addr(const Ctx& cx, int s) {
+    return smem_u32(cx.smem + SM_KQ + s * KQ_STAGE);
+}
+
+// ------------------------------------------------------------------ producer
+__device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
+    ChunkCursor cur;
+    cur.init(p);
+    uint32_t g = 0;
+    uint32_t kq_issued[2] = {0, 0}, av_issued = 0;
+    const float* beta_st = reinterpret_cast<const float*>(cx.smem + SM_BETA);
+    while (cur.valid) {
+        const int s = g & 1;
+        const int64_t tok0 = cur.info.t0 + (int64_t)cur.c * C;
+        const int nvalid = min(C, cur.info.len - cur.c * C);
+        const int h = cur.info.h;
+        if (g >= 2) {
+            int r = 1;
+            if (lane == 0) r = wait1(cx, B_KQ_EMPTY + s, ((g >> 1) + 1) & 1);
+            __syncwarp();
+            if (!__shfl_sync(0xffffffffu, r, 0)) break;
+        }
+        float* bst = const_cast<float*>(beta_st) + s * C;
+        for (int j = lane; j < C; j += 32)
+            bst[j] = j < nvalid ? p.beta[(tok0 + j) * p.H + h] : 0.f;
+        __syncwarp();
+        if (lane == 0) {
+            uint64_t* bar = &cx.bars[B_KQ_FULL + s];
+            uint8_t* st = cx.smem + SM_KQ + s * KQ_STAGE;
+            mbar_arrive_expect_tx(bar, KQ_STAGE);
+            tma_load_3d(st, &p.tm_k, bar, 0, h, (int32_t)tok0);
+            tma_load_3d(st + KQ_KBLOCK, &p.tm_k, bar, 64, h, (int32_t)tok0);
+            tma_load_3d(st + 8192, &p.tm_q, bar, 0, h, (int32_t)tok0);
+            tma_load_3d(st + KQ_KBLOCK + 8192, &p.tm_q, bar, 64, h, (int32_t)tok0);
+        }
+        ++kq_issued[s];
+        if (g >= 1) {
+            int r = 1;
+            if (lane == 0) r = wait1(cx, B_AV_EMPTY, (g - 1) & 1);
+            __syncwarp();
+            if (!__shfl_sync(0xffffffffu, r, 0)) break;
+        }
+        if (lane == 0) {
+            uint64_t* bar = &cx.bars[B_AV_FULL];
+            mbar_arrive_expect_tx(bar, 64 * DVB * 4 + 64 * DVB * 2);
+            tma_load_3d(cx.smem + SM_ALPHA, &p.tm_a, bar, cur.info.vb * DVB, h, (int32_t)tok0);
+            tma_load_3d(cx.smem + SM_V, &p.tm_v, bar, cur.info.vb * DVB, h, (int32_t)tok0);
+        }
+        ++av_issued;
+        ++g;
+        cur.next(p);
+    }
+    // drain: every issued copy must have landed before the CTA may exit
+    if (lane == 0) {
+        for (int s = 0; s < 2; ++s)
+            if (kq_issued[s]) mbar_wait(&cx.bars[B_KQ_FULL + s], (kq_issued[s] - 1) & 1, cx.never, kTimeoutNs);
+        if (av_issued) mbar_wait(&cx.bars[B_AV_FULL], (av_issued - 1) & 1, cx.never, kTimeoutNs);
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ bool issue_kqk(const TcParams& p, const Ctx& cx, uint32_t g) {
+    const int s = g & 1;
+    if (!wait1(cx, B_KQ_FULL + s, (g >> 1) & 1)) return false;
+    if (g >= 1 && !wait1(cx, B_KQK_FREE, (g - 1) & 1)) return false;
+    tc_fence_after();
+    const uint32_t base = kq_addr(cx, s);
+    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t d = smem_desc_sw128(base + (kk >> 2) * KQ_KBLOCK + (kk & 3) * 32, 0, 1024);
+        mma_ss(cx.tmem + TM_KQK, d, d, idesc, kk > 0);   // A = 128 rows [K;Q], B = first 64 rows
+    }
+    mma_commit(&cx.bars[B_KQK_DONE]);
+    return true;
+}
+
+__device__ void run_mma(const TcParams& p, const Ctx& cx) {
+    ChunkCursor cur, ahead;
+    cur.init(p);
+    ahead = cur;
+    uint32_t g = 0;
+    int last_commit_bar = -1;
+    uint32_t last_commit_parity = 0;
+    const uint32_t tm = cx.tmem;
+    const uint32_t id_n128 = idesc_bf16_f32(128, 128, 0, 0);
+    const uint32_t id_n64 = idesc_bf16_f32(128, 64, 0, 0);
+    const uint32_t id_n128_bmn = idesc_bf16_f32(128, 128, 0, 1);
+    bool ok = true;
+    if (cur.valid) {
+        ok = issue_kqk(p, cx, 0);
+        last_commit_bar = B_KQK_DONE;
+        last_commit_parity = 0;
+        ahead.next(p);
+    }
+    while (cur.valid && ok) {
+        const int s = g & 1;
+        const uint32_t kq = kq_addr(cx, s);
+        // SKQ = S_hi [K;Q]^T + S_lo [K;Q]^T
+        if (!(ok = wait1(cx, B_S_READY, g & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            const uint32_t a0 = tm + (part == 0 ? TM_SHI : TM_SLO);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t b =
+                    smem_desc_sw128(kq + (kk >> 2) * KQ_KBLOCK + (kk & 3) * 32, 0, 1024);
+                mma_ts(tm + TM_SKQ, a0 + 8 * kk, b, id_n128, (part | kk) != 0);
+            }
+        }
+        mma_commit(&cx.bars[B_SKQ_DONE]);
+        last_commit_bar = B_SKQ_DONE;
+        last_commit_parity = g & 1;
+        // next chunk's [K;Q]K^T, so the token group can build its T and P early
+        if (ahead.valid) {
+            if (!(ok = issue_kqk(p, cx, g + 1))) break;
+            last_commit_bar = B_KQK_DONE;
+            last_commit_parity = (g + 1) & 1;
+            ahead.next(p);
+        }
+        // U^T = X^T T^T   (hi*hi + hi*lo + lo*hi)
+        if (!(ok = wait1(cx, B_X_READY, g & 1))) break;
+        if (!(ok = wait1(cx, B_TP_READY + s, (g >> 1) & 1))) break;
+        tc_fence_after();
+        {
+            const uint32_t t_hi = smem_u32(cx.smem + SM_T + s * TP_BUF);
+            const uint32_t t_lo = t_hi + TP_LO;
+            const uint32_t as[3] = {tm + TM_XHI, tm + TM_XHI, tm + TM_XLO};
+            const uint32_t bs[3] = {t_hi, t_lo, t_hi};
+#pragma unroll
+            for (int part = 0; part < 3; ++part)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tm + TM_SKQ, as[part] + 8 * kk,
+                           smem_desc_sw128(bs[part] + kk * 32, 0, 1024), id_n64,
+                           (part | kk) != 0);
+        }
+        mma_commit(&cx.bars[B_U_DONE]);
+        last_commit_bar = B_U_DONE;
+        last_commit_parity = g & 1;
+        // O^T += U^T P^T ;  S += U^T K
+        if (!(ok = wait1(cx, B_U_READY, g & 1))) break;
+        tc_fence_after();
+        {
+            const uint32_t p_hi = smem_u32(cx.smem + SM_P + s * TP_BUF);
+            const uint32_t p_lo = p_hi + TP_LO;
+            const uint32_t as[3] = {tm + TM_XHI, tm + TM_XHI, tm + TM_XLO};
+            const uint32_t bs[3] = {p_hi, p_lo, p_hi};
+#pragma unroll
+            for (int part = 0; part < 3; ++part)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tm + TM_SKQ + 64, as[part] + 8 * kk,
+                           smem_desc_sw128(bs[part] + kk * 32, 0, 1024), id_n64, 1);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tm + TM_S, (part == 0 ? tm + TM_XHI : tm + TM_XLO) + 8 * kk,
+                           smem_desc_sw128(kq + kk * 2048, KQ_KBLOCK, 1024), id_n128_bmn, 1);
+        }
+        mma_commit(&cx.bars[B_SO_DONE]);
+        mma_commit(&cx.bars[B_TP_FREE + s]);
+        mma_commit(&cx.bars[B_KQ_EMPTY + s]);
+        last_commit_bar = B_SO_DONE;
+        last_commit_parity = g & 1;
+        ++g;
+        cur.next(p);
+    }
+    // drain: the MMAs issued last must finish before TMEM is released
+    if (last_commit_bar >= 0)
+        mbar_wait(&cx.bars[last_commit_bar], last_commit_parity, cx.never, kTimeoutNs);
+}
+
+// ------------------------------------------------------------------ token group
+__device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int quarter) {
+    Group grp{t, 1, 0, cx.slots};
+    ChunkCursor cur;
+    cur.init(p);
+    uint32_t g = 0;
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+    float* Ls = reinterpret_cast<float*>(cx.smem + SM_L);
+    while (cur.valid) {
+        const int s = g & 1;
+        if (!grp.wait(cx, B_KQK_DONE, g & 1)) break;
+        if (!grp.wait(cx, B_KQ_FULL + s, (g >> 1) & 1)) break;   // acquire for beta
+        if (g >= 2 && !grp.wait(cx, B_TP_FREE + s, ((g >> 1) + 1) & 1)) break;
+        tc_fence_after();
+        const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + s * C;
+        uint8_t* t_hi = cx.smem + SM_T + s * TP_BUF;
+        uint8_t* p_hi = cx.smem + SM_P + s * TP_BUF;
+        if (t < 64) {
+            // row t of L = diag(beta) strict_lower(K K^T)
+            const float bt = bst[t];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[16];
+                tmem_ld16(cx.tmem + lane_base + TM_KQK + 16 * q4, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const int col = 16 * q4 + j;
+                    float4 l;
+                    l.x = col + 0 < t ? bt * __uint_as_float(v[j + 0]) : 0.f;
+                    l.y = col + 1 < t ? bt * __uint_as_float(v[j + 1]) : 0.f;
+                    l.z = col + 2 < t ? bt * __uint_as_float(v[j + 2]) : 0.f;
+                    l.w = col + 3 < t ? bt * __uint_as_float(v[j + 3]) : 0.f;
+                    *reinterpret_cast<float4*>(Ls + t * LSTR + col) = l;
+                }
+            }
+        } else {
+            // row tq of P = tril_incl(Q K^T), split into hi / lo, 128B-swizzled
+            const int tq = t - 64;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[16];
+                tmem_ld16(cx.tmem + lane_base + TM_KQK + 16 * q4, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = 16 * q4 + 8 * h8 + 2 * e;
+                        const float x0 = col <= tq ? __uint_as_float(v[8 * h8 + 2 * e]) : 0.f;
+                        const float x1 = col + 1 <= tq ? __uint_as_float(v[8 * h8 + 2 * e + 1]) : 0.f;
+                        uint16_t h0, l0, h1, l1;
+                        split_bf16(x0, h0, l0);
+                        split_bf16(x1, h1, l1);
+                        hi[e] = pack2(h0, h1);
+                        lo[e] = pack2(l0, l1);
+                    }
+                    const uint32_t off = sw128_offset(tq, 16 * q4 + 8 * h8);
+                    *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(p_hi + TP_LO + off) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&cx.bars[B_KQK_FREE]);
+        named_bar_sync(1, 128);   // L complete
+        if (t < 64) {
+            // column c of T = (I + L)^{-1}: T[i][c] = delta_ic - sum_{j<i} L[i][j] T[j][c]
+            const int c = t;
+            float tc_[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                float a0 = i == c ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                const float* Lr = Ls + i * LSTR;
+#pragma unroll
+                for (int j = 0; j + 3 < i; j += 4) {
+                    const float4 l = *reinterpret_cast<const float4*>(Lr + j);
+                    a0 = fmaf(-l.x, tc_[j + 0], a0);
+                    a1 = fmaf(-l.y, tc_[j + 1], a1);
+                    a2 = fmaf(-l.z, tc_[j + 2], a2);
+                    a3 = fmaf(-l.w, tc_[j + 3], a3);
+                }
+#pragma unroll
+                for (int j = i & ~3; j < i; ++j) a0 = fmaf(-Lr[j], tc_[j], a0);
+                tc_[i] = (a0 + a1) + (a2 + a3);
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                uint16_t hb, lb;
+                split_bf16(tc_[i], hb, lb);
+                const uint32_t off = sw128_offset(i, c);
+                *reinterpret_cast<uint16_t*>(t_hi + off) = hb;
+                *reinterpret_cast<uint16_t*>(t_hi + TP_LO + off) = lb;
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&cx.bars[B_TP_READY + s]);
+        ++g;
+        cur.next(p);
+    }
+}
+
+// ------------------------------------------------------------------ row group
+__device__ __forceinline__ void stage_state_quarter(uint32_t taddr_lane, int q4, const float* x) {
+    // fp32 S (32 columns) and its hi/lo bf16 pairs (16 columns each)
+    uint32_t raw[32], hi[16], lo[16];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(x[j]);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        uint16_t h0, l0, h1, l1;
+        split_bf16(x[2 * j], h0, l0);
+        split_bf16(x[2 * j + 1], h1, l1);
+        hi[j] = pack2(h0, h1);
+        lo[j] = pack2(l0, l1);
+    }
+    tmem_st32(taddr_lane + TM_S + 32 * q4, raw);
+    tmem_st16(taddr_lane + TM_SHI + 16 * q4, hi);
+    tmem_st16(taddr_lane + TM_SLO + 16 * q4, lo);
+}
+
+__device__ void run_row_group(const TcParams& p, const Ctx& cx, int r, int quarter) {
+    Group grp{r, 2, 0, cx.slots + 2};
+    const uint32_t lane_addr = cx.tmem + ((uint32_t)(32 * quarter) << 16);
+    uint32_t g = 0;
+    bool ok = true;
+    const float* al = reinterpret_cast<const float*>(cx.smem + SM_ALPHA);
+    const uint16_t* vs = reinterpret_cast<const uint16_t*>(cx.smem + SM_V);
+    for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+        const ItemInfo it = item_info(p, item);
+        const int ch = it.vb * DVB + r;   // value channel
+        const size_t srow = (((size_t)it.n * p.H + it.h) * p.d_v + ch) * DK;
+        if (it.nc == 0) {
+            for (int j = 0; j < DK; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.S0) x = *reinterpret_cast<const float4*>(p.S0 + srow + j);
+                *reinterpret_cast<float4*>(p.S_T + srow + j) = x;
+            }
+            continue;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.S0) v4 = *reinterpret_cast<const float4*>(p.S0 + srow + 32 * q4 + j);
+                x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
+            }
+            stage_state_quarter(lane_addr, q4, x);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&cx.bars[B_S_READY]);
+
+        for (int c = 0; c < it.nc; ++c, ++g) {
+            const int64_t tok0 = it.t0 + (int64_t)c * C;
+            const int nvalid = min(C, it.len - c * C);
+            const bool last = c + 1 == it.nc;
+            if (!(ok = grp.wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
+            if (!(ok = grp.wait(cx, B_AV_FULL, g & 1))) break;
+            // Gamma: running product of alpha over the chunk (padded tokens: alpha = 1)
+            float gam[C];
+            {
+                float run = 1.f;
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    const float a = t < nvalid ? al[t * DVB + r] : 1.f;
+                    run *= a;
+                    gam[t] = run;
+                }
+            }
+            if (!(ok = grp.wait(cx, B_SKQ_DONE, g & 1))) break;
+            tc_fence_after();
+            const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
+            // X = beta (V / Gamma - S K^T), split and staged as the A operand of U^T = X^T T^T
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t sk[16], hi[8], lo[8];
+                tmem_ld16(lane_addr + TM_SKQ + 16 * q4, sk);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t0 = 16 * q4 + 2 * j;
+                    // padded tokens (beta = 0) contribute exactly nothing
+                    const float x0 = t0 < nvalid
+                                         ? bst[t0] * (bf2f(vs[t0 * DVB + r]) / gam[t0] -
+                                                      __uint_as_float(sk[2 * j]))
+                                         : 0.f;
+                    const float x1 = t0 + 1 < nvalid
+                                         ? bst[t0 + 1] * (bf2f(vs[(t0 + 1) * DVB + r]) /
+                                                              gam[t0 + 1] -
+                                                          __uint_as_float(sk[2 * j + 1]))
+                                         : 0.f;
+                    uint16_t h0, l0, h1, l1;
+                    split_bf16(x0, h0, l0);
+                    split_bf16(x1, h1, l1);
+                    hi[j] = pack2(h0, h1);
+                    lo[j] = pack2(l0, l1);
+                }
+                tmem_st8(lane_addr + TM_XHI + 8 * q4, hi);
+                tmem_st8(lane_addr + TM_XLO + 8 * q4, lo);
+            }
+            mbar_arrive(&cx.bars[B_AV_EMPTY]);   // alpha and V of this chunk consumed
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&cx.bars[B_X_READY]);
+
+            // U^T back from TMEM, split and staged as the A operand of U^T P^T and U^T K
+            if (!(ok = grp.wait(cx, B_U_DONE, g & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t u[16], hi[8], lo[8];
+                tmem_ld16(lane_addr + TM_SKQ + 16 * q4, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint16_t h0, l0, h1, l1;
+                    split_bf16(__uint_as_float(u[2 * j]), h0, l0);
+                    split_bf16(__uint_as_float(u[2 * j + 1]), h1, l1);
+                    hi[j] = pack2(h0, h1);
+                    lo[j] = pack2(l0, l1);
+                }
+                tmem_st8(lane_addr + TM_XHI + 8 * q4, hi);
+                tmem_st8(lane_addr + TM_XLO + 8 * q4, lo);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&cx.bars[B_U_READY]);
+
+            // O = Gamma * (Q S^T + P U);  S <- gamma_C (S + U^T K)
+            if (!(ok = grp.wait(cx, B_SO_DONE, g & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t ov[16];
+                tmem_ld16(lane_addr + TM_SKQ + 64 + 16 * q4, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = 16 * q4 + j;
+                    if (t < nvalid)
+                        p.o[((tok0 + t) * p.H + it.h) * (int64_t)p.d_v + ch] =
+                            __float2bfloat16_rn(gam[t] * __uint_as_float(ov[j]));
+                }
+            }
+            const float gC = gam[C - 1];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t sv[32];
+                tmem_ld32(lane_addr + TM_S + 32 * q4, sv);
+                tmem_ld_wait();
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = gC * __uint_as_float(sv[j]);
+                if (last) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(p.S_T + srow + 32 * q4 + j) =
+                            make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                } else {
+                    stage_state_quarter(lane_addr, q4, x);
+                }
+            }
+            if (!last) {
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&cx.bars[B_S_READY]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p) {
+    if (*p.status != 0) return;   // planner rejected cu_seqlens
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Ctx cx;
+    cx.smem = smem;
+    cx.bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + SM_MISC);
+    cx.abort = reinterpret_cast<volatile int*>(smem + SM_MISC + 4);
+    cx.never = reinterpret_cast<volatile int*>(smem + SM_MISC + 8);
+    cx.slots = reinterpret_cast<volatile int*>(smem + SM_MISC + 16);
+    cx.status = p.status;
+
+    if (tid == 0) {
+        *cx.abort = 0;
+        *cx.never = 0;
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 128, 1, 128, 128, 128,
+                                          1, 1, 128, 1, 128, 1, 128, 1};
+        for (int b = 0; b < B_COUNT; ++b) mbar_init(&cx.bars[b], counts[b]);
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_a);
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cx.tmem = *tslot;
+
+    if (warp == 0) {
+        run_producer(p, cx, lane);
+    } else if (warp == 1) {
+        if (lane == 0) run_mma(p, cx);
+        __syncwarp();   // the final __syncthreads is warp-aligned
+    } else if (warp >= 4 && warp < 8) {
+        run_token_group(p, cx, tid - 128, warp - 4);
+    } else if (warp >= 8) {
+        run_row_group(p, cx, tid - 256, warp - 8);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(cx.tmem, TM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 3-D map over a [T][H][D] tensor with a (box_d, 1, 64) box.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t esz, int64_t T,
+              int H, int D, uint32_t box_d, CUtensorMapSwizzle sw) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
+    cuuint32_t box[3] = {box_d, 1, (cuuint32_t)C};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_tc_supports(const PrefillArgs& a) {
+    return a.dtype == KDA_BF16 && a.d_k == DK && a.d_v % DVB == 0 && a.d_v <= 1024 &&
+           a.chunk == C;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
+    if (!prefill_tc_supports(a)) return cudaErrorInvalidValue;
+    // nothing to load: the portable kernel copies S0 to S_T
+    if (a.total_tokens == 0) return launch_prefill_simt(a, stream);
+    TcParams p;
+    if (!make_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, DK, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, DK, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, a.d_v,
+                  DVB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&p.tm_a, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.total_tokens, a.H,
+                  a.d_v, DVB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    p.beta = a.beta;
+    p.S0 = a.S0;
+    p.S_T = a.S_T;
+    p.o = static_cast<__nv_bfloat16*>(a.o);
+    p.cu = a.cu_seqlens;
+    p.order = a.order;
+    p.status = a.status;
+    p.H = a.H;
+    p.d_v = a.d_v;
+    p.nvb = a.d_v / DVB;
+    p.num_items = a.num_seqs * a.H * p.nvb;
+    if (p.num_items == 0) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(kda_prefill_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    const int sms = sm_count();
+    const int grid = p.num_items < sms ? p.num_items : sms;
+    kda_prefill_tc_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
 
 }  // namespace kda
