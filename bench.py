@@ -428,6 +428,78 @@ def run_e2e(args, kda, d, steps, spec, dev, stream):
             "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
 
+def run_component(args):
+    """Time one workload's kernel alone (``--workload prefill|long|decode``): the
+    other configurations, reported as kernel-level lines next to the full step."""
+    from gated_delta_rule_45_gb300 import kda
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    hbm_peak, peak_src = peaks()
+    events = []
+    if args.workload == "decode":
+        spec = synth.DECODE
+        d = synth.decode_inputs(spec)
+        g = {key: d[key].to(dev) for key in ("q", "k", "v", "alpha", "beta", "S")}
+        o = torch.empty((spec.B, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
+
+        def launch():
+            kda.decode_step(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S"], o,
+                            stream=stream)
+        esz = 2
+        bh = spec.B * spec.H
+        nbytes = bh * (2 * spec.d_k * esz + 2 * spec.d_v * esz + spec.d_v * 4 + 4
+                       + 2 * spec.d_v * spec.d_k * 4)
+        units, unit = bh, "state-updates/s"
+        desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
+    else:
+        spec = synth.WORKLOADS[args.workload]
+        d = synth.prefill_inputs(spec)
+        g = {key: (d[key].to(dev) if d[key] is not None else None)
+             for key in ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")}
+        T = int(d["cu_seqlens"][-1])
+        o = torch.empty((T, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
+        S = torch.empty((spec.num_seqs, spec.H, spec.d_v, spec.d_k), device=dev)
+        wsp = torch.empty(kda.workspace_size(spec.num_seqs), dtype=torch.uint8, device=dev)
+
+        def launch():
+            kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                             g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
+        nbytes, _ = workload_bytes(spec, T, 0)
+        units, unit = T, "tokens/s"
+        desc = (f"{args.workload}: N={spec.num_seqs}, T={T}, H={spec.H}, d_k={spec.d_k}, "
+                f"d_v={spec.d_v}, chunk={spec.chunk}")
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+            events.append((e0, e1))
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in events)
+    achieved = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": METRIC, "value": units / (ms / 1e3), "unit": unit, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in/out; fp32 state", "data": "synthetic (seeded)",
+        "config": {"workload": desc, "l2": "no flush: inputs exceed L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_src},
+        "clocks": clock_info, "component_only": True}), flush=True)
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -437,6 +509,9 @@ def main(argv=None):
     p.add_argument("--ref-budget", type=float, default=None,
                    help="seconds of CPU work per reference step / cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", choices=["varlen", "prefill", "long", "decode"],
+                   default="varlen",
+                   help="varlen (default): the full step; others time one kernel alone")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)
@@ -444,6 +519,8 @@ def main(argv=None):
         args.ref_budget = max(1.0, min(8.0, 120.0 / max(1, args.steps)))
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "varlen":
+        run_component(args)
     else:
         run_ours(args)
     if torch.distributed.is_available() and torch.distributed.is_initialized():
