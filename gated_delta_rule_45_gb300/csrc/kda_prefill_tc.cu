@@ -25,13 +25,14 @@
 // lo*hi).  Plain bf16 rounding of these intermediates would cost ~1e-3
 // relative error on its own.
 //
-// Roles (384 threads, one CTA per SM, items (sequence, head, 128-channel
+// Roles (448 threads, one CTA per SM, items (sequence, head, 128-channel
 // block) assigned round-robin in the planner's longest-first order):
 //   warp 0      TMA producer: K, Q (128B-swizzled) and alpha, V tiles, beta
 //   warp 1      MMA issuer (one thread)
-//   warps 4-7   token group: T by forward substitution, P = tril_incl(Q K^T)
-//   warps 8-11  row group: one thread per value channel: Gamma, X, U staging,
-//               output, state decay and hi/lo staging of S
+//   warps 2-5   token group: T by blocked (16 x 16) inversion, P = tril_incl(Q K^T)
+//   warps 6-13  row group: two threads per value channel (one per half of the
+//               chunk's tokens / of the key channels): Gamma, X, U staging,
+//               state decay and hi/lo staging of S, then the output
 // Every wait is bounded; on a timeout the CTA records KDA_ERR_DEVICE_TIMEOUT,
 // stops issuing work, drains what it issued, frees TMEM and exits.
 #include "kda_internal.h"
@@ -49,7 +50,7 @@ using namespace tc;
 constexpr int C = 64;        // tokens per chunk
 constexpr int DK = 128;      // key channels
 constexpr int DVB = 128;     // value channels per work item
-constexpr int kThreads = 384;
+constexpr int kThreads = 448;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // TMEM columns (512 allocated)
@@ -75,7 +76,9 @@ constexpr uint32_t TP_LO = 8192;
 constexpr uint32_t SM_BETA = 180224;     // 2 stages x 64 fp32
 constexpr uint32_t SM_L = 180736;        // [64][LSTR] fp32: diag(beta) strict_lower(K K^T)
 constexpr uint32_t LSTR = 68;
-constexpr uint32_t SM_BAR = 198144;
+constexpr uint32_t SM_TF = 198144;       // [64][LSTR] fp32: T
+constexpr uint32_t SM_Y = 215552;        // [3][16][17] fp32 scratch of the blocked inverse
+constexpr uint32_t SM_BAR = 218880;
 constexpr uint32_t SM_MISC = SM_BAR + 256;
 constexpr uint32_t SMEM_BYTES = SM_MISC + 64 + 1024;
 
@@ -84,16 +87,16 @@ enum {
     B_KQ_FULL = 0,     // [2] producer -> K/Q/beta stage loaded
     B_KQ_EMPTY = 2,    // [2] MMA commit -> stage free
     B_AV_FULL = 4,     // producer -> alpha/V loaded
-    B_AV_EMPTY = 5,    // row group (128) -> alpha/V consumed
+    B_AV_EMPTY = 5,    // row group (8 warps) -> alpha/V consumed
     B_KQK_DONE = 6,    // MMA commit -> [K;Q]K^T ready
-    B_KQK_FREE = 7,    // token group (128) -> KQK read
-    B_TP_READY = 8,    // [2] token group (128) -> T, P written
+    B_KQK_FREE = 7,    // token group (4 warps) -> KQK read
+    B_TP_READY = 8,    // [2] token group (4 warps) -> T, P written
     B_TP_FREE = 10,    // [2] MMA commit -> T, P buffer consumed
-    B_S_READY = 12,    // row group (128) -> S and S hi/lo staged
+    B_S_READY = 12,    // row group (8 warps) -> S and S hi/lo staged
     B_SKQ_DONE = 13,   // MMA commit
-    B_X_READY = 14,    // row group (128)
+    B_X_READY = 14,    // row group (8 warps)
     B_U_DONE = 15,     // MMA commit
-    B_U_READY = 16,    // row group (128)
+    B_U_READY = 16,    // row group (8 warps)
     B_SO_DONE = 17,    // MMA commit
     B_COUNT = 18
 };
@@ -179,18 +182,18 @@ __device__ __forceinline__ bool wait1(const Ctx& cx, int b, uint32_t parity) {
     return false;
 }
 
-// One thread of a 128-thread group waits; the outcome is shared through a
+// One thread of a thread group waits; the outcome is shared through a
 // named barrier, so the whole group continues or stops together.  Each
 // thread then takes its own acquire on the (already completed) phase.
 struct Group {
-    int tid, bar_id, flip;
+    int tid, bar_id, nthreads, flip;
     volatile int* slot;
     __device__ bool wait(const Ctx& cx, int b, uint32_t parity) {
         volatile int* s = slot + flip;
         flip ^= 1;
         if (tid == 0) *s = wait1(cx, b, parity) ? 1 : 0;
         __syncwarp();   // bar.sync is warp-aligned: reconverge after the elected wait
-        named_bar_sync(bar_id, 128);
+        named_bar_sync(bar_id, nthreads);
         if (*s == 0) return false;
         if (!mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs)) {
             fail(cx);
@@ -379,13 +382,21 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------ token group
-__device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int quarter) {
-    Group grp{t, 1, 0, cx.slots};
+// Per chunk: L = diag(beta) strict_lower(K K^T) and P = tril_incl(Q K^T) from
+// the KQK accumulator, then T = (I + L)^{-1} by blocks of 16: the four
+// diagonal blocks by forward substitution, then block rows a = 1..3 as
+// T_ab = -D_a sum_{b<=k<a} L_ak T_kb, and finally T and P as bf16 hi/lo tiles.
+__device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int warp, int lane) {
+    Group grp{t, 1, 128, 0, cx.slots};
+    const int quarter = warp & 3;
+    const int kr = 32 * quarter + lane;   // accumulator row: 0-63 K K^T, 64-127 Q K^T
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+    float* Ls = reinterpret_cast<float*>(cx.smem + SM_L);
+    float* Tf = reinterpret_cast<float*>(cx.smem + SM_TF);
+    float* Ys = reinterpret_cast<float*>(cx.smem + SM_Y);
     ChunkCursor cur;
     cur.init(p);
     uint32_t g = 0;
-    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    float* Ls = reinterpret_cast<float*>(cx.smem + SM_L);
     while (cur.valid) {
         const int s = g & 1;
         if (!grp.wait(cx, B_KQK_DONE, g & 1)) break;
@@ -395,9 +406,8 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int qua
         const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + s * C;
         uint8_t* t_hi = cx.smem + SM_T + s * TP_BUF;
         uint8_t* p_hi = cx.smem + SM_P + s * TP_BUF;
-        if (t < 64) {
-            // row t of L = diag(beta) strict_lower(K K^T)
-            const float bt = bst[t];
+        if (kr < 64) {
+            const float bt = bst[kr];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t v[16];
@@ -407,16 +417,15 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int qua
                 for (int j = 0; j < 16; j += 4) {
                     const int col = 16 * q4 + j;
                     float4 l;
-                    l.x = col + 0 < t ? bt * __uint_as_float(v[j + 0]) : 0.f;
-                    l.y = col + 1 < t ? bt * __uint_as_float(v[j + 1]) : 0.f;
-                    l.z = col + 2 < t ? bt * __uint_as_float(v[j + 2]) : 0.f;
-                    l.w = col + 3 < t ? bt * __uint_as_float(v[j + 3]) : 0.f;
-                    *reinterpret_cast<float4*>(Ls + t * LSTR + col) = l;
+                    l.x = col + 0 < kr ? bt * __uint_as_float(v[j + 0]) : 0.f;
+                    l.y = col + 1 < kr ? bt * __uint_as_float(v[j + 1]) : 0.f;
+                    l.z = col + 2 < kr ? bt * __uint_as_float(v[j + 2]) : 0.f;
+                    l.w = col + 3 < kr ? bt * __uint_as_float(v[j + 3]) : 0.f;
+                    *reinterpret_cast<float4*>(Ls + kr * LSTR + col) = l;
                 }
             }
         } else {
-            // row tq of P = tril_incl(Q K^T), split into hi / lo, 128B-swizzled
-            const int tq = t - 64;
+            const int tq = kr - 64;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t v[16];
@@ -429,12 +438,9 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int qua
                     for (int e = 0; e < 4; ++e) {
                         const int col = 16 * q4 + 8 * h8 + 2 * e;
                         const float x0 = col <= tq ? __uint_as_float(v[8 * h8 + 2 * e]) : 0.f;
-                        const float x1 = col + 1 <= tq ? __uint_as_float(v[8 * h8 + 2 * e + 1]) : 0.f;
-                        uint16_t h0, l0, h1, l1;
-                        split_bf16(x0, h0, l0);
-                        split_bf16(x1, h1, l1);
-                        hi[e] = pack2(h0, h1);
-                        lo[e] = pack2(l0, l1);
+                        const float x1 =
+                            col + 1 <= tq ? __uint_as_float(v[8 * h8 + 2 * e + 1]) : 0.f;
+                        split2_bf16(x0, x1, hi[e], lo[e]);
                     }
                     const uint32_t off = sw128_offset(tq, 16 * q4 + 8 * h8);
                     *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -444,65 +450,98 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int qua
             }
         }
         tc_fence_before();
-        mbar_arrive(&cx.bars[B_KQK_FREE]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cx.bars[B_KQK_FREE]);
         named_bar_sync(1, 128);   // L complete
+
+        // diagonal blocks: (I + L_bb)^{-1} column by column; the other threads
+        // clear the six blocks above the diagonal
         if (t < 64) {
-            // column c of T = (I + L)^{-1}: T[i][c] = delta_ic - sum_{j<i} L[i][j] T[j][c]
-            const int c = t;
-            float tc_[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                float a0 = i == c ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                const float* Lr = Ls + i * LSTR;
-#pragma unroll
-                for (int j = 0; j + 3 < i; j += 4) {
-                    const float4 l = *reinterpret_cast<const float4*>(Lr + j);
-                    a0 = fmaf(-l.x, tc_[j + 0], a0);
-                    a1 = fmaf(-l.y, tc_[j + 1], a1);
-                    a2 = fmaf(-l.z, tc_[j + 2], a2);
-                    a3 = fmaf(-l.w, tc_[j + 3], a3);
-                }
-#pragma unroll
-                for (int j = i & ~3; j < i; ++j) a0 = fmaf(-Lr[j], tc_[j], a0);
-                tc_[i] = (a0 + a1) + (a2 + a3);
+            const int b = t >> 4, cc = t & 15, c = 16 * b + cc;
+            for (int i = 0; i < 16; ++i) {
+                float x = i == cc ? 1.f : 0.f;
+                for (int j = cc; j < i; ++j)
+                    x = fmaf(-Ls[(16 * b + i) * LSTR + 16 * b + j], Tf[(16 * b + j) * LSTR + c], x);
+                Tf[(16 * b + i) * LSTR + c] = x;
             }
+        } else {
+            for (int e = t - 64; e < 6 * 256; e += 64) {
+                const int blk = e >> 8, w = e & 255;
+                const int ba = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                Tf[(16 * ba + (w >> 4)) * LSTR + 16 * bb + (w & 15)] = 0.f;
+            }
+        }
+        named_bar_sync(1, 128);
+        for (int a = 1; a < 4; ++a) {
+            for (int e = t; e < a * 256; e += 128) {
+                const int b = e >> 8, i = (e >> 4) & 15, j = e & 15;
+                float y = 0.f;
+                for (int k = b; k < a; ++k) {
+                    const float* Lr = Ls + (16 * a + i) * LSTR + 16 * k;
+                    const float* Tc = Tf + (16 * k) * LSTR + 16 * b + j;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                uint16_t hb, lb;
-                split_bf16(tc_[i], hb, lb);
-                const uint32_t off = sw128_offset(i, c);
-                *reinterpret_cast<uint16_t*>(t_hi + off) = hb;
-                *reinterpret_cast<uint16_t*>(t_hi + TP_LO + off) = lb;
+                    for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Tc[m * LSTR], y);
+                }
+                Ys[(16 * b + i) * 17 + j] = y;
+            }
+            named_bar_sync(1, 128);
+            for (int e = t; e < a * 256; e += 128) {
+                const int b = e >> 8, i = (e >> 4) & 15, j = e & 15;
+                const float* Dr = Tf + (16 * a + i) * LSTR + 16 * a;
+                float x = 0.f;
+                for (int m = 0; m <= i; ++m) x = fmaf(-Dr[m], Ys[(16 * b + m) * 17 + j], x);
+                Tf[(16 * a + i) * LSTR + 16 * b + j] = x;
+            }
+            named_bar_sync(1, 128);
+        }
+        // T as bf16 hi/lo, 128B-swizzled B operand: thread t writes half of row t / 2
+        {
+            const int i = t >> 1, c0 = (t & 1) * 32;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const float4 x0 = *reinterpret_cast<const float4*>(Tf + i * LSTR + c0 + 8 * ch);
+                const float4 x1 = *reinterpret_cast<const float4*>(Tf + i * LSTR + c0 + 8 * ch + 4);
+                uint32_t hi[4], lo[4];
+                split2_bf16(x0.x, x0.y, hi[0], lo[0]);
+                split2_bf16(x0.z, x0.w, hi[1], lo[1]);
+                split2_bf16(x1.x, x1.y, hi[2], lo[2]);
+                split2_bf16(x1.z, x1.w, hi[3], lo[3]);
+                const uint32_t off = sw128_offset(i, c0 + 8 * ch);
+                *reinterpret_cast<uint4*>(t_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(t_hi + TP_LO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&cx.bars[B_TP_READY + s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cx.bars[B_TP_READY + s]);
         ++g;
         cur.next(p);
     }
 }
 
 // ------------------------------------------------------------------ row group
-__device__ __forceinline__ void stage_state_quarter(uint32_t taddr_lane, int q4, const float* x) {
-    // fp32 S (32 columns) and its hi/lo bf16 pairs (16 columns each)
-    uint32_t raw[32], hi[16], lo[16];
+// Thread (r, h): value channel r of the item's block; h selects tokens
+// 32h..32h+31 for X, U and O, and key channels 64h..64h+63 for S.
+__device__ __forceinline__ void stage_state_half(uint32_t lane_addr, int h, const float* x) {
+    uint32_t raw[32], hi[32], lo[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(x[j]);
+    for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        uint16_t h0, l0, h1, l1;
-        split_bf16(x[2 * j], h0, l0);
-        split_bf16(x[2 * j + 1], h1, l1);
-        hi[j] = pack2(h0, h1);
-        lo[j] = pack2(l0, l1);
+        for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(x[32 * half + j]);
+        tmem_st32(lane_addr + TM_S + 64 * h + 32 * half, raw);
     }
-    tmem_st32(taddr_lane + TM_S + 32 * q4, raw);
-    tmem_st16(taddr_lane + TM_SHI + 16 * q4, hi);
-    tmem_st16(taddr_lane + TM_SLO + 16 * q4, lo);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) split2_bf16(x[2 * j], x[2 * j + 1], hi[j], lo[j]);
+    tmem_st32(lane_addr + TM_SHI + 32 * h, hi);
+    tmem_st32(lane_addr + TM_SLO + 32 * h, lo);
 }
 
-__device__ void run_row_group(const TcParams& p, const Ctx& cx, int r, int quarter) {
-    Group grp{r, 2, 0, cx.slots + 2};
+__device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp, int lane) {
+    Group grp{rt, 2, 256, 0, cx.slots + 2};
+    const int quarter = warp & 3;
+    const int h = rt >> 7;                 // token half / key-channel half
+    const int r = 32 * quarter + lane;     // value channel within the block = TMEM lane
     const uint32_t lane_addr = cx.tmem + ((uint32_t)(32 * quarter) << 16);
     uint32_t g = 0;
     bool ok = true;
@@ -511,29 +550,29 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int r, int quart
     for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
         const ItemInfo it = item_info(p, item);
         const int ch = it.vb * DVB + r;   // value channel
-        const size_t srow = (((size_t)it.n * p.H + it.h) * p.d_v + ch) * DK;
+        const size_t srow = (((size_t)it.n * p.H + it.h) * p.d_v + ch) * DK + 64 * h;
         if (it.nc == 0) {
-            for (int j = 0; j < DK; j += 4) {
+            for (int j = 0; j < 64; j += 4) {
                 float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (p.S0) x = *reinterpret_cast<const float4*>(p.S0 + srow + j);
                 *reinterpret_cast<float4*>(p.S_T + srow + j) = x;
             }
             continue;
         }
+        {
+            float x[64];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            float x[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
+            for (int j = 0; j < 64; j += 4) {
                 float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.S0) v4 = *reinterpret_cast<const float4*>(p.S0 + srow + 32 * q4 + j);
+                if (p.S0) v4 = *reinterpret_cast<const float4*>(p.S0 + srow + j);
                 x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
             }
-            stage_state_quarter(lane_addr, q4, x);
+            stage_state_half(lane_addr, h, x);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&cx.bars[B_S_READY]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
 
         for (int c = 0; c < it.nc; ++c, ++g) {
             const int64_t tok0 = it.t0 + (int64_t)c * C;
@@ -541,114 +580,118 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int r, int quart
             const bool last = c + 1 == it.nc;
             if (!(ok = grp.wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
             if (!(ok = grp.wait(cx, B_AV_FULL, g & 1))) break;
-            // Gamma: running product of alpha over the chunk (padded tokens: alpha = 1)
-            float gam[C];
+            const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
+            // Gamma over the whole chunk (padded tokens: alpha = 1); keep this
+            // thread's half, and vg = beta V / Gamma for its tokens
+            float gam[32], vg[32], gC;
             {
                 float run = 1.f;
+#pragma unroll 8
+                for (int t = 0; t < 32 * h; ++t) run *= t < nvalid ? al[t * DVB + r] : 1.f;
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    const float a = t < nvalid ? al[t * DVB + r] : 1.f;
-                    run *= a;
-                    gam[t] = run;
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * h + j;
+                    run *= t < nvalid ? al[t * DVB + r] : 1.f;
+                    gam[j] = run;
+                    vg[j] = t < nvalid ? bst[t] * __fdividef(bf2f(vs[t * DVB + r]), run) : 0.f;
                 }
+#pragma unroll 8
+                for (int t = 32 * h + 32; t < C; ++t) run *= t < nvalid ? al[t * DVB + r] : 1.f;
+                gC = run;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.bars[B_AV_EMPTY]);   // alpha, V consumed
+
+            // X = vg - beta (S K^T), split and staged as the A operand of U^T = X^T T^T
             if (!(ok = grp.wait(cx, B_SKQ_DONE, g & 1))) break;
             tc_fence_after();
-            const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
-            // X = beta (V / Gamma - S K^T), split and staged as the A operand of U^T = X^T T^T
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 uint32_t sk[16], hi[8], lo[8];
-                tmem_ld16(lane_addr + TM_SKQ + 16 * q4, sk);
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16 * q2, sk);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int t0 = 16 * q4 + 2 * j;
-                    // padded tokens (beta = 0) contribute exactly nothing
-                    const float x0 = t0 < nvalid
-                                         ? bst[t0] * (bf2f(vs[t0 * DVB + r]) / gam[t0] -
-                                                      __uint_as_float(sk[2 * j]))
-                                         : 0.f;
-                    const float x1 = t0 + 1 < nvalid
-                                         ? bst[t0 + 1] * (bf2f(vs[(t0 + 1) * DVB + r]) /
-                                                              gam[t0 + 1] -
-                                                          __uint_as_float(sk[2 * j + 1]))
-                                         : 0.f;
-                    uint16_t h0, l0, h1, l1;
-                    split_bf16(x0, h0, l0);
-                    split_bf16(x1, h1, l1);
-                    hi[j] = pack2(h0, h1);
-                    lo[j] = pack2(l0, l1);
+                    const int jj = 16 * q2 + 2 * j;
+                    const int t = 32 * h + jj;
+                    const float x0 = fmaf(-bst[t], __uint_as_float(sk[2 * j]), vg[jj]);
+                    const float x1 = fmaf(-bst[t + 1], __uint_as_float(sk[2 * j + 1]), vg[jj + 1]);
+                    split2_bf16(x0, x1, hi[j], lo[j]);
                 }
-                tmem_st8(lane_addr + TM_XHI + 8 * q4, hi);
-                tmem_st8(lane_addr + TM_XLO + 8 * q4, lo);
+                tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
+                tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
             }
-            mbar_arrive(&cx.bars[B_AV_EMPTY]);   // alpha and V of this chunk consumed
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&cx.bars[B_X_READY]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.bars[B_X_READY]);
 
             // U^T back from TMEM, split and staged as the A operand of U^T P^T and U^T K
             if (!(ok = grp.wait(cx, B_U_DONE, g & 1))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 uint32_t u[16], hi[8], lo[8];
-                tmem_ld16(lane_addr + TM_SKQ + 16 * q4, u);
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16 * q2, u);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint16_t h0, l0, h1, l1;
-                    split_bf16(__uint_as_float(u[2 * j]), h0, l0);
-                    split_bf16(__uint_as_float(u[2 * j + 1]), h1, l1);
-                    hi[j] = pack2(h0, h1);
-                    lo[j] = pack2(l0, l1);
-                }
-                tmem_st8(lane_addr + TM_XHI + 8 * q4, hi);
-                tmem_st8(lane_addr + TM_XLO + 8 * q4, lo);
+                for (int j = 0; j < 8; ++j)
+                    split2_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]), hi[j], lo[j]);
+                tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
+                tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&cx.bars[B_U_READY]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.bars[B_U_READY]);
 
-            // O = Gamma * (Q S^T + P U);  S <- gamma_C (S + U^T K)
+            // O = Gamma * (Q S^T + P U) into registers, then S <- gamma_C (S + U^T K)
             if (!(ok = grp.wait(cx, B_SO_DONE, g & 1))) break;
             tc_fence_after();
+            uint32_t opk[16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 uint32_t ov[16];
-                tmem_ld16(lane_addr + TM_SKQ + 64 + 16 * q4, ov);
+                tmem_ld16(lane_addr + TM_SKQ + 64 + 32 * h + 16 * q2, ov);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = 16 * q4 + j;
-                    if (t < nvalid)
-                        p.o[((tok0 + t) * p.H + it.h) * (int64_t)p.d_v + ch] =
-                            __float2bfloat16_rn(gam[t] * __uint_as_float(ov[j]));
-                }
+                for (int j = 0; j < 8; ++j)
+                    opk[8 * q2 + j] =
+                        pack_bf16x2(gam[16 * q2 + 2 * j] * __uint_as_float(ov[2 * j]),
+                                    gam[16 * q2 + 2 * j + 1] * __uint_as_float(ov[2 * j + 1]));
             }
-            const float gC = gam[C - 1];
+            {
+                float x[64];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t sv[32];
-                tmem_ld32(lane_addr + TM_S + 32 * q4, sv);
-                tmem_ld_wait();
-                float x[32];
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sv[32];
+                    tmem_ld32(lane_addr + TM_S + 64 * h + 32 * half, sv);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = gC * __uint_as_float(sv[j]);
+                    for (int j = 0; j < 32; ++j) x[32 * half + j] = gC * __uint_as_float(sv[j]);
+                }
                 if (last) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(p.S_T + srow + 32 * q4 + j) =
+                    for (int j = 0; j < 64; j += 4)
+                        *reinterpret_cast<float4*>(p.S_T + srow + j) =
                             make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
                 } else {
-                    stage_state_quarter(lane_addr, q4, x);
+                    stage_state_half(lane_addr, h, x);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
                 }
             }
-            if (!last) {
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&cx.bars[B_S_READY]);
+            // the output leaves after the state has been handed back to the MMA warp
+            __nv_bfloat16* orow = p.o + ((tok0 + 32 * h) * p.H + it.h) * (int64_t)p.d_v + ch;
+            const int64_t ostride = (int64_t)p.H * p.d_v;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = 32 * h + 2 * j;
+                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[j]);
+                if (t < nvalid) orow[(2 * j) * ostride] = pr.x;
+                if (t + 1 < nvalid) orow[(2 * j + 1) * ostride] = pr.y;
             }
         }
     }
@@ -672,8 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     if (tid == 0) {
         *cx.abort = 0;
         *cx.never = 0;
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 128, 1, 128, 128, 128,
-                                          1, 1, 128, 1, 128, 1, 128, 1};
+        // arrivals per phase: 1 for TMA / MMA commits, one per warp of a group
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 8, 1, 4, 4, 4,
+                                          1, 1, 8, 1, 8, 1, 8, 1};
         for (int b = 0; b < B_COUNT; ++b) mbar_init(&cx.bars[b], counts[b]);
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_q);
@@ -695,10 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     } else if (warp == 1) {
         if (lane == 0) run_mma(p, cx);
         __syncwarp();   // the final __syncthreads is warp-aligned
-    } else if (warp >= 4 && warp < 8) {
-        run_token_group(p, cx, tid - 128, warp - 4);
-    } else if (warp >= 8) {
-        run_row_group(p, cx, tid - 256, warp - 8);
+    } else if (warp >= 2 && warp < 6) {
+        run_token_group(p, cx, tid - 64, warp, lane);
+    } else {
+        run_row_group(p, cx, tid - 192, warp, lane);
     }
     tc_fence_before();
     __syncthreads();

@@ -267,6 +267,21 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) 
     lo = __bfloat16_as_ushort(l);
 }
 
+// Split two floats at once: hi = bf16x2(a, b), lo = bf16x2(a - hi.a, b - hi.b);
+// element a lands in the low 16 bits (the lower K index of a packed pair).
+__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint32_t pack2(uint16_t lo_elem, uint16_t hi_elem) {
     return (uint32_t)lo_elem | ((uint32_t)hi_elem << 16);
 }
