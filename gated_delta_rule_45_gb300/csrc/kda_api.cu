@@ -37,6 +37,10 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
     return a0 < b0 + bn && b0 < a0 + an;
 }
 
+}  // namespace
+
+namespace kda {
+
 kda_status prefill_impl(const void* q, const void* k, const void* v, const float* alpha,
                         const float* beta, const float* S0, const int32_t* cu_seqlens,
                         int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
@@ -95,7 +99,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-}  // namespace
+}  // namespace kda
 
 extern "C" {
 
@@ -111,9 +115,9 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
                        int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                        int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
                        void* workspace, size_t workspace_bytes, kda_stream_t stream) {
-    return prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
-                        d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, KDA_KERNEL_AUTO,
-                        stream);
+    return kda::prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
+                             d_k, d_v, dtype, chunk, o, S_T, workspace, workspace_bytes,
+                             KDA_KERNEL_AUTO, stream);
 }
 
 kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const float* alpha,
@@ -122,8 +126,9 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
                           int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
                           void* workspace, size_t workspace_bytes, kda_prefill_kernel kernel,
                           kda_stream_t stream) {
-    return prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
-                        d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, kernel, stream);
+    return kda::prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
+                             d_k, d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, kernel,
+                             stream);
 }
 
 kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d_k, int32_t d_v,

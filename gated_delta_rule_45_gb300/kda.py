@@ -53,6 +53,9 @@ def load(path: str | None = None):
     lib.kda_prefill.argtypes = prefill_args + [vp]
     lib.kda_prefill_ex.restype = ctypes.c_int
     lib.kda_prefill_ex.argtypes = prefill_args + [ctypes.c_int, vp]
+    lib.kda_prefill_noalloc.restype = ctypes.c_int
+    lib.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                        ctypes.c_int, i32, vp, vp, vp]
     lib.kda_prefill_supported.restype = ctypes.c_int
     lib.kda_prefill_supported.argtypes = [ctypes.c_int, i32, i32, i32, ctypes.c_int, i32]
     lib.kda_prefill_device_status.restype = ctypes.c_int
@@ -152,6 +155,29 @@ def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64, kernel: st
     if check_device_status:
         device_status(ws, stream=stream)
     return o, S_T
+
+
+NOALLOC_MAX_SEQS = 65536
+
+
+def prefill_noalloc_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, *, chunk: int = 64,
+                         stream=None) -> None:
+    """Enqueue kda_prefill_noalloc: like ``prefill_into`` but the scratch lives in
+    the library (for callers that cannot allocate).  Calls must not overlap on
+    the GPU; at most NOALLOC_MAX_SEQS sequences."""
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T)
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if N > NOALLOC_MAX_SEQS:
+        raise ValueError(f"kda_prefill_noalloc takes at most {NOALLOC_MAX_SEQS} sequences, "
+                         f"got {N}")
+    st = load().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                    _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v,
+                                    _dtype_code(q), chunk, _ptr(o), _ptr(S_T),
+                                    _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_prefill_noalloc")
 
 
 def device_status(workspace, stream=None) -> None:

@@ -145,6 +145,38 @@ kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d
  */
 kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream);
 
+/* Largest num_seqs that kda_prefill_noalloc accepts. */
+#define KDA_NOALLOC_MAX_SEQS 65536
+
+/*
+ * kda_prefill without a workspace argument.  The pages have no counterpart to
+ * this call; it exists for callers that cannot allocate device memory: code
+ * that runs inside a host program which owns every device allocation and
+ * gives its extensions no scratch buffer, or serving code that must not
+ * allocate once it is running, where an allocation can stall the device or
+ * break a memory plan fixed in advance.
+ *
+ * Same arguments and results as kda_prefill, minus the workspace.  The
+ * scratch it needs lives in a device array built into the library (about
+ * 256 KB on every GPU that loads it, held until the process exits).  The
+ * first call on a device looks up that array's address with the device
+ * current; make that first call before any stream capture.  The call itself
+ * allocates nothing.
+ *
+ * Every call shares the one array and leaves its contents behind; each call
+ * clears what it needs cleared, but calls that overlap on the GPU (issued on
+ * different streams with no ordering between them) race on it and must not
+ * be made.  num_seqs > KDA_NOALLOC_MAX_SEQS returns KDA_ERR_UNSUPPORTED.
+ * Device-detected input errors leave the outputs unwritten; they cannot be
+ * queried afterwards, because kda_prefill_device_status needs a workspace.
+ */
+kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v,
+                               const float* alpha, const float* beta, const float* S0,
+                               const int32_t* cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                               kda_dtype dtype, int32_t chunk, void* o, float* S_T,
+                               kda_stream_t stream);
+
 /*
  * One decode step for B sequences with one new token each, state updated in
  * place: for every (b, h), S[b][h] <- S_1 and o[b][h] <- S_1 q for the single
