@@ -14,7 +14,7 @@
 // Everything is computed value-channel-major (the M = 128 dimension of every
 // MMA is a block of 128 rows of S), so each MMA result lands with one value
 // channel per TMEM lane:
-//   SKQ  = S [K;Q]^T        M128 N128 K128   (A = S from TMEM, B = [K;Q] tile)
+//   SK   = S K^T            M128 N64  K128   (A = S from TMEM, B = K tile); then S Q^T
 //   KQK  = [K;Q] K^T        M128 N64  K128   (rows 0-63: K K^T, rows 64-127: Q K^T)
 //   U^T  = X^T T^T          M128 N64  K64    (A = X^T from TMEM, B = T)
 //   O^T += U^T P^T          M128 N64  K64    (accumulates onto the Q S^T half of SKQ)
@@ -77,8 +77,9 @@ constexpr uint32_t SM_BETA = 180224;     // 2 stages x 64 fp32
 constexpr uint32_t SM_L = 180736;        // [64][LSTR] fp32: diag(beta) strict_lower(K K^T)
 constexpr uint32_t LSTR = 68;
 constexpr uint32_t SM_TF = 198144;       // [64][LSTR] fp32: T
-constexpr uint32_t SM_Y = 215552;        // [3][16][17] fp32 scratch of the blocked inverse
-constexpr uint32_t SM_BAR = 218880;
+constexpr uint32_t SM_Y = 215552;        // [3 warps][16][YSTR] fp32 scratch of the blocked inverse
+constexpr uint32_t YSTR = 24;
+constexpr uint32_t SM_BAR = 220160;
 constexpr uint32_t SM_MISC = SM_BAR + 256;
 constexpr uint32_t SMEM_BYTES = SM_MISC + 64 + 1024;
 
@@ -97,8 +98,10 @@ enum {
     B_X_READY = 14,    // row group (8 warps)
     B_U_DONE = 15,     // MMA commit
     B_U_READY = 16,    // row group (8 warps)
-    B_SO_DONE = 17,    // MMA commit
-    B_COUNT = 18
+    B_S_DONE = 17,     // MMA commit: S += U^T K complete
+    B_O_DONE = 18,     // MMA commit: O^T += U^T P^T complete
+    B_O_READ = 19,     // row group (8 warps) -> O read out of TMEM (its columns are free)
+    B_COUNT = 20
 };
 
 struct TcParams {
@@ -291,7 +294,6 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
     int last_commit_bar = -1;
     uint32_t last_commit_parity = 0;
     const uint32_t tm = cx.tmem;
-    const uint32_t id_n128 = idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t id_n64 = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_n128_bmn = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = true;
@@ -304,22 +306,31 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
     while (cur.valid && ok) {
         const int s = g & 1;
         const uint32_t kq = kq_addr(cx, s);
-        // SKQ = S_hi [K;Q]^T + S_lo [K;Q]^T
+        // S K^T = S_hi K^T + S_lo K^T first (it feeds the next step of the chain),
+        // then S Q^T (needed only for the output)
         if (!(ok = wait1(cx, B_S_READY, g & 1))) break;
         tc_fence_after();
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const uint32_t a0 = tm + (part == 0 ? TM_SHI : TM_SLO);
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t b =
-                    smem_desc_sw128(kq + (kk >> 2) * KQ_KBLOCK + (kk & 3) * 32, 0, 1024);
-                mma_ts(tm + TM_SKQ, a0 + 8 * kk, b, id_n128, (part | kk) != 0);
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t a0 = tm + (part == 0 ? TM_SHI : TM_SLO);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t b = smem_desc_sw128(
+                        kq + (kk >> 2) * KQ_KBLOCK + (kk & 3) * 32 + half * 8192, 0, 1024);
+                    mma_ts(tm + TM_SKQ + 64 * half, a0 + 8 * kk, b, id_n64, (part | kk) != 0);
+                }
+            }
+            if (half == 0) {
+                mma_commit(&cx.bars[B_SKQ_DONE]);
+                last_commit_bar = B_SKQ_DONE;
+                last_commit_parity = g & 1;
+                // S Q^T reuses the columns the previous chunk's O was read from
+                if (g >= 1 && !(ok = wait1(cx, B_O_READ, (g - 1) & 1))) break;
             }
         }
-        mma_commit(&cx.bars[B_SKQ_DONE]);
-        last_commit_bar = B_SKQ_DONE;
-        last_commit_parity = g & 1;
+        if (!ok) break;
         // next chunk's [K;Q]K^T, so the token group can build its T and P early
         if (ahead.valid) {
             if (!(ok = issue_kqk(p, cx, g + 1))) break;
@@ -347,9 +358,16 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
         mma_commit(&cx.bars[B_U_DONE]);
         last_commit_bar = B_U_DONE;
         last_commit_parity = g & 1;
-        // O^T += U^T P^T ;  S += U^T K
+        // S += U^T K first (the chain), then O^T += U^T P^T
         if (!(ok = wait1(cx, B_U_READY, g & 1))) break;
         tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tm + TM_S, (part == 0 ? tm + TM_XHI : tm + TM_XLO) + 8 * kk,
+                       smem_desc_sw128(kq + kk * 2048, KQ_KBLOCK, 1024), id_n128_bmn, 1);
+        mma_commit(&cx.bars[B_S_DONE]);
         {
             const uint32_t p_hi = smem_u32(cx.smem + SM_P + s * TP_BUF);
             const uint32_t p_lo = p_hi + TP_LO;
@@ -361,17 +379,11 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ts(tm + TM_SKQ + 64, as[part] + 8 * kk,
                            smem_desc_sw128(bs[part] + kk * 32, 0, 1024), id_n64, 1);
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tm + TM_S, (part == 0 ? tm + TM_XHI : tm + TM_XLO) + 8 * kk,
-                           smem_desc_sw128(kq + kk * 2048, KQ_KBLOCK, 1024), id_n128_bmn, 1);
         }
-        mma_commit(&cx.bars[B_SO_DONE]);
+        mma_commit(&cx.bars[B_O_DONE]);
         mma_commit(&cx.bars[B_TP_FREE + s]);
         mma_commit(&cx.bars[B_KQ_EMPTY + s]);
-        last_commit_bar = B_SO_DONE;
+        last_commit_bar = B_O_DONE;
         last_commit_parity = g & 1;
         ++g;
         cur.next(p);
@@ -382,10 +394,45 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------ token group
+// acc (16 x 16 as two 16 x 8 tiles) += A (16 x 16) * B (16 x 16), both fp32 in
+// shared memory with row strides lda / ldb, on one warp (tf32 mma.sync).
+__device__ __forceinline__ void warp_mm16(float (&acc)[2][4], const float* A, int lda,
+                                          const float* B, int ldb, int lane) {
+    const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        uint32_t a[4];
+        a[0] = f32_to_tf32(A[g * lda + 8 * ks + tq]);
+        a[1] = f32_to_tf32(A[(g + 8) * lda + 8 * ks + tq]);
+        a[2] = f32_to_tf32(A[g * lda + 8 * ks + tq + 4]);
+        a[3] = f32_to_tf32(A[(g + 8) * lda + 8 * ks + tq + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b[2];
+            b[0] = f32_to_tf32(B[(8 * ks + tq) * ldb + 8 * nt + g]);
+            b[1] = f32_to_tf32(B[(8 * ks + tq + 4) * ldb + 8 * nt + g]);
+            mma_sync_tf32(acc[nt], a, b);
+        }
+    }
+}
+
+__device__ __forceinline__ void warp_store16(float* Y, int ldy, const float (&acc)[2][4],
+                                             float scale, int lane) {
+    const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        Y[g * ldy + 8 * nt + 2 * tq] = scale * acc[nt][0];
+        Y[g * ldy + 8 * nt + 2 * tq + 1] = scale * acc[nt][1];
+        Y[(g + 8) * ldy + 8 * nt + 2 * tq] = scale * acc[nt][2];
+        Y[(g + 8) * ldy + 8 * nt + 2 * tq + 1] = scale * acc[nt][3];
+    }
+}
+
 // Per chunk: L = diag(beta) strict_lower(K K^T) and P = tril_incl(Q K^T) from
 // the KQK accumulator, then T = (I + L)^{-1} by blocks of 16: the four
-// diagonal blocks by forward substitution, then block rows a = 1..3 as
-// T_ab = -D_a sum_{b<=k<a} L_ak T_kb, and finally T and P as bf16 hi/lo tiles.
+// diagonal blocks D_b by forward substitution, then the blocks below the
+// diagonal in order of their distance from it, T_ab = -D_a sum_{b<=k<a} L_ak T_kb,
+// and finally T and P as bf16 hi/lo tiles.
 __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int warp, int lane) {
     Group grp{t, 1, 128, 0, cx.slots};
     const int quarter = warp & 3;
@@ -454,16 +501,24 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
         if (lane == 0) mbar_arrive(&cx.bars[B_KQK_FREE]);
         named_bar_sync(1, 128);   // L complete
 
-        // diagonal blocks: (I + L_bb)^{-1} column by column; the other threads
-        // clear the six blocks above the diagonal
+        // diagonal blocks D_b = (I + L_bb)^{-1}: one thread per column, the column
+        // held in registers; the other threads clear the six blocks above the diagonal
         if (t < 64) {
-            const int b = t >> 4, cc = t & 15, c = 16 * b + cc;
+            const int b = t >> 4, cc = t & 15;
+            const float* Lb = Ls + (16 * b) * LSTR + 16 * b;
+            float col[16];
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float x = i == cc ? 1.f : 0.f;
-                for (int j = cc; j < i; ++j)
-                    x = fmaf(-Ls[(16 * b + i) * LSTR + 16 * b + j], Tf[(16 * b + j) * LSTR + c], x);
-                Tf[(16 * b + i) * LSTR + c] = x;
+                float x0 = i == cc ? 1.f : 0.f, x1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j) {
+                    if (j & 1) x1 = fmaf(-Lb[i * LSTR + j], col[j], x1);
+                    else x0 = fmaf(-Lb[i * LSTR + j], col[j], x0);
+                }
+                col[i] = x0 + x1;
             }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LSTR + 16 * b + cc] = col[i];
         } else {
             for (int e = t - 64; e < 6 * 256; e += 64) {
                 const int blk = e >> 8, w = e & 255;
@@ -473,27 +528,28 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
             }
         }
         named_bar_sync(1, 128);
-        for (int a = 1; a < 4; ++a) {
-            for (int e = t; e < a * 256; e += 128) {
-                const int b = e >> 8, i = (e >> 4) & 15, j = e & 15;
-                float y = 0.f;
-                for (int k = b; k < a; ++k) {
-                    const float* Lr = Ls + (16 * a + i) * LSTR + 16 * k;
-                    const float* Tc = Tf + (16 * k) * LSTR + 16 * b + j;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Tc[m * LSTR], y);
+        // blocks below the diagonal, by distance from it:
+        // T_ab = -D_a (sum_{b<=k<a} L_ak T_kb), 16 x 16 products on tf32 mma.sync
+        {
+            const int w = t >> 5;
+            float* Yw = Ys + w * (16 * YSTR);
+#pragma unroll 1
+            for (int dist = 1; dist < 4; ++dist) {
+                if (w < 4 - dist) {
+                    const int b = w, a = w + dist;
+                    float acc[2][4] = {};
+#pragma unroll 1
+                    for (int k = b; k < a; ++k)
+                        warp_mm16(acc, Ls + (16 * a) * LSTR + 16 * k, LSTR,
+                                  Tf + (16 * k) * LSTR + 16 * b, LSTR, lane);
+                    warp_store16(Yw, YSTR, acc, 1.f, lane);
+                    __syncwarp();
+                    float acc2[2][4] = {};
+                    warp_mm16(acc2, Tf + (16 * a) * LSTR + 16 * a, LSTR, Yw, YSTR, lane);
+                    warp_store16(Tf + (16 * a) * LSTR + 16 * b, LSTR, acc2, -1.f, lane);
                 }
-                Ys[(16 * b + i) * 17 + j] = y;
+                named_bar_sync(1, 128);
             }
-            named_bar_sync(1, 128);
-            for (int e = t; e < a * 256; e += 128) {
-                const int b = e >> 8, i = (e >> 4) & 15, j = e & 15;
-                const float* Dr = Tf + (16 * a + i) * LSTR + 16 * a;
-                float x = 0.f;
-                for (int m = 0; m <= i; ++m) x = fmaf(-Dr[m], Ys[(16 * b + m) * 17 + j], x);
-                Tf[(16 * a + i) * LSTR + 16 * b + j] = x;
-            }
-            named_bar_sync(1, 128);
         }
         // T as bf16 hi/lo, 128B-swizzled B operand: thread t writes half of row t / 2
         {
@@ -523,18 +579,17 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
 // ------------------------------------------------------------------ row group
 // Thread (r, h): value channel r of the item's block; h selects tokens
 // 32h..32h+31 for X, U and O, and key channels 64h..64h+63 for S.
-__device__ __forceinline__ void stage_state_half(uint32_t lane_addr, int h, const float* x) {
-    uint32_t raw[32], hi[32], lo[32];
+// 32 key channels (piece q of this thread's half): fp32 S and its bf16 hi/lo pairs
+__device__ __forceinline__ void stage_state_piece(uint32_t lane_addr, int h, int q,
+                                                  const float (&x)[32]) {
+    uint32_t raw[32], hi[16], lo[16];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(x[j]);
+    tmem_st32(lane_addr + TM_S + 64 * h + 32 * q, raw);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(x[32 * half + j]);
-        tmem_st32(lane_addr + TM_S + 64 * h + 32 * half, raw);
-    }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) split2_bf16(x[2 * j], x[2 * j + 1], hi[j], lo[j]);
-    tmem_st32(lane_addr + TM_SHI + 32 * h, hi);
-    tmem_st32(lane_addr + TM_SLO + 32 * h, lo);
+    for (int j = 0; j < 16; ++j) split2_bf16(x[2 * j], x[2 * j + 1], hi[j], lo[j]);
+    tmem_st16(lane_addr + TM_SHI + 32 * h + 16 * q, hi);
+    tmem_st16(lane_addr + TM_SLO + 32 * h + 16 * q, lo);
 }
 
 __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp, int lane) {
@@ -559,15 +614,16 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             }
             continue;
         }
-        {
-            float x[64];
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
+        for (int q = 0; q < 2; ++q) {
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
                 float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.S0) v4 = *reinterpret_cast<const float4*>(p.S0 + srow + j);
+                if (p.S0) v4 = *reinterpret_cast<const float4*>(p.S0 + srow + 32 * q + j);
                 x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
             }
-            stage_state_half(lane_addr, h, x);
+            stage_state_piece(lane_addr, h, q, x);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -586,18 +642,21 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             float gam[32], vg[32], gC;
             {
                 float run = 1.f;
-#pragma unroll 8
-                for (int t = 0; t < 32 * h; ++t) run *= t < nvalid ? al[t * DVB + r] : 1.f;
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    run *= t < nvalid ? al[t * DVB + r] : 1.f;
+                    if (t < 32) {
+                        if (h == 0) gam[t] = run;
+                    } else {
+                        if (h == 1) gam[t - 32] = run;
+                    }
+                }
+                gC = run;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = 32 * h + j;
-                    run *= t < nvalid ? al[t * DVB + r] : 1.f;
-                    gam[j] = run;
-                    vg[j] = t < nvalid ? bst[t] * __fdividef(bf2f(vs[t * DVB + r]), run) : 0.f;
+                    vg[j] = t < nvalid ? bst[t] * __fdividef(bf2f(vs[t * DVB + r]), gam[j]) : 0.f;
                 }
-#pragma unroll 8
-                for (int t = 32 * h + 32; t < C; ++t) run *= t < nvalid ? al[t * DVB + r] : 1.f;
-                gC = run;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&cx.bars[B_AV_EMPTY]);   // alpha, V consumed
@@ -645,8 +704,34 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             __syncwarp();
             if (lane == 0) mbar_arrive(&cx.bars[B_U_READY]);
 
-            // O = Gamma * (Q S^T + P U) into registers, then S <- gamma_C (S + U^T K)
-            if (!(ok = grp.wait(cx, B_SO_DONE, g & 1))) break;
+            // S <- gamma_C (S + U^T K), handed back to the MMA warp
+            if (!(ok = grp.wait(cx, B_S_DONE, g & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t sv[32];
+                tmem_ld32(lane_addr + TM_S + 64 * h + 32 * q, sv);
+                tmem_ld_wait();
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = gC * __uint_as_float(sv[j]);
+                if (last) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(p.S_T + srow + 32 * q + j) =
+                            make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                } else {
+                    stage_state_piece(lane_addr, h, q, x);
+                }
+            }
+            if (!last) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
+            }
+            // O = Gamma * (Q S^T + P U); leaves after the state has been handed back
+            if (!(ok = grp.wait(cx, B_O_DONE, g & 1))) break;
             tc_fence_after();
             uint32_t opk[16];
 #pragma unroll
@@ -660,30 +745,9 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                         pack_bf16x2(gam[16 * q2 + 2 * j] * __uint_as_float(ov[2 * j]),
                                     gam[16 * q2 + 2 * j + 1] * __uint_as_float(ov[2 * j + 1]));
             }
-            {
-                float x[64];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sv[32];
-                    tmem_ld32(lane_addr + TM_S + 64 * h + 32 * half, sv);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) x[32 * half + j] = gC * __uint_as_float(sv[j]);
-                }
-                if (last) {
-#pragma unroll
-                    for (int j = 0; j < 64; j += 4)
-                        *reinterpret_cast<float4*>(p.S_T + srow + j) =
-                            make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-                } else {
-                    stage_state_half(lane_addr, h, x);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
-                }
-            }
-            // the output leaves after the state has been handed back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
             __nv_bfloat16* orow = p.o + ((tok0 + 32 * h) * p.H + it.h) * (int64_t)p.d_v + ch;
             const int64_t ostride = (int64_t)p.H * p.d_v;
 #pragma unroll
@@ -717,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         *cx.never = 0;
         // arrivals per phase: 1 for TMA / MMA commits, one per warp of a group
         const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 8, 1, 4, 4, 4,
-                                          1, 1, 8, 1, 8, 1, 8, 1};
+                                          1, 1, 8, 1, 8, 1, 8, 1, 1, 8};
         for (int b = 0; b < B_COUNT; ++b) mbar_init(&cx.bars[b], counts[b]);
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_q);
