@@ -77,11 +77,12 @@ constexpr uint32_t SM_BETA = 180224;     // 2 stages x 64 fp32
 constexpr uint32_t SM_L = 180736;        // [64][LSTR] fp32: diag(beta) strict_lower(K K^T)
 constexpr uint32_t LSTR = 68;
 constexpr uint32_t SM_TF = 198144;       // [64][LSTR] fp32: T
-constexpr uint32_t SM_Y = 215552;        // [3 warps][16][YSTR] fp32 scratch of the blocked inverse
+constexpr uint32_t SM_Y = 215552;        // [4 warps][16][YSTR] fp32 scratch of the blocked inverse
 constexpr uint32_t YSTR = 24;
-constexpr uint32_t SM_BAR = 220160;
+constexpr uint32_t SM_BAR = 221696;
 constexpr uint32_t SM_MISC = SM_BAR + 256;
-constexpr uint32_t SMEM_BYTES = SM_MISC + 64 + 1024;
+constexpr uint32_t SM_HALF = SM_MISC + 64;   // [2][128] fp32: per-half products of alpha
+constexpr uint32_t SMEM_BYTES = SM_HALF + 1024 + 1024;
 
 // mbarrier indices
 enum {
@@ -430,9 +431,8 @@ __device__ __forceinline__ void warp_store16(float* Y, int ldy, const float (&ac
 
 // Per chunk: L = diag(beta) strict_lower(K K^T) and P = tril_incl(Q K^T) from
 // the KQK accumulator, then T = (I + L)^{-1} by blocks of 16: the four
-// diagonal blocks D_b by forward substitution, then the blocks below the
-// diagonal in order of their distance from it, T_ab = -D_a sum_{b<=k<a} L_ak T_kb,
-// and finally T and P as bf16 hi/lo tiles.
+// diagonal blocks D_b by forward substitution, the rest by recursive doubling
+// of the block-triangular inverse, and finally T and P as bf16 hi/lo tiles.
 __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int warp, int lane) {
     Group grp{t, 1, 128, 0, cx.slots};
     const int quarter = warp & 3;
@@ -453,21 +453,22 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
         const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + s * C;
         uint8_t* t_hi = cx.smem + SM_T + s * TP_BUF;
         uint8_t* p_hi = cx.smem + SM_P + s * TP_BUF;
+        uint32_t v[4][16];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(cx.tmem + lane_base + TM_KQK + 16 * q4, v[q4]);
+        tmem_ld_wait();
         if (kr < 64) {
             const float bt = bst[kr];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t v[16];
-                tmem_ld16(cx.tmem + lane_base + TM_KQK + 16 * q4, v);
-                tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; j += 4) {
                     const int col = 16 * q4 + j;
                     float4 l;
-                    l.x = col + 0 < kr ? bt * __uint_as_float(v[j + 0]) : 0.f;
-                    l.y = col + 1 < kr ? bt * __uint_as_float(v[j + 1]) : 0.f;
-                    l.z = col + 2 < kr ? bt * __uint_as_float(v[j + 2]) : 0.f;
-                    l.w = col + 3 < kr ? bt * __uint_as_float(v[j + 3]) : 0.f;
+                    l.x = col + 0 < kr ? bt * __uint_as_float(v[q4][j + 0]) : 0.f;
+                    l.y = col + 1 < kr ? bt * __uint_as_float(v[q4][j + 1]) : 0.f;
+                    l.z = col + 2 < kr ? bt * __uint_as_float(v[q4][j + 2]) : 0.f;
+                    l.w = col + 3 < kr ? bt * __uint_as_float(v[q4][j + 3]) : 0.f;
                     *reinterpret_cast<float4*>(Ls + kr * LSTR + col) = l;
                 }
             }
@@ -475,18 +476,15 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
             const int tq = kr - 64;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t v[16];
-                tmem_ld16(cx.tmem + lane_base + TM_KQK + 16 * q4, v);
-                tmem_ld_wait();
 #pragma unroll
                 for (int h8 = 0; h8 < 2; ++h8) {
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int col = 16 * q4 + 8 * h8 + 2 * e;
-                        const float x0 = col <= tq ? __uint_as_float(v[8 * h8 + 2 * e]) : 0.f;
+                        const float x0 = col <= tq ? __uint_as_float(v[q4][8 * h8 + 2 * e]) : 0.f;
                         const float x1 =
-                            col + 1 <= tq ? __uint_as_float(v[8 * h8 + 2 * e + 1]) : 0.f;
+                            col + 1 <= tq ? __uint_as_float(v[q4][8 * h8 + 2 * e + 1]) : 0.f;
                         split2_bf16(x0, x1, hi[e], lo[e]);
                     }
                     const uint32_t off = sw128_offset(tq, 16 * q4 + 8 * h8);
@@ -528,28 +526,41 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
             }
         }
         named_bar_sync(1, 128);
-        // blocks below the diagonal, by distance from it:
-        // T_ab = -D_a (sum_{b<=k<a} L_ak T_kb), 16 x 16 products on tf32 mma.sync
+        // blocks below the diagonal by recursive doubling, 16 x 16 products on
+        // tf32 mma.sync (T(i,j) is block (i,j) of T, N(i,j) of L):
+        //   T(1,0) = -D_1 N(1,0) D_0,   T(3,2) = -D_3 N(3,2) D_2
+        //   Y = N(2:4, 0:2) T(0:2, 0:2),  T(2:4, 0:2) = -T(2:4, 2:4) Y
         {
             const int w = t >> 5;
-            float* Yw = Ys + w * (16 * YSTR);
-#pragma unroll 1
-            for (int dist = 1; dist < 4; ++dist) {
-                if (w < 4 - dist) {
-                    const int b = w, a = w + dist;
-                    float acc[2][4] = {};
-#pragma unroll 1
-                    for (int k = b; k < a; ++k)
-                        warp_mm16(acc, Ls + (16 * a) * LSTR + 16 * k, LSTR,
-                                  Tf + (16 * k) * LSTR + 16 * b, LSTR, lane);
-                    warp_store16(Yw, YSTR, acc, 1.f, lane);
-                    __syncwarp();
-                    float acc2[2][4] = {};
-                    warp_mm16(acc2, Tf + (16 * a) * LSTR + 16 * a, LSTR, Yw, YSTR, lane);
-                    warp_store16(Tf + (16 * a) * LSTR + 16 * b, LSTR, acc2, -1.f, lane);
-                }
-                named_bar_sync(1, 128);
+            auto Tb = [&](int i, int j) { return Tf + (16 * i) * LSTR + 16 * j; };
+            auto Nb = [&](int i, int j) { return Ls + (16 * i) * LSTR + 16 * j; };
+            auto Yb = [&](int k) { return Ys + k * (16 * YSTR); };
+            if (w < 2) {
+                const int i = 1 + 2 * w, j = i - 1;
+                float acc[2][4] = {};
+                warp_mm16(acc, Nb(i, j), LSTR, Tb(j, j), LSTR, lane);
+                warp_store16(Yb(w), YSTR, acc, 1.f, lane);
+                __syncwarp();
+                float acc2[2][4] = {};
+                warp_mm16(acc2, Tb(i, i), LSTR, Yb(w), YSTR, lane);
+                warp_store16(Tb(i, j), LSTR, acc2, -1.f, lane);
             }
+            named_bar_sync(1, 128);
+            const int i = 2 + (w >> 1), j = w & 1;
+            {
+                float acc[2][4] = {};
+                warp_mm16(acc, Nb(i, j), LSTR, Tb(j, j), LSTR, lane);
+                if (j == 0) warp_mm16(acc, Nb(i, 1), LSTR, Tb(1, 0), LSTR, lane);
+                warp_store16(Yb(w), YSTR, acc, 1.f, lane);
+            }
+            named_bar_sync(1, 128);
+            {
+                float acc[2][4] = {};
+                if (i == 3) warp_mm16(acc, Tb(3, 2), LSTR, Yb(j), YSTR, lane);
+                warp_mm16(acc, Tb(i, i), LSTR, Yb(w), YSTR, lane);
+                warp_store16(Tb(i, j), LSTR, acc, -1.f, lane);
+            }
+            named_bar_sync(1, 128);
         }
         // T as bf16 hi/lo, 128B-swizzled B operand: thread t writes half of row t / 2
         {
@@ -637,25 +648,51 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             if (!(ok = grp.wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
             if (!(ok = grp.wait(cx, B_AV_FULL, g & 1))) break;
             const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
-            // Gamma over the whole chunk (padded tokens: alpha = 1); keep this
-            // thread's half, and vg = beta V / Gamma for its tokens
+            // Gamma (padded tokens: alpha = 1): each thread takes the running
+            // product over its half of the tokens, the halves swap their totals
+            // through shared memory; then vg = beta V / Gamma for its tokens
             float gam[32], vg[32], gC;
             {
+                float* half_tot = reinterpret_cast<float*>(cx.smem + SM_HALF);
+                // The tiles always hold finite values (TMA fills rows past the tensor
+                // with zeros; rows past the sequence belong to the next one), so the
+                // loads are unconditional and padded tokens are masked afterwards.
+                float a[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a[j] = al[(32 * h + j) * DVB + r];
                 float run = 1.f;
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    run *= t < nvalid ? al[t * DVB + r] : 1.f;
-                    if (t < 32) {
-                        if (h == 0) gam[t] = run;
-                    } else {
-                        if (h == 1) gam[t - 32] = run;
+                for (int j = 0; j < 32; ++j) {
+                    run *= 32 * h + j < nvalid ? a[j] : 1.f;
+                    gam[j] = run;
+                }
+                half_tot[h * DVB + r] = run;
+                named_bar_sync(2, 256);
+                const float other = half_tot[(1 - h) * DVB + r];
+                if (h == 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float2 gg = __fmul2_rn(make_float2(gam[j], gam[j + 1]),
+                                                     make_float2(other, other));
+                        gam[j] = gg.x;
+                        gam[j + 1] = gg.y;
                     }
                 }
-                gC = run;
+                gC = h == 0 ? run * other : gam[31];
+                const float4* b4 = reinterpret_cast<const float4*>(bst + 32 * h);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = 32 * h + j;
-                    vg[j] = t < nvalid ? bst[t] * __fdividef(bf2f(vs[t * DVB + r]), gam[j]) : 0.f;
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 bq = b4[j4];
+                    const int j = 4 * j4, t = 32 * h + j;
+                    float vq[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float q = __fdividef(bf2f(vs[(t + e) * DVB + r]), gam[j + e]);
+                        vq[e] = t + e < nvalid ? q : 0.f;
+                    }
+                    const float2 v01 = __fmul2_rn(make_float2(vq[0], vq[1]), make_float2(bq.x, bq.y));
+                    const float2 v23 = __fmul2_rn(make_float2(vq[2], vq[3]), make_float2(bq.z, bq.w));
+                    vg[j] = v01.x; vg[j + 1] = v01.y; vg[j + 2] = v23.x; vg[j + 3] = v23.y;
                 }
             }
             __syncwarp();
@@ -664,21 +701,33 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             // X = vg - beta (S K^T), split and staged as the A operand of U^T = X^T T^T
             if (!(ok = grp.wait(cx, B_SKQ_DONE, g & 1))) break;
             tc_fence_after();
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t sk[16], hi[8], lo[8];
-                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16 * q2, sk);
+            {
+                uint32_t sk[2][16];
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h, sk[0]);
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16, sk[1]);
                 tmem_ld_wait();
+                const float4* b4 = reinterpret_cast<const float4*>(bst + 32 * h);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int jj = 16 * q2 + 2 * j;
-                    const int t = 32 * h + jj;
-                    const float x0 = fmaf(-bst[t], __uint_as_float(sk[2 * j]), vg[jj]);
-                    const float x1 = fmaf(-bst[t + 1], __uint_as_float(sk[2 * j + 1]), vg[jj + 1]);
-                    split2_bf16(x0, x1, hi[j], lo[j]);
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int j2 = 0; j2 < 4; ++j2) {
+                        const float4 bq = b4[4 * q2 + j2];
+                        const int jj = 16 * q2 + 4 * j2;
+                        const float2 x01 = __ffma2_rn(
+                            make_float2(-bq.x, -bq.y),
+                            make_float2(__uint_as_float(sk[q2][4 * j2]), __uint_as_float(sk[q2][4 * j2 + 1])),
+                            make_float2(vg[jj], vg[jj + 1]));
+                        const float2 x23 = __ffma2_rn(
+                            make_float2(-bq.z, -bq.w),
+                            make_float2(__uint_as_float(sk[q2][4 * j2 + 2]), __uint_as_float(sk[q2][4 * j2 + 3])),
+                            make_float2(vg[jj + 2], vg[jj + 3]));
+                        split2_bf16(x01.x, x01.y, hi[2 * j2], lo[2 * j2]);
+                        split2_bf16(x23.x, x23.y, hi[2 * j2 + 1], lo[2 * j2 + 1]);
+                    }
+                    tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
+                    tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
                 }
-                tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
-                tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -688,16 +737,21 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             // U^T back from TMEM, split and staged as the A operand of U^T P^T and U^T K
             if (!(ok = grp.wait(cx, B_U_DONE, g & 1))) break;
             tc_fence_after();
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t u[16], hi[8], lo[8];
-                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16 * q2, u);
+            {
+                uint32_t u[2][16];
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h, u[0]);
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16, u[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    split2_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]), hi[j], lo[j]);
-                tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
-                tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        split2_bf16(__uint_as_float(u[q2][2 * j]), __uint_as_float(u[q2][2 * j + 1]),
+                                    hi[j], lo[j]);
+                    tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
+                    tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -714,7 +768,13 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 tmem_ld_wait();
                 float x[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = gC * __uint_as_float(sv[j]);
+                for (int j = 0; j < 32; j += 2) {
+                    const float2 xx = __fmul2_rn(
+                        make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
+                        make_float2(gC, gC));
+                    x[j] = xx.x;
+                    x[j + 1] = xx.y;
+                }
                 if (last) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
@@ -734,16 +794,17 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             if (!(ok = grp.wait(cx, B_O_DONE, g & 1))) break;
             tc_fence_after();
             uint32_t opk[16];
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t ov[16];
-                tmem_ld16(lane_addr + TM_SKQ + 64 + 32 * h + 16 * q2, ov);
+            {
+                uint32_t ov[32];
+                tmem_ld32(lane_addr + TM_SKQ + 64 + 32 * h, ov);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    opk[8 * q2 + j] =
-                        pack_bf16x2(gam[16 * q2 + 2 * j] * __uint_as_float(ov[2 * j]),
-                                    gam[16 * q2 + 2 * j + 1] * __uint_as_float(ov[2 * j + 1]));
+                for (int j = 0; j < 16; ++j) {
+                    const float2 oo = __fmul2_rn(make_float2(gam[2 * j], gam[2 * j + 1]),
+                                                 make_float2(__uint_as_float(ov[2 * j]),
+                                                             __uint_as_float(ov[2 * j + 1])));
+                    opk[j] = pack_bf16x2(oo.x, oo.y);
+                }
             }
             tc_fence_before();
             __syncwarp();

@@ -290,7 +290,9 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) 
 __device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    // (a, b) - (hi_a, hi_b) as one packed fp32x2 operation
+    const float2 d = __ffma2_rn(hf, make_float2(-1.f, -1.f), make_float2(a, b));
+    const __nv_bfloat162 l = __floats2bfloat162_rn(d.x, d.y);
     hi = *reinterpret_cast<const uint32_t*>(&h);
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
