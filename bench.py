@@ -36,10 +36,11 @@ from gated_delta_rule_45_gb300 import synth  # noqa: E402
 METRIC = "KDA prefill tokens/s & decode state-updates/s at 1 GB300; % of TC/HBM roofline"
 UNIT = "tokens/s"
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel from one ncu capture, scaled to this workload (see profiles/);
-# None until a capture of the current kernel exists.
-NCU_TRAFFIC_BYTES_PER_LAUNCH = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
+# kernel (the prefill kernel on this workload's full-size batch, 1-pass ncu
+# capture; see profiles/kda_prefill_tc_prefill_workload.md).  Must be set back
+# to None whenever that kernel changes until it is captured again.
+NCU_TRAFFIC_BYTES_PER_LAUNCH = 10.33e9
 
 
 # ---------------------------------------------------------------- distributed
@@ -454,7 +455,7 @@ def run_component(args):
         units, unit = bh, "state-updates/s"
         desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
     else:
-        spec = synth.WORKLOADS[args.workload]
+        spec = synth.WORKLOADS["varlen" if args.workload == "varlen_prefill" else args.workload]
         d = synth.prefill_inputs(spec)
         g = {key: (d[key].to(dev) if d[key] is not None else None)
              for key in ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")}
@@ -509,9 +510,11 @@ def main(argv=None):
     p.add_argument("--ref-budget", type=float, default=None,
                    help="seconds of CPU work per reference step / cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", choices=["varlen", "prefill", "long", "decode"],
+    p.add_argument("--workload",
+                   choices=["varlen", "varlen_prefill", "prefill", "long", "decode"],
                    default="varlen",
-                   help="varlen (default): the full step; others time one kernel alone")
+                   help="varlen (default): the full step; others time one kernel alone "
+                        "(varlen_prefill: the varlen batch's prefill without the decode steps)")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)
