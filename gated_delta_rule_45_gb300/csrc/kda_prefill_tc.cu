@@ -102,7 +102,8 @@ enum {
     B_S_DONE = 17,     // MMA commit: S += U^T K complete
     B_O_DONE = 18,     // MMA commit: O^T += U^T P^T complete
     B_O_READ = 19,     // row group (8 warps) -> O read out of TMEM (its columns are free)
-    B_COUNT = 20
+    B_PAIR = 20,       // [4] the two row warps of a TMEM lane quarter swap half-chunk products
+    B_COUNT = 24
 };
 
 struct TcParams {
@@ -169,7 +170,7 @@ struct Ctx {
     uint8_t* smem;
     uint64_t* bars;
     volatile int* abort;
-    volatile int* slots;   // [2 groups][2] broadcast slots
+    volatile int* slots;   // [2] broadcast slots of the token group
     volatile int* never;   // always 0: lets drain waits ignore the abort flag
     uint32_t tmem;
     int32_t* status;
@@ -182,6 +183,15 @@ __device__ __forceinline__ void fail(const Ctx& cx) {
 
 __device__ __forceinline__ bool wait1(const Ctx& cx, int b, uint32_t parity) {
     if (mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs)) return true;
+    fail(cx);
+    return false;
+}
+
+// Every lane of the calling warp waits; the warp goes on only if all lanes
+// saw the phase complete, so its control flow stays uniform.
+__device__ __forceinline__ bool warp_wait(const Ctx& cx, int b, uint32_t parity) {
+    const bool ok = mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs);
+    if (__all_sync(0xffffffffu, ok)) return true;
     fail(cx);
     return false;
 }
@@ -273,20 +283,24 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
 // ------------------------------------------------------------------ MMA issuer
 __device__ bool issue_kqk(const TcParams& p, const Ctx& cx, uint32_t g) {
     const int s = g & 1;
-    if (!wait1(cx, B_KQ_FULL + s, (g >> 1) & 1)) return false;
-    if (g >= 1 && !wait1(cx, B_KQK_FREE, (g - 1) & 1)) return false;
+    if (!warp_wait(cx, B_KQ_FULL + s, (g >> 1) & 1)) return false;
+    if (g >= 1 && !warp_wait(cx, B_KQK_FREE, (g - 1) & 1)) return false;
     tc_fence_after();
-    const uint32_t base = kq_addr(cx, s);
-    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t d = smem_desc_sw128(base + (kk >> 2) * KQ_KBLOCK + (kk & 3) * 32, 0, 1024);
-        mma_ss(cx.tmem + TM_KQK, d, d, idesc, kk > 0);   // A = 128 rows [K;Q], B = first 64 rows
+    if (elect_one()) {
+        const uint32_t base = kq_addr(cx, s);
+        // A = 128 rows [K;Q], B = its first 64 rows; one 128-byte k-block per group
+#pragma unroll 1
+        for (int kb = 0; kb < 2; ++kb)
+            mma_ss4_same(cx.tmem + TM_KQK, smem_desc_sw128(base + kb * KQ_KBLOCK, 0, 1024), 2,
+                         idesc_bf16_f32(128, 64, 0, 0), kb != 0);
+        mma_commit(&cx.bars[B_KQK_DONE]);
     }
-    mma_commit(&cx.bars[B_KQK_DONE]);
+    __syncwarp();
     return true;
 }
 
+// The whole warp runs the schedule and waits; one elected lane issues each
+// group of MMAs together with the commit that tracks it.
 __device__ void run_mma(const TcParams& p, const Ctx& cx) {
     ChunkCursor cur, ahead;
     cur.init(p);
@@ -309,26 +323,27 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
         const uint32_t kq = kq_addr(cx, s);
         // S K^T = S_hi K^T + S_lo K^T first (it feeds the next step of the chain),
         // then S Q^T (needed only for the output)
-        if (!(ok = wait1(cx, B_S_READY, g & 1))) break;
+        if (!(ok = warp_wait(cx, B_S_READY, g & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const uint32_t a0 = tm + (part == 0 ? TM_SHI : TM_SLO);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t b = smem_desc_sw128(
-                        kq + (kk >> 2) * KQ_KBLOCK + (kk & 3) * 32 + half * 8192, 0, 1024);
-                    mma_ts(tm + TM_SKQ + 64 * half, a0 + 8 * kk, b, id_n64, (part | kk) != 0);
+            if (elect_one()) {
+                // groups: (S_hi, k-block 0), (S_hi, 1), (S_lo, 0), (S_lo, 1)
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t a0 = tm + ((i >> 1) == 0 ? TM_SHI : TM_SLO) + 32 * (i & 1);
+                    const uint64_t b =
+                        smem_desc_sw128(kq + (i & 1) * KQ_KBLOCK + half * 8192, 0, 1024);
+                    mma_ts4(tm + TM_SKQ + 64 * half, a0, 8, b, 2, id_n64, i != 0);
                 }
+                if (half == 0) mma_commit(&cx.bars[B_SKQ_DONE]);
             }
+            __syncwarp();
             if (half == 0) {
-                mma_commit(&cx.bars[B_SKQ_DONE]);
                 last_commit_bar = B_SKQ_DONE;
                 last_commit_parity = g & 1;
                 // S Q^T reuses the columns the previous chunk's O was read from
-                if (g >= 1 && !(ok = wait1(cx, B_O_READ, (g - 1) & 1))) break;
+                if (g >= 1 && !(ok = warp_wait(cx, B_O_READ, (g - 1) & 1))) break;
             }
         }
         if (!ok) break;
@@ -340,50 +355,41 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
             ahead.next(p);
         }
         // U^T = X^T T^T   (hi*hi + hi*lo + lo*hi)
-        if (!(ok = wait1(cx, B_X_READY, g & 1))) break;
-        if (!(ok = wait1(cx, B_TP_READY + s, (g >> 1) & 1))) break;
+        if (!(ok = warp_wait(cx, B_X_READY, g & 1))) break;
+        if (!(ok = warp_wait(cx, B_TP_READY + s, (g >> 1) & 1))) break;
         tc_fence_after();
-        {
+        if (elect_one()) {
             const uint32_t t_hi = smem_u32(cx.smem + SM_T + s * TP_BUF);
-            const uint32_t t_lo = t_hi + TP_LO;
-            const uint32_t as[3] = {tm + TM_XHI, tm + TM_XHI, tm + TM_XLO};
-            const uint32_t bs[3] = {t_hi, t_lo, t_hi};
-#pragma unroll
+#pragma unroll 1
             for (int part = 0; part < 3; ++part)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tm + TM_SKQ, as[part] + 8 * kk,
-                           smem_desc_sw128(bs[part] + kk * 32, 0, 1024), id_n64,
-                           (part | kk) != 0);
+                mma_ts4(tm + TM_SKQ, tm + (part == 2 ? TM_XLO : TM_XHI), 8,
+                        smem_desc_sw128(t_hi + (part == 1 ? TP_LO : 0), 0, 1024), 2, id_n64,
+                        part != 0);
+            mma_commit(&cx.bars[B_U_DONE]);
         }
-        mma_commit(&cx.bars[B_U_DONE]);
+        __syncwarp();
         last_commit_bar = B_U_DONE;
         last_commit_parity = g & 1;
         // S += U^T K first (the chain), then O^T += U^T P^T
-        if (!(ok = wait1(cx, B_U_READY, g & 1))) break;
+        if (!(ok = warp_wait(cx, B_U_READY, g & 1))) break;
         tc_fence_after();
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tm + TM_S, (part == 0 ? tm + TM_XHI : tm + TM_XLO) + 8 * kk,
-                       smem_desc_sw128(kq + kk * 2048, KQ_KBLOCK, 1024), id_n128_bmn, 1);
-        mma_commit(&cx.bars[B_S_DONE]);
-        {
+        if (elect_one()) {
+            // B = the K tile read MN-major: 16 tokens (2048 bytes) per k-step
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part)
+                mma_ts4(tm + TM_S, tm + (part == 0 ? TM_XHI : TM_XLO), 8,
+                        smem_desc_sw128(kq, KQ_KBLOCK, 1024), 2048 >> 4, id_n128_bmn, 1);
+            mma_commit(&cx.bars[B_S_DONE]);
             const uint32_t p_hi = smem_u32(cx.smem + SM_P + s * TP_BUF);
-            const uint32_t p_lo = p_hi + TP_LO;
-            const uint32_t as[3] = {tm + TM_XHI, tm + TM_XHI, tm + TM_XLO};
-            const uint32_t bs[3] = {p_hi, p_lo, p_hi};
-#pragma unroll
+#pragma unroll 1
             for (int part = 0; part < 3; ++part)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tm + TM_SKQ + 64, as[part] + 8 * kk,
-                           smem_desc_sw128(bs[part] + kk * 32, 0, 1024), id_n64, 1);
+                mma_ts4(tm + TM_SKQ + 64, tm + (part == 2 ? TM_XLO : TM_XHI), 8,
+                        smem_desc_sw128(p_hi + (part == 1 ? TP_LO : 0), 0, 1024), 2, id_n64, 1);
+            mma_commit(&cx.bars[B_O_DONE]);
+            mma_commit(&cx.bars[B_TP_FREE + s]);
+            mma_commit(&cx.bars[B_KQ_EMPTY + s]);
         }
-        mma_commit(&cx.bars[B_O_DONE]);
-        mma_commit(&cx.bars[B_TP_FREE + s]);
-        mma_commit(&cx.bars[B_KQ_EMPTY + s]);
+        __syncwarp();
         last_commit_bar = B_O_DONE;
         last_commit_parity = g & 1;
         ++g;
@@ -392,6 +398,7 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
     // drain: the MMAs issued last must finish before TMEM is released
     if (last_commit_bar >= 0)
         mbar_wait(&cx.bars[last_commit_bar], last_commit_parity, cx.never, kTimeoutNs);
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ token group
@@ -604,7 +611,6 @@ __device__ __forceinline__ void stage_state_piece(uint32_t lane_addr, int h, int
 }
 
 __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp, int lane) {
-    Group grp{rt, 2, 256, 0, cx.slots + 2};
     const int quarter = warp & 3;
     const int h = rt >> 7;                 // token half / key-channel half
     const int r = 32 * quarter + lane;     // value channel within the block = TMEM lane
@@ -645,8 +651,8 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             const int64_t tok0 = it.t0 + (int64_t)c * C;
             const int nvalid = min(C, it.len - c * C);
             const bool last = c + 1 == it.nc;
-            if (!(ok = grp.wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
-            if (!(ok = grp.wait(cx, B_AV_FULL, g & 1))) break;
+            if (!(ok = warp_wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
+            if (!(ok = warp_wait(cx, B_AV_FULL, g & 1))) break;
             const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
             // Gamma (padded tokens: alpha = 1): each thread takes the running
             // product over its half of the tokens, the halves swap their totals
@@ -663,11 +669,14 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 float run = 1.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    run *= 32 * h + j < nvalid ? a[j] : 1.f;
+                    a[j] = 32 * h + j < nvalid ? a[j] : 1.f;
+                    run *= a[j];
                     gam[j] = run;
                 }
                 half_tot[h * DVB + r] = run;
-                named_bar_sync(2, 256);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cx.bars[B_PAIR + quarter]);
+                if (!(ok = warp_wait(cx, B_PAIR + quarter, g & 1))) break;
                 const float other = half_tot[(1 - h) * DVB + r];
                 if (h == 1) {
 #pragma unroll
@@ -679,6 +688,11 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                     }
                 }
                 gC = h == 0 ? run * other : gam[31];
+                // 1 / gamma_t from one reciprocal and the products of the later alphas
+                float inv[32];
+                inv[31] = __frcp_rn(gam[31]);
+#pragma unroll
+                for (int j = 30; j >= 0; --j) inv[j] = inv[j + 1] * a[j + 1];
                 const float4* b4 = reinterpret_cast<const float4*>(bst + 32 * h);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
@@ -687,7 +701,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                     float vq[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float q = __fdividef(bf2f(vs[(t + e) * DVB + r]), gam[j + e]);
+                        const float q = bf2f(vs[(t + e) * DVB + r]) * inv[j + e];
                         vq[e] = t + e < nvalid ? q : 0.f;
                     }
                     const float2 v01 = __fmul2_rn(make_float2(vq[0], vq[1]), make_float2(bq.x, bq.y));
@@ -699,7 +713,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             if (lane == 0) mbar_arrive(&cx.bars[B_AV_EMPTY]);   // alpha, V consumed
 
             // X = vg - beta (S K^T), split and staged as the A operand of U^T = X^T T^T
-            if (!(ok = grp.wait(cx, B_SKQ_DONE, g & 1))) break;
+            if (!(ok = warp_wait(cx, B_SKQ_DONE, g & 1))) break;
             tc_fence_after();
             {
                 uint32_t sk[2][16];
@@ -735,7 +749,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             if (lane == 0) mbar_arrive(&cx.bars[B_X_READY]);
 
             // U^T back from TMEM, split and staged as the A operand of U^T P^T and U^T K
-            if (!(ok = grp.wait(cx, B_U_DONE, g & 1))) break;
+            if (!(ok = warp_wait(cx, B_U_DONE, g & 1))) break;
             tc_fence_after();
             {
                 uint32_t u[2][16];
@@ -759,7 +773,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             if (lane == 0) mbar_arrive(&cx.bars[B_U_READY]);
 
             // S <- gamma_C (S + U^T K), handed back to the MMA warp
-            if (!(ok = grp.wait(cx, B_S_DONE, g & 1))) break;
+            if (!(ok = warp_wait(cx, B_S_DONE, g & 1))) break;
             tc_fence_after();
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -791,7 +805,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
             }
             // O = Gamma * (Q S^T + P U); leaves after the state has been handed back
-            if (!(ok = grp.wait(cx, B_O_DONE, g & 1))) break;
+            if (!(ok = warp_wait(cx, B_O_DONE, g & 1))) break;
             tc_fence_after();
             uint32_t opk[16];
             {
@@ -811,12 +825,14 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
             __nv_bfloat16* orow = p.o + ((tok0 + 32 * h) * p.H + it.h) * (int64_t)p.d_v + ch;
             const int64_t ostride = (int64_t)p.H * p.d_v;
+            const int lim = nvalid - 32 * h;
+            uint16_t* optr = reinterpret_cast<uint16_t*>(orow);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int t = 32 * h + 2 * j;
-                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&opk[j]);
-                if (t < nvalid) orow[(2 * j) * ostride] = pr.x;
-                if (t + 1 < nvalid) orow[(2 * j + 1) * ostride] = pr.y;
+                if (2 * j < lim) optr[0] = (uint16_t)(opk[j] & 0xffffu);
+                optr += ostride;
+                if (2 * j + 1 < lim) optr[0] = (uint16_t)(opk[j] >> 16);
+                optr += ostride;
             }
         }
     }
@@ -841,8 +857,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         *cx.abort = 0;
         *cx.never = 0;
         // arrivals per phase: 1 for TMA / MMA commits, one per warp of a group
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 8, 1, 4, 4, 4,
-                                          1, 1, 8, 1, 8, 1, 8, 1, 1, 8};
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 8, 1, 4, 4, 4, 1, 1,
+                                          8, 1, 8, 1, 8, 1, 1, 8, 2, 2, 2, 2};
         for (int b = 0; b < B_COUNT; ++b) mbar_init(&cx.bars[b], counts[b]);
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_q);
@@ -862,8 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     if (warp == 0) {
         run_producer(p, cx, lane);
     } else if (warp == 1) {
-        if (lane == 0) run_mma(p, cx);
-        __syncwarp();   // the final __syncthreads is warp-aligned
+        run_mma(p, cx);
     } else if (warp >= 2 && warp < 6) {
         run_token_group(p, cx, tid - 64, warp, lane);
     } else {

@@ -67,9 +67,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  Gives up after
 // `timeout_ns` of wall time, or as soon as *abort becomes non-zero, and then
 // returns false; the caller must stop issuing work.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                           const volatile int* abort, uint64_t timeout_ns) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -78,6 +77,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
             if (global_timer_ns() - t0 > timeout_ns) return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, timeout_ns);
 }
 
 // ---------------------------------------------------------------- fences
@@ -223,6 +227,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // ---------------------------------------------------------------- MMA
+// True on one lane of the (converged) calling warp; the MMAs and the commit
+// that tracks them are issued by that lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "elect.sync _|p, 0xffffffff;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T   (one elected thread issues)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -247,6 +265,24 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Four MMAs along K.  A advances by `a_step` TMEM columns (TS) or B's step
+// (SS, A and B sharing one descriptor walk); B's descriptor advances by
+// `b_step` 16-byte units.  Only the first may start a fresh accumulator.
+// Groups of four keep the issuing loops short without slowing issue.
+__device__ __forceinline__ void mma_ts4(uint32_t d_tmem, uint32_t a_tmem, uint32_t a_step,
+                                        uint64_t b_desc, uint32_t b_step, uint32_t idesc,
+                                        uint32_t acc_first) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        mma_ts(d_tmem, a_tmem + j * a_step, b_desc + j * b_step, idesc, j == 0 ? acc_first : 1u);
+}
+__device__ __forceinline__ void mma_ss4_same(uint32_t d_tmem, uint64_t desc, uint32_t step,
+                                             uint32_t idesc, uint32_t acc_first) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        mma_ss(d_tmem, desc + j * step, desc + j * step, idesc, j == 0 ? acc_first : 1u);
 }
 
 // Round fp32 to tf32 (nearest, ties away), as the operand of a tf32 mma.sync.
