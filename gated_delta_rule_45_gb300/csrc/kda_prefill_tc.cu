@@ -68,28 +68,29 @@ constexpr uint32_t SM_KQ = 0;            // 2 stages: [k-block 2][128 rows: 64 K
 constexpr uint32_t KQ_STAGE = 32768;
 constexpr uint32_t KQ_KBLOCK = 16384;
 constexpr uint32_t SM_ALPHA = 65536;     // [64 tokens][128 channels] fp32
-constexpr uint32_t SM_V = 98304;         // [64][128] bf16
+constexpr uint32_t SM_V = 98304;         // [64][128] bf16, V buffer 0 (buffer 1 at SM_V1)
 constexpr uint32_t SM_T = 114688;        // 2 buffers x (hi, lo) x [64][64] bf16, swizzled
 constexpr uint32_t SM_P = 147456;        // same for P
 constexpr uint32_t TP_BUF = 16384;
 constexpr uint32_t TP_LO = 8192;
 constexpr uint32_t SM_BETA = 180224;     // 2 stages x 64 fp32
-constexpr uint32_t SM_L = 180736;        // [64][LSTR] fp32: diag(beta) strict_lower(K K^T)
+constexpr uint32_t SM_L = 180736;        // [64][LSTR] fp32: diag(beta) strict_lower(K K^T), then T in place
 constexpr uint32_t LSTR = 68;
-constexpr uint32_t SM_TF = 198144;       // [64][LSTR] fp32: T
-constexpr uint32_t SM_Y = 215552;        // [4 warps][16][YSTR] fp32 scratch of the blocked inverse
+constexpr uint32_t SM_V1 = 198144;       // V buffer 1
+constexpr uint32_t SM_Y = 214528;        // [4 warps][16][YSTR] fp32 scratch of the blocked inverse
 constexpr uint32_t YSTR = 24;
-constexpr uint32_t SM_BAR = 221696;
+constexpr uint32_t SM_BAR = 220672;
 constexpr uint32_t SM_MISC = SM_BAR + 256;
 constexpr uint32_t SM_HALF = SM_MISC + 64;   // [2][128] fp32: per-half products of alpha
-constexpr uint32_t SMEM_BYTES = SM_HALF + 1024 + 1024;
+constexpr uint32_t SM_OST = SM_HALF + 1024;   // [8 row warps][16 tokens][32 channels] bf16
+constexpr uint32_t SMEM_BYTES = SM_OST + 8 * 1024 + 1024;
 
 // mbarrier indices
 enum {
     B_KQ_FULL = 0,     // [2] producer -> K/Q/beta stage loaded
     B_KQ_EMPTY = 2,    // [2] MMA commit -> stage free
-    B_AV_FULL = 4,     // producer -> alpha/V loaded
-    B_AV_EMPTY = 5,    // row group (8 warps) -> alpha/V consumed
+    B_A_FULL = 4,      // producer -> alpha loaded
+    B_A_EMPTY = 5,     // row group (8 warps) -> alpha read
     B_KQK_DONE = 6,    // MMA commit -> [K;Q]K^T ready
     B_KQK_FREE = 7,    // token group (4 warps) -> KQK read
     B_TP_READY = 8,    // [2] token group (4 warps) -> T, P written
@@ -103,7 +104,9 @@ enum {
     B_O_DONE = 18,     // MMA commit: O^T += U^T P^T complete
     B_O_READ = 19,     // row group (8 warps) -> O read out of TMEM (its columns are free)
     B_PAIR = 20,       // [4] the two row warps of a TMEM lane quarter swap half-chunk products
-    B_COUNT = 24
+    B_V_FULL = 24,     // [2] producer -> V buffer loaded
+    B_V_EMPTY = 26,    // [2] row group (8 warps) -> V buffer read
+    B_COUNT = 28
 };
 
 struct TcParams {
@@ -228,7 +231,7 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
     ChunkCursor cur;
     cur.init(p);
     uint32_t g = 0;
-    uint32_t kq_issued[2] = {0, 0}, av_issued = 0;
+    uint32_t kq_issued[2] = {0, 0}, a_issued = 0, v_issued[2] = {0, 0};
     const float* beta_st = reinterpret_cast<const float*>(cx.smem + SM_BETA);
     while (cur.valid) {
         const int s = g & 1;
@@ -255,19 +258,33 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
             tma_load_3d(st + KQ_KBLOCK + 8192, &p.tm_q, bar, 64, h, (int32_t)tok0);
         }
         ++kq_issued[s];
+        // alpha: one buffer, free once the row group has read it into registers
         if (g >= 1) {
             int r = 1;
-            if (lane == 0) r = wait1(cx, B_AV_EMPTY, (g - 1) & 1);
+            if (lane == 0) r = wait1(cx, B_A_EMPTY, (g - 1) & 1);
             __syncwarp();
             if (!__shfl_sync(0xffffffffu, r, 0)) break;
         }
         if (lane == 0) {
-            uint64_t* bar = &cx.bars[B_AV_FULL];
-            mbar_arrive_expect_tx(bar, 64 * DVB * 4 + 64 * DVB * 2);
+            uint64_t* bar = &cx.bars[B_A_FULL];
+            mbar_arrive_expect_tx(bar, 64 * DVB * 4);
             tma_load_3d(cx.smem + SM_ALPHA, &p.tm_a, bar, cur.info.vb * DVB, h, (int32_t)tok0);
-            tma_load_3d(cx.smem + SM_V, &p.tm_v, bar, cur.info.vb * DVB, h, (int32_t)tok0);
         }
-        ++av_issued;
+        ++a_issued;
+        // V: two buffers
+        if (g >= 2) {
+            int r = 1;
+            if (lane == 0) r = wait1(cx, B_V_EMPTY + s, ((g >> 1) + 1) & 1);
+            __syncwarp();
+            if (!__shfl_sync(0xffffffffu, r, 0)) break;
+        }
+        if (lane == 0) {
+            uint64_t* bar = &cx.bars[B_V_FULL + s];
+            mbar_arrive_expect_tx(bar, 64 * DVB * 2);
+            tma_load_3d(cx.smem + (s ? SM_V1 : SM_V), &p.tm_v, bar, cur.info.vb * DVB, h,
+                        (int32_t)tok0);
+        }
+        ++v_issued[s];
         ++g;
         cur.next(p);
     }
@@ -275,7 +292,9 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
     if (lane == 0) {
         for (int s = 0; s < 2; ++s)
             if (kq_issued[s]) mbar_wait(&cx.bars[B_KQ_FULL + s], (kq_issued[s] - 1) & 1, cx.never, kTimeoutNs);
-        if (av_issued) mbar_wait(&cx.bars[B_AV_FULL], (av_issued - 1) & 1, cx.never, kTimeoutNs);
+        if (a_issued) mbar_wait(&cx.bars[B_A_FULL], (a_issued - 1) & 1, cx.never, kTimeoutNs);
+        for (int s = 0; s < 2; ++s)
+            if (v_issued[s]) mbar_wait(&cx.bars[B_V_FULL + s], (v_issued[s] - 1) & 1, cx.never, kTimeoutNs);
     }
     __syncwarp();
 }
@@ -446,7 +465,6 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
     const int kr = 32 * quarter + lane;   // accumulator row: 0-63 K K^T, 64-127 Q K^T
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     float* Ls = reinterpret_cast<float*>(cx.smem + SM_L);
-    float* Tf = reinterpret_cast<float*>(cx.smem + SM_TF);
     float* Ys = reinterpret_cast<float*>(cx.smem + SM_Y);
     ChunkCursor cur;
     cur.init(p);
@@ -460,44 +478,39 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
         const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + s * C;
         uint8_t* t_hi = cx.smem + SM_T + s * TP_BUF;
         uint8_t* p_hi = cx.smem + SM_P + s * TP_BUF;
-        uint32_t v[4][16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(cx.tmem + lane_base + TM_KQK + 16 * q4, v[q4]);
-        tmem_ld_wait();
-        if (kr < 64) {
-            const float bt = bst[kr];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+        const bool krow = kr < 64;           // warp-uniform
+        const float bt = krow ? bst[kr] : 0.f;
+        const int tq = kr - 64;
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t v[16];
+            tmem_ld16(cx.tmem + lane_base + TM_KQK + 16 * q4, v);
+            tmem_ld_wait();
+            if (krow) {
 #pragma unroll
                 for (int j = 0; j < 16; j += 4) {
                     const int col = 16 * q4 + j;
                     float4 l;
-                    l.x = col + 0 < kr ? bt * __uint_as_float(v[q4][j + 0]) : 0.f;
-                    l.y = col + 1 < kr ? bt * __uint_as_float(v[q4][j + 1]) : 0.f;
-                    l.z = col + 2 < kr ? bt * __uint_as_float(v[q4][j + 2]) : 0.f;
-                    l.w = col + 3 < kr ? bt * __uint_as_float(v[q4][j + 3]) : 0.f;
+                    l.x = col + 0 < kr ? bt * __uint_as_float(v[j + 0]) : 0.f;
+                    l.y = col + 1 < kr ? bt * __uint_as_float(v[j + 1]) : 0.f;
+                    l.z = col + 2 < kr ? bt * __uint_as_float(v[j + 2]) : 0.f;
+                    l.w = col + 3 < kr ? bt * __uint_as_float(v[j + 3]) : 0.f;
                     *reinterpret_cast<float4*>(Ls + kr * LSTR + col) = l;
                 }
-            }
-        } else {
-            const int tq = kr - 64;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            } else {
 #pragma unroll
                 for (int h8 = 0; h8 < 2; ++h8) {
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int col = 16 * q4 + 8 * h8 + 2 * e;
-                        const float x0 = col <= tq ? __uint_as_float(v[q4][8 * h8 + 2 * e]) : 0.f;
-                        const float x1 =
-                            col + 1 <= tq ? __uint_as_float(v[q4][8 * h8 + 2 * e + 1]) : 0.f;
+                        const float x0 = col <= tq ? __uint_as_float(v[8 * h8 + 2 * e]) : 0.f;
+                        const float x1 = col + 1 <= tq ? __uint_as_float(v[8 * h8 + 2 * e + 1]) : 0.f;
                         split2_bf16(x0, x1, hi[e], lo[e]);
                     }
                     const uint32_t off = sw128_offset(tq, 16 * q4 + 8 * h8);
                     *reinterpret_cast<uint4*>(p_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(p_hi + TP_LO + off) =
-                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(p_hi + TP_LO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
         }
@@ -506,66 +519,67 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
         if (lane == 0) mbar_arrive(&cx.bars[B_KQK_FREE]);
         named_bar_sync(1, 128);   // L complete
 
-        // diagonal blocks D_b = (I + L_bb)^{-1}: one thread per column, the column
-        // held in registers; the other threads clear the six blocks above the diagonal
-        if (t < 64) {
-            const int b = t >> 4, cc = t & 15;
-            const float* Lb = Ls + (16 * b) * LSTR + 16 * b;
+        // T is built in place over L: the blocks of L above the diagonal are
+        // already zero, and each block below it is read for the last time before
+        // its block of T is written.
+        // Diagonal blocks D_b = (I + L_bb)^{-1}: one thread per column, the column
+        // held in registers until every column of the block is solved.
+        {
+            const int b = (t >> 4) & 3, cc = t & 15;
             float col[16];
+            if (t < 64) {
+                const float* Lb = Ls + (16 * b) * LSTR + 16 * b;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float x0 = i == cc ? 1.f : 0.f, x1 = 0.f;
+                for (int i = 0; i < 16; ++i) {
+                    float x0 = i == cc ? 1.f : 0.f, x1 = 0.f;
 #pragma unroll
-                for (int j = 0; j < i; ++j) {
-                    if (j & 1) x1 = fmaf(-Lb[i * LSTR + j], col[j], x1);
-                    else x0 = fmaf(-Lb[i * LSTR + j], col[j], x0);
+                    for (int j = 0; j < i; ++j) {
+                        if (j & 1) x1 = fmaf(-Lb[i * LSTR + j], col[j], x1);
+                        else x0 = fmaf(-Lb[i * LSTR + j], col[j], x0);
+                    }
+                    col[i] = x0 + x1;
                 }
-                col[i] = x0 + x1;
             }
+            named_bar_sync(1, 128);
+            if (t < 64) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Tf[(16 * b + i) * LSTR + 16 * b + cc] = col[i];
-        } else {
-            for (int e = t - 64; e < 6 * 256; e += 64) {
-                const int blk = e >> 8, w = e & 255;
-                const int ba = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                const int bb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                Tf[(16 * ba + (w >> 4)) * LSTR + 16 * bb + (w & 15)] = 0.f;
+                for (int i = 0; i < 16; ++i) Ls[(16 * b + i) * LSTR + 16 * b + cc] = col[i];
             }
+            named_bar_sync(1, 128);
         }
-        named_bar_sync(1, 128);
         // blocks below the diagonal by recursive doubling, 16 x 16 products on
-        // tf32 mma.sync (T(i,j) is block (i,j) of T, N(i,j) of L):
+        // tf32 mma.sync (T(i,j) is block (i,j) of T, N(i,j) the same block of L
+        // before it is overwritten):
         //   T(1,0) = -D_1 N(1,0) D_0,   T(3,2) = -D_3 N(3,2) D_2
         //   Y = N(2:4, 0:2) T(0:2, 0:2),  T(2:4, 0:2) = -T(2:4, 2:4) Y
         {
             const int w = t >> 5;
-            auto Tb = [&](int i, int j) { return Tf + (16 * i) * LSTR + 16 * j; };
-            auto Nb = [&](int i, int j) { return Ls + (16 * i) * LSTR + 16 * j; };
+            auto Bk = [&](int i, int j) { return Ls + (16 * i) * LSTR + 16 * j; };
             auto Yb = [&](int k) { return Ys + k * (16 * YSTR); };
             if (w < 2) {
                 const int i = 1 + 2 * w, j = i - 1;
                 float acc[2][4] = {};
-                warp_mm16(acc, Nb(i, j), LSTR, Tb(j, j), LSTR, lane);
+                warp_mm16(acc, Bk(i, j), LSTR, Bk(j, j), LSTR, lane);
                 warp_store16(Yb(w), YSTR, acc, 1.f, lane);
                 __syncwarp();
                 float acc2[2][4] = {};
-                warp_mm16(acc2, Tb(i, i), LSTR, Yb(w), YSTR, lane);
-                warp_store16(Tb(i, j), LSTR, acc2, -1.f, lane);
+                warp_mm16(acc2, Bk(i, i), LSTR, Yb(w), YSTR, lane);
+                warp_store16(Bk(i, j), LSTR, acc2, -1.f, lane);
             }
             named_bar_sync(1, 128);
             const int i = 2 + (w >> 1), j = w & 1;
             {
                 float acc[2][4] = {};
-                warp_mm16(acc, Nb(i, j), LSTR, Tb(j, j), LSTR, lane);
-                if (j == 0) warp_mm16(acc, Nb(i, 1), LSTR, Tb(1, 0), LSTR, lane);
+                warp_mm16(acc, Bk(i, j), LSTR, Bk(j, j), LSTR, lane);
+                if (j == 0) warp_mm16(acc, Bk(i, 1), LSTR, Bk(1, 0), LSTR, lane);
                 warp_store16(Yb(w), YSTR, acc, 1.f, lane);
             }
             named_bar_sync(1, 128);
             {
                 float acc[2][4] = {};
-                if (i == 3) warp_mm16(acc, Tb(3, 2), LSTR, Yb(j), YSTR, lane);
-                warp_mm16(acc, Tb(i, i), LSTR, Yb(w), YSTR, lane);
-                warp_store16(Tb(i, j), LSTR, acc, -1.f, lane);
+                if (i == 3) warp_mm16(acc, Bk(3, 2), LSTR, Yb(j), YSTR, lane);
+                warp_mm16(acc, Bk(i, i), LSTR, Yb(w), YSTR, lane);
+                warp_store16(Bk(i, j), LSTR, acc, -1.f, lane);
             }
             named_bar_sync(1, 128);
         }
@@ -574,8 +588,8 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
             const int i = t >> 1, c0 = (t & 1) * 32;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
-                const float4 x0 = *reinterpret_cast<const float4*>(Tf + i * LSTR + c0 + 8 * ch);
-                const float4 x1 = *reinterpret_cast<const float4*>(Tf + i * LSTR + c0 + 8 * ch + 4);
+                const float4 x0 = *reinterpret_cast<const float4*>(Ls + i * LSTR + c0 + 8 * ch);
+                const float4 x1 = *reinterpret_cast<const float4*>(Ls + i * LSTR + c0 + 8 * ch + 4);
                 uint32_t hi[4], lo[4];
                 split2_bf16(x0.x, x0.y, hi[0], lo[0]);
                 split2_bf16(x0.z, x0.w, hi[1], lo[1]);
@@ -618,7 +632,6 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
     uint32_t g = 0;
     bool ok = true;
     const float* al = reinterpret_cast<const float*>(cx.smem + SM_ALPHA);
-    const uint16_t* vs = reinterpret_cast<const uint16_t*>(cx.smem + SM_V);
     for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
         const ItemInfo it = item_info(p, item);
         const int ch = it.vb * DVB + r;   // value channel
@@ -631,7 +644,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             }
             continue;
         }
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 2; ++q) {
             float x[32];
 #pragma unroll
@@ -652,7 +665,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             const int nvalid = min(C, it.len - c * C);
             const bool last = c + 1 == it.nc;
             if (!(ok = warp_wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
-            if (!(ok = warp_wait(cx, B_AV_FULL, g & 1))) break;
+            if (!(ok = warp_wait(cx, B_A_FULL, g & 1))) break;
             const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
             // Gamma (padded tokens: alpha = 1): each thread takes the running
             // product over its half of the tokens, the halves swap their totals
@@ -666,6 +679,8 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 float a[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) a[j] = al[(32 * h + j) * DVB + r];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cx.bars[B_A_EMPTY]);   // alpha is in registers
                 float run = 1.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -693,6 +708,9 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 inv[31] = __frcp_rn(gam[31]);
 #pragma unroll
                 for (int j = 30; j >= 0; --j) inv[j] = inv[j + 1] * a[j + 1];
+                if (!(ok = warp_wait(cx, B_V_FULL + (g & 1), (g >> 1) & 1))) break;
+                const uint16_t* vs =
+                    reinterpret_cast<const uint16_t*>(cx.smem + ((g & 1) ? SM_V1 : SM_V));
                 const float4* b4 = reinterpret_cast<const float4*>(bst + 32 * h);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
@@ -710,7 +728,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&cx.bars[B_AV_EMPTY]);   // alpha, V consumed
+            if (lane == 0) mbar_arrive(&cx.bars[B_V_EMPTY + (g & 1)]);   // V consumed
 
             // X = vg - beta (S K^T), split and staged as the A operand of U^T = X^T T^T
             if (!(ok = warp_wait(cx, B_SKQ_DONE, g & 1))) break;
@@ -775,7 +793,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             // S <- gamma_C (S + U^T K), handed back to the MMA warp
             if (!(ok = warp_wait(cx, B_S_DONE, g & 1))) break;
             tc_fence_after();
-#pragma unroll
+#pragma unroll 1
             for (int q = 0; q < 2; ++q) {
                 uint32_t sv[32];
                 tmem_ld32(lane_addr + TM_S + 64 * h + 32 * q, sv);
@@ -823,16 +841,30 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
-            __nv_bfloat16* orow = p.o + ((tok0 + 32 * h) * p.H + it.h) * (int64_t)p.d_v + ch;
+            // Out through a transpose in this warp's shared-memory slot: its 32
+            // channels x 16 tokens at a time leave as 16-byte pieces of token rows.
+            uint16_t* ost = reinterpret_cast<uint16_t*>(cx.smem + SM_OST + (warp - 6) * 1024);
             const int64_t ostride = (int64_t)p.H * p.d_v;
-            const int lim = nvalid - 32 * h;
-            uint16_t* optr = reinterpret_cast<uint16_t*>(orow);
+            __nv_bfloat16* obase = p.o + (tok0 + 32 * h) * ostride + (int64_t)it.h * p.d_v +
+                                   it.vb * DVB + 32 * quarter;
+            const int lim = nvalid - 32 * h;   // tokens of this half inside the sequence
+            const int prow = lane >> 2, pcol = (lane & 3) * 8;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (2 * j < lim) optr[0] = (uint16_t)(opk[j] & 0xffffu);
-                optr += ostride;
-                if (2 * j + 1 < lim) optr[0] = (uint16_t)(opk[j] >> 16);
-                optr += ostride;
+            for (int k = 0; k < 2; ++k) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    ost[(2 * j) * 32 + lane] = (uint16_t)(opk[8 * k + j] & 0xffffu);
+                    ost[(2 * j + 1) * 32 + lane] = (uint16_t)(opk[8 * k + j] >> 16);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int row = prow + 8 * e;
+                    const uint4 v = *reinterpret_cast<const uint4*>(ost + row * 32 + pcol);
+                    if (16 * k + row < lim)
+                        *reinterpret_cast<uint4*>(obase + (int64_t)(16 * k + row) * ostride + pcol) = v;
+                }
+                __syncwarp();
             }
         }
     }
@@ -857,8 +889,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         *cx.abort = 0;
         *cx.never = 0;
         // arrivals per phase: 1 for TMA / MMA commits, one per warp of a group
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 8, 1, 4, 4, 4, 1, 1,
-                                          8, 1, 8, 1, 8, 1, 1, 8, 2, 2, 2, 2};
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 8, 1, 4, 4, 4, 1, 1, 8, 1,
+                                          8, 1, 8, 1, 1, 8, 2, 2, 2, 2, 1, 1, 8, 8};
         for (int b = 0; b < B_COUNT; ++b) mbar_init(&cx.bars[b], counts[b]);
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_q);
@@ -922,8 +954,9 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t e
 }  // namespace
 
 bool prefill_tc_supports(const PrefillArgs& a) {
+    // o is written in 16-byte pieces
     return a.dtype == KDA_BF16 && a.d_k == DK && a.d_v % DVB == 0 && a.d_v <= 1024 &&
-           a.chunk == C;
+           a.chunk == C && (reinterpret_cast<uintptr_t>(a.o) & 15u) == 0;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
