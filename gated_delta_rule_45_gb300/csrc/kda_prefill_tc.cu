@@ -318,6 +318,13 @@ __device__ bool issue_kqk(const TcParams& p, const Ctx& cx, uint32_t g) {
     return true;
 }
 
+// True when [K;Q]K^T of chunk g could be issued without waiting (warp-uniform).
+__device__ __forceinline__ bool kqk_ready(const Ctx& cx, uint32_t g) {
+    bool r = mbar_test_wait(&cx.bars[B_KQ_FULL + (g & 1)], (g >> 1) & 1);
+    if (g >= 1) r = r && mbar_test_wait(&cx.bars[B_KQK_FREE], (g - 1) & 1);
+    return __all_sync(0xffffffffu, r);
+}
+
 // The whole warp runs the schedule and waits; one elected lane issues each
 // group of MMAs together with the commit that tracks it.
 __device__ void run_mma(const TcParams& p, const Ctx& cx) {
@@ -366,12 +373,16 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
             }
         }
         if (!ok) break;
-        // next chunk's [K;Q]K^T, so the token group can build its T and P early
-        if (ahead.valid) {
+        // next chunk's [K;Q]K^T, so the token group can build its T and P early;
+        // issued here only if its tiles are in, else after the U or the S MMAs,
+        // so that it never holds up this chunk's chain
+        bool kqk_due = ahead.valid;
+        if (kqk_due && kqk_ready(cx, g + 1)) {
             if (!(ok = issue_kqk(p, cx, g + 1))) break;
             last_commit_bar = B_KQK_DONE;
             last_commit_parity = (g + 1) & 1;
             ahead.next(p);
+            kqk_due = false;
         }
         // U^T = X^T T^T   (hi*hi + hi*lo + lo*hi)
         if (!(ok = warp_wait(cx, B_X_READY, g & 1))) break;
@@ -389,6 +400,13 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
         __syncwarp();
         last_commit_bar = B_U_DONE;
         last_commit_parity = g & 1;
+        if (kqk_due && kqk_ready(cx, g + 1)) {
+            if (!(ok = issue_kqk(p, cx, g + 1))) break;
+            last_commit_bar = B_KQK_DONE;
+            last_commit_parity = (g + 1) & 1;
+            ahead.next(p);
+            kqk_due = false;
+        }
         // S += U^T K first (the chain), then O^T += U^T P^T
         if (!(ok = warp_wait(cx, B_U_READY, g & 1))) break;
         tc_fence_after();
@@ -399,6 +417,7 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
                 mma_ts4(tm + TM_S, tm + (part == 0 ? TM_XHI : TM_XLO), 8,
                         smem_desc_sw128(kq, KQ_KBLOCK, 1024), 2048 >> 4, id_n128_bmn, 1);
             mma_commit(&cx.bars[B_S_DONE]);
+            mma_commit(&cx.bars[B_KQ_EMPTY + s]);   // the O MMAs do not read K or Q
             const uint32_t p_hi = smem_u32(cx.smem + SM_P + s * TP_BUF);
 #pragma unroll 1
             for (int part = 0; part < 3; ++part)
@@ -406,11 +425,16 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
                         smem_desc_sw128(p_hi + (part == 1 ? TP_LO : 0), 0, 1024), 2, id_n64, 1);
             mma_commit(&cx.bars[B_O_DONE]);
             mma_commit(&cx.bars[B_TP_FREE + s]);
-            mma_commit(&cx.bars[B_KQ_EMPTY + s]);
         }
         __syncwarp();
         last_commit_bar = B_O_DONE;
         last_commit_parity = g & 1;
+        if (kqk_due) {
+            if (!(ok = issue_kqk(p, cx, g + 1))) break;
+            last_commit_bar = B_KQK_DONE;
+            last_commit_parity = (g + 1) & 1;
+            ahead.next(p);
+        }
         ++g;
         cur.next(p);
     }
