@@ -71,7 +71,12 @@ VARLEN = PrefillSpec(num_seqs=64, len_lo=128, len_hi=8192, H=16, d_k=128, d_v=25
                      chunk=64, alpha_mu=3.0, s0_std=0.1)
 VARLEN_DECODE_STEPS = 32
 
-WORKLOADS = {"tiny": TINY, "decode": DECODE, "prefill": PREFILL, "long": LONG, "varlen": VARLEN}
+# Contraction-phase case: 152 independent (sequence, head) chains of 6 chunks,
+# ~110 MB of inputs and states, so that back-to-back launches are served from L2.
+L2_RESIDENT = PrefillSpec(num_seqs=152, len_lo=384, len_hi=384, H=1, d_k=128, d_v=128,
+                          chunk=64, s0_std=0.1)
+WORKLOADS = {"tiny": TINY, "decode": DECODE, "prefill": PREFILL, "long": LONG, "varlen": VARLEN,
+             "l2_resident": L2_RESIDENT}
 
 
 def _normal(gen: torch.Generator, shape, mean: float = 0.0, std: float = 1.0) -> torch.Tensor:

@@ -1,4 +1,4 @@
-"""The four GPU workloads at full size, in the launch configuration the bench
+"""The GPU workloads at full size, in the launch configuration the bench
 times (kernel choice "auto"), checked against the oracle on sampled
 (sequence, head) pairs, each over its whole sequence."""
 import numpy as np
@@ -95,3 +95,16 @@ def test_varlen_workload_with_decode_continuation():
         worst_o = max(worst_o, parity.rel_gate(np.stack(o_gpus), np.stack(o_refs), torch.bfloat16))
         worst_s = max(worst_s, parity.rel(S_gpu[n, h], s_ref))
     assert worst_o <= parity.TOL_BF16 and worst_s <= parity.TOL_BF16, (worst_o, worst_s)
+
+
+def test_l2_resident_contraction_case():
+    """The bench's L2-resident case (152 chains of 384 tokens, H = 1): every chain
+    against the oracle."""
+    spec = synth.L2_RESIDENT
+    d = synth.prefill_inputs(spec)
+    dev = parity.to_device(d)
+    o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], chunk=spec.chunk, check_device_status=True)
+    ref = parity.oracle_pairs(d, [(n, 0) for n in range(spec.num_seqs)])
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
