@@ -391,16 +391,35 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+E2E_GROUPS = 8          # sequence groups streamed through the GPU per end-to-end step
+
+
 def run_e2e(args, kda, d, steps, spec, dev, stream):
     """Same step through the public API with pinned host buffers; H2D of inputs and
-    D2H of outputs inside the timed region."""
-    keys = ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")
-    host = {key: d[key].pin_memory() for key in keys}
-    host_dec = [{key: st[key].pin_memory() for key in ("q", "k", "v", "alpha", "beta")}
-                for st in steps]
-    T = int(d["cu_seqlens"][-1])
+    D2H of outputs inside the timed region.
+
+    The batch is cut into E2E_GROUPS groups of consecutive sequences (about equal
+    token counts).  Group g's inputs go up on two alternating copy streams while
+    group g-1 is prefilled on the compute stream and group g-2's outputs come
+    down on a third stream; the 32 decode steps run on the whole batch once every
+    group is prefilled, then the state and the decode outputs come down."""
+    keys = ("q", "k", "v", "alpha", "beta")
+    host = {key: d[key].pin_memory() for key in keys + ("S0",)}
+    host_dec = [{key: st[key].pin_memory() for key in keys} for st in steps]
+    cu_host = d["cu_seqlens"].to(torch.int64)
+    T = int(cu_host[-1])
     N, H, d_k, d_v = spec.num_seqs, spec.H, spec.d_k, spec.d_v
-    g = {key: torch.empty_like(host[key], device=dev) for key in keys}
+    # groups of consecutive sequences with about equal token counts
+    bounds = [0]
+    for gi in range(1, E2E_GROUPS):
+        n = int(torch.searchsorted(cu_host, T * gi // E2E_GROUPS))
+        bounds.append(min(max(n, bounds[-1] + 1), N - (E2E_GROUPS - gi)))
+    bounds.append(N)
+    groups = [(bounds[i], bounds[i + 1]) for i in range(E2E_GROUPS) if bounds[i + 1] > bounds[i]]
+    cu_g_host = [(cu_host[n0:n1 + 1] - cu_host[n0]).to(torch.int32).pin_memory()
+                 for n0, n1 in groups]
+    g = {key: torch.empty_like(host[key], device=dev) for key in host}
+    cu_g = [torch.empty_like(c, device=dev) for c in cu_g_host]
     gd = [{key: torch.empty_like(x[key], device=dev) for key in x} for x in host_dec]
     o = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev)
     S = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
@@ -410,40 +429,77 @@ def run_e2e(args, kda, d, steps, spec, dev, stream):
     S_h = torch.empty(S.shape, dtype=S.dtype).pin_memory()
     od_h = torch.empty(o_dec.shape, dtype=o_dec.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host.values()) + \
+        sum(x.numel() * x.element_size() for x in cu_g_host) + \
         sum(x.numel() * x.element_size() for hd in host_dec for x in hd.values())
     d2h = sum(x.numel() * x.element_size() for x in (o_h, S_h, od_h))
+    up = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    down = torch.cuda.Stream(device=dev)
 
-    def step():
+    def step(start_ev):
+        for st in up + [down]:
+            st.wait_event(start_ev)
+        done_down = []
+        for gi, (n0, n1) in enumerate(groups):
+            t0, t1 = int(cu_host[n0]), int(cu_host[n1])
+            cs = up[gi % 2]
+            with torch.cuda.stream(cs):
+                for key in keys:
+                    g[key][t0:t1].copy_(host[key][t0:t1], non_blocking=True)
+                g["S0"][n0:n1].copy_(host["S0"][n0:n1], non_blocking=True)
+                cu_g[gi].copy_(cu_g_host[gi], non_blocking=True)
+                if gi == len(groups) - 1:
+                    for i, hd in enumerate(host_dec):
+                        for key in hd:
+                            gd[i][key].copy_(hd[key], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(cs)
+            stream.wait_event(ev_in)
+            with torch.cuda.stream(stream):
+                kda.prefill_into(g["q"][t0:t1], g["k"][t0:t1], g["v"][t0:t1],
+                                 g["alpha"][t0:t1], g["beta"][t0:t1], g["S0"][n0:n1],
+                                 cu_g[gi], o[t0:t1], S[n0:n1], wsp, chunk=spec.chunk,
+                                 stream=stream)
+                ev_pf = torch.cuda.Event()
+                ev_pf.record(stream)
+            down.wait_event(ev_pf)
+            with torch.cuda.stream(down):
+                o_h[t0:t1].copy_(o[t0:t1], non_blocking=True)
         with torch.cuda.stream(stream):
-            for key in keys:
-                g[key].copy_(host[key], non_blocking=True)
-            for i, hd in enumerate(host_dec):
-                for key in hd:
-                    gd[i][key].copy_(hd[key], non_blocking=True)
-            kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
-                             g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
             for i, x in enumerate(gd):
                 kda.decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S, o_dec[i],
                                 stream=stream)
-            o_h.copy_(o, non_blocking=True)
+            ev_dec = torch.cuda.Event()
+            ev_dec.record(stream)
+        down.wait_event(ev_dec)
+        with torch.cuda.stream(down):
             S_h.copy_(S, non_blocking=True)
             od_h.copy_(o_dec, non_blocking=True)
+            ev_end = torch.cuda.Event()
+            ev_end.record(down)
+        stream.wait_event(ev_end)
 
     e2e_steps = max(1, min(args.steps, 3))
-    step()
+    ev0 = torch.cuda.Event()
+    ev0.record(stream)
+    step(ev0)
     torch.cuda.synchronize()
     barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    prev = t0
     for _ in range(e2e_steps):
-        step()
+        step(prev)
+        prev = torch.cuda.Event()
+        prev.record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     el, units = reduce_max_sum(t0.elapsed_time(t1) / 1e3,
                                float((T + len(steps) * N) * e2e_steps), dev)
     return {"value": units / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+            "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+            "pipeline": f"{len(groups)} sequence groups: H2D on 2 streams, prefill, D2H on a "
+                        "third stream, overlapped; decode steps after the last group"}
 
 
 def run_component(args):
