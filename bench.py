@@ -535,7 +535,8 @@ def run_component(args):
         T = int(d["cu_seqlens"][-1])
         o = torch.empty((T, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
         S = torch.empty((spec.num_seqs, spec.H, spec.d_v, spec.d_k), device=dev)
-        wsp = torch.empty(kda.workspace_size(spec.num_seqs), dtype=torch.uint8, device=dev)
+        wsp = torch.empty(kda.workspace_size(spec.num_seqs, spec.H, spec.d_k, spec.d_v, spec.chunk),
+                          dtype=torch.uint8, device=dev)
 
         def launch():
             kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],

@@ -52,7 +52,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
         return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_CHUNK_SIMT &&
-        kernel != KDA_KERNEL_CHUNK_TC)
+        kernel != KDA_KERNEL_CHUNK_TC && kernel != KDA_KERNEL_CHUNK_TC_SPLIT)
         return KDA_ERR_INVALID_ARG;
     if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
     if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
@@ -89,13 +89,32 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     a.order = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kOrder);
 
     const bool tc_ok = kda::prefill_tc_supports(a);
-    if (kernel == KDA_KERNEL_CHUNK_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
-    const bool use_tc = kernel == KDA_KERNEL_CHUNK_TC || (kernel == KDA_KERNEL_AUTO && tc_ok);
+    const bool want_tc = kernel == KDA_KERNEL_CHUNK_TC || kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
+    if (want_tc && !tc_ok) return KDA_ERR_UNSUPPORTED;
+    const bool use_tc = want_tc || (kernel == KDA_KERNEL_AUTO && tc_ok);
+    // sequence-axis split: few chains, long sequences, room in the workspace
+    kda::SplitLayout split;
+    if (use_tc && kernel != KDA_KERNEL_CHUNK_TC && num_seqs > 0) {
+        const int M = kda::split_segments(num_seqs, H, d_k, d_v, chunk);
+        const bool forced = kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
+        if (forced && M < 3) return KDA_ERR_UNSUPPORTED;
+        const bool long_enough = total_tokens >= (int64_t)num_seqs * M * 2048;
+        if (M >= 3 && (long_enough || forced)) {
+            split = kda::split_layout(num_seqs, H, d_k, d_v, M);
+            if (workspace_bytes < split.end) {
+                if (forced) return KDA_ERR_INVALID_ARG;
+                split.M = 1;
+            }
+        }
+    }
 
     if (kda::launch_planner(a, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (num_seqs == 0) return KDA_OK;
-    const cudaError_t err = use_tc ? kda::launch_prefill_tc(a, stream)
-                                   : kda::launch_prefill_simt(a, stream);
+    cudaError_t err;
+    if (use_tc && split.M >= 3)
+        err = kda::launch_prefill_tc_split(a, split, ws, stream);
+    else
+        err = use_tc ? kda::launch_prefill_tc(a, stream) : kda::launch_prefill_simt(a, stream);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -105,9 +124,13 @@ extern "C" {
 
 size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
                                   int32_t chunk) {
-    (void)H; (void)d_k; (void)d_v; (void)chunk;
     if (num_seqs < 0) return 0;
-    return kda::WorkspaceLayout::bytes(num_seqs);
+    const size_t base = kda::WorkspaceLayout::bytes(num_seqs);
+    if (H < 1 || d_k < 1 || d_v < 1) return base;
+    const int M = kda::split_segments(num_seqs, H, d_k, d_v, chunk);
+    if (M < 3) return base;
+    const size_t split = kda::split_layout(num_seqs, H, d_k, d_v, M).end;
+    return split > base ? split : base;
 }
 
 kda_status kda_prefill(const void* q, const void* k, const void* v, const float* alpha,
@@ -134,13 +157,13 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
 kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d_k, int32_t d_v,
                                  kda_dtype dtype, int32_t chunk) {
     if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_CHUNK_SIMT &&
-        kernel != KDA_KERNEL_CHUNK_TC)
+        kernel != KDA_KERNEL_CHUNK_TC && kernel != KDA_KERNEL_CHUNK_TC_SPLIT)
         return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
     if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
     if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
-    if (kernel != KDA_KERNEL_CHUNK_TC) return KDA_OK;
+    if (kernel != KDA_KERNEL_CHUNK_TC && kernel != KDA_KERNEL_CHUNK_TC_SPLIT) return KDA_OK;
     kda::PrefillArgs a = {};
     a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.chunk = chunk;
     return kda::prefill_tc_supports(a) ? KDA_OK : KDA_ERR_UNSUPPORTED;

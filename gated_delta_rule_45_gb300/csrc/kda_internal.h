@@ -23,6 +23,24 @@ struct WorkspaceLayout {
     }
 };
 
+// Sequence-axis split of the tensor-core prefill (few long chains): each
+// sequence is cut into M segments of whole chunks.  Virtual sequence
+// v = j * N + n is segment j of sequence n.  Buffers appended to the workspace:
+//   vt0   int64 [M N]           first token of each segment
+//   vlen  int32 [M N]           its length
+//   sfin  fp32 [(M-1) N][H][d_v][d_k]   final state of segments 0..M-2
+//             (segment 0 from the true S0, the others from zero)
+//   pbuf  fp32 [(M-2) N][H][d_k][d_k]   transition P of segments 1..M-2
+//   gbuf  fp32 [(M-1) N][H][d_v]        prod alpha over segments 0..M-2
+//   sst   fp32 [(M-1) N][H][d_v][d_k]   true initial state of segments 1..M-1
+struct SplitLayout {
+    int M = 1;
+    size_t vt0 = 0, vlen = 0, sfin = 0, pbuf = 0, gbuf = 0, sst = 0, end = 0;
+};
+// Segments for this shape on the current device (1: no split).
+int split_segments(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int32_t chunk);
+SplitLayout split_layout(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int M);
+
 struct PrefillArgs {
     const void* q;
     const void* k;
@@ -59,6 +77,14 @@ struct DecodeArgs {
 cudaError_t launch_planner(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+// The split form: segment planner, three chunk-kernel launches and the scan of
+// the segment maps in between (ws: the workspace base).
+cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, char* ws,
+                                    cudaStream_t stream);
+cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, char* ws,
+                              cudaStream_t stream);
+cudaError_t launch_split_combine(const PrefillArgs& a, const SplitLayout& L, char* ws,
+                                 cudaStream_t stream);
 bool prefill_tc_supports(const PrefillArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

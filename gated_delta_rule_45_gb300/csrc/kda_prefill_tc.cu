@@ -119,6 +119,18 @@ struct TcParams {
     const int32_t* order;
     int32_t* status;
     int32_t H, d_v, nvb, num_items;
+    // Sequence-axis split (null vt0: plain launch).  Items then run over virtual
+    // sequences v = n_base + rank with token ranges [vt0[v], vt0[v] + vlen[v]);
+    // S0 is read for v in [s0_lo, s0_hi) (row v - s0_lo, zero elsewhere) and the
+    // final state written for v in [st_lo, st_hi) (row v - st_lo); g_out[v]
+    // receives prod alpha over the item per channel.  CTAs from a_ctas on run
+    // transition items instead: v = n_base_p + rank, alpha = 1, v = 0, S0 = I,
+    // one 128-row block, final state to P_out[v - n_base_p], no output.
+    const int64_t* vt0;
+    const int32_t* vlen;
+    int32_t n_base, n_base_p, s0_lo, s0_hi, st_lo, st_hi, a_ctas, num_items_p;
+    float* g_out;
+    float* P_out;
 };
 
 struct ItemInfo {
@@ -126,44 +138,71 @@ struct ItemInfo {
     int64_t t0;
 };
 
-__device__ __forceinline__ ItemInfo item_info(const TcParams& p, int item) {
+// SPLIT: the kernel serves the split launches (virtual sequences, transition
+// items); the plain instantiation compiles none of that.
+template <bool SPLIT>
+__device__ __forceinline__ ItemInfo item_info(const TcParams& p, int item, bool pk) {
     ItemInfo it;
-    const int per_rank = p.H * p.nvb;
+    const int nvb = pk ? 1 : p.nvb;
+    const int per_rank = p.H * nvb;
     const int rank = item / per_rank, rem = item % per_rank;
-    it.h = rem / p.nvb;
-    it.vb = rem % p.nvb;
-    it.n = p.order[rank];
-    it.t0 = p.cu[it.n];
-    it.len = p.cu[it.n + 1] - p.cu[it.n];
+    it.h = rem / nvb;
+    it.vb = rem % nvb;
+    if (SPLIT) {
+        it.n = (pk ? p.n_base_p : p.n_base) + rank;
+        it.t0 = p.vt0[it.n];
+        it.len = p.vlen[it.n];
+    } else {
+        it.n = p.order[rank];
+        it.t0 = p.cu[it.n];
+        it.len = p.cu[it.n + 1] - p.cu[it.n];
+    }
     it.nc = (it.len + C - 1) / C;
     return it;
 }
 
+// This CTA's share of the items: its kind (plain / transition), first item,
+// stride and item count.
+template <bool SPLIT>
+struct ItemRange {
+    bool pk;
+    int first, stride, count;
+    __device__ explicit ItemRange(const TcParams& p) {
+        pk = SPLIT && (int)blockIdx.x >= p.a_ctas;
+        first = pk ? (int)blockIdx.x - p.a_ctas : (int)blockIdx.x;
+        stride = pk ? (int)gridDim.x - p.a_ctas : p.a_ctas;
+        count = pk ? p.num_items_p : p.num_items;
+    }
+};
+
 // Walks the chunks of this CTA's items in order, skipping empty items.
+template <bool SPLIT>
 struct ChunkCursor {
     int item, c;
     bool valid;
     ItemInfo info;
+    ItemRange<SPLIT> rg;
+    __device__ explicit ChunkCursor(const TcParams& p) : rg(p) {}
     __device__ void init(const TcParams& p) {
-        item = blockIdx.x;
+        item = rg.first;
         c = 0;
         seek(p);
     }
     __device__ void seek(const TcParams& p) {
         valid = false;
-        while (item < p.num_items) {
-            info = item_info(p, item);
+        while (item < rg.count) {
+            info = item_info<SPLIT>(p, item, rg.pk);
             if (info.nc > 0) {
                 valid = true;
                 return;
             }
-            item += gridDim.x;
+            item += rg.stride;
         }
     }
     __device__ void next(const TcParams& p) {
         if (++c >= info.nc) {
             c = 0;
-            item += gridDim.x;
+            item += rg.stride;
             seek(p);
         }
     }
@@ -227,9 +266,11 @@ __device__ __forceinline__ uint32_t kq_addr(const Ctx& cx, int s) {
 }
 
 // ------------------------------------------------------------------ producer
+template <bool SPLIT>
 __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
-    ChunkCursor cur;
+    ChunkCursor<SPLIT> cur(p);
     cur.init(p);
+    const bool pk = cur.rg.pk;
     uint32_t g = 0;
     uint32_t kq_issued[2] = {0, 0}, a_issued = 0, v_issued[2] = {0, 0};
     const float* beta_st = reinterpret_cast<const float*>(cx.smem + SM_BETA);
@@ -258,6 +299,11 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
             tma_load_3d(st + KQ_KBLOCK + 8192, &p.tm_q, bar, 64, h, (int32_t)tok0);
         }
         ++kq_issued[s];
+        if (pk) {   // transition items: alpha = 1 and v = 0, nothing to load
+            ++g;
+            cur.next(p);
+            continue;
+        }
         // alpha: one buffer, free once the row group has read it into registers
         if (g >= 1) {
             int r = 1;
@@ -327,8 +373,9 @@ __device__ __forceinline__ bool kqk_ready(const Ctx& cx, uint32_t g) {
 
 // The whole warp runs the schedule and waits; one elected lane issues each
 // group of MMAs together with the commit that tracks it.
+template <bool SPLIT>
 __device__ void run_mma(const TcParams& p, const Ctx& cx) {
-    ChunkCursor cur, ahead;
+    ChunkCursor<SPLIT> cur(p), ahead(p);
     cur.init(p);
     ahead = cur;
     uint32_t g = 0;
@@ -483,6 +530,7 @@ __device__ __forceinline__ void warp_store16(float* Y, int ldy, const float (&ac
 // the KQK accumulator, then T = (I + L)^{-1} by blocks of 16: the four
 // diagonal blocks D_b by forward substitution, the rest by recursive doubling
 // of the block-triangular inverse, and finally T and P as bf16 hi/lo tiles.
+template <bool SPLIT>
 __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int warp, int lane) {
     Group grp{t, 1, 128, 0, cx.slots};
     const int quarter = warp & 3;
@@ -490,7 +538,7 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     float* Ls = reinterpret_cast<float*>(cx.smem + SM_L);
     float* Ys = reinterpret_cast<float*>(cx.smem + SM_Y);
-    ChunkCursor cur;
+    ChunkCursor<SPLIT> cur(p);
     cur.init(p);
     uint32_t g = 0;
     while (cur.valid) {
@@ -648,6 +696,7 @@ __device__ __forceinline__ void stage_state_piece(uint32_t lane_addr, int h, int
     tmem_st16(lane_addr + TM_SLO + 32 * h + 16 * q, lo);
 }
 
+template <bool SPLIT>
 __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp, int lane) {
     const int quarter = warp & 3;
     const int h = rt >> 7;                 // token half / key-channel half
@@ -656,16 +705,40 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
     uint32_t g = 0;
     bool ok = true;
     const float* al = reinterpret_cast<const float*>(cx.smem + SM_ALPHA);
-    for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
-        const ItemInfo it = item_info(p, item);
+    const ItemRange<SPLIT> rg(p);
+    float* const st_base = rg.pk ? p.P_out : p.S_T;
+    const int dvs = rg.pk ? DK : p.d_v;   // rows per head of the state layout
+    for (int item = rg.first; item < rg.count && ok; item += rg.stride) {
+        const ItemInfo it = item_info<SPLIT>(p, item, rg.pk);
         const int ch = it.vb * DVB + r;   // value channel
-        const size_t srow = (((size_t)it.n * p.H + it.h) * p.d_v + ch) * DK + 64 * h;
-        if (it.nc == 0) {
-            for (int j = 0; j < 64; j += 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.S0) x = *reinterpret_cast<const float4*>(p.S0 + srow + j);
-                *reinterpret_cast<float4*>(p.S_T + srow + j) = x;
+        // rows of the initial and final state of this item (-1: zero / not written)
+        int s0_row = p.S0 ? it.n : -1, st_row = it.n;
+        if (SPLIT) {
+            s0_row = -1;
+            st_row = it.n - p.n_base_p;
+            if (!rg.pk) {
+                if (p.S0 && it.n >= p.s0_lo && it.n < p.s0_hi) s0_row = it.n - p.s0_lo;
+                st_row = it.n >= p.st_lo && it.n < p.st_hi ? it.n - p.st_lo : -1;
             }
+        }
+        const size_t s0off = (((size_t)s0_row * p.H + it.h) * dvs + ch) * DK + 64 * h;
+        const size_t stoff = (((size_t)st_row * p.H + it.h) * dvs + ch) * DK + 64 * h;
+        // initial state, 4 key channels from 64 h + j: S0, zero, or the identity
+        auto init4 = [&](int j) {
+            if (rg.pk) {
+                const int c0 = 64 * h + j;
+                return make_float4(c0 == ch ? 1.f : 0.f, c0 + 1 == ch ? 1.f : 0.f,
+                                   c0 + 2 == ch ? 1.f : 0.f, c0 + 3 == ch ? 1.f : 0.f);
+            }
+            return s0_row >= 0 ? *reinterpret_cast<const float4*>(p.S0 + s0off + j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        if (it.nc == 0) {
+            if (st_row >= 0)
+                for (int j = 0; j < 64; j += 4)
+                    *reinterpret_cast<float4*>(st_base + stoff + j) = init4(j);
+            if (SPLIT && p.g_out && !rg.pk && h == 0)
+                p.g_out[((size_t)it.n * p.H + it.h) * p.d_v + ch] = 1.f;
             continue;
         }
 #pragma unroll 1
@@ -673,12 +746,12 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             float x[32];
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
-                float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.S0) v4 = *reinterpret_cast<const float4*>(p.S0 + srow + 32 * q + j);
+                const float4 v4 = init4(32 * q + j);
                 x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
             }
             stage_state_piece(lane_addr, h, q, x);
         }
+        float gtot = 1.f;   // prod alpha over the item, for g_out
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -689,13 +762,17 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             const int nvalid = min(C, it.len - c * C);
             const bool last = c + 1 == it.nc;
             if (!(ok = warp_wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
-            if (!(ok = warp_wait(cx, B_A_FULL, g & 1))) break;
             const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
             // Gamma (padded tokens: alpha = 1): each thread takes the running
             // product over its half of the tokens, the halves swap their totals
-            // through shared memory; then vg = beta V / Gamma for its tokens
-            float gam[32], vg[32], gC;
-            {
+            // through shared memory; then vg = beta V / Gamma for its tokens.
+            // Transition items have alpha = 1 and v = 0.
+            float gam[32], vg[32], gC = 1.f;
+            if (rg.pk) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vg[j] = 0.f;
+            } else {
+                if (!(ok = warp_wait(cx, B_A_FULL, g & 1))) break;
                 float* half_tot = reinterpret_cast<float*>(cx.smem + SM_HALF);
                 // The tiles always hold finite values (TMA fills rows past the tensor
                 // with zeros; rows past the sequence belong to the next one), so the
@@ -750,9 +827,10 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                     const float2 v23 = __fmul2_rn(make_float2(vq[2], vq[3]), make_float2(bq.z, bq.w));
                     vg[j] = v01.x; vg[j + 1] = v01.y; vg[j + 2] = v23.x; vg[j + 3] = v23.y;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cx.bars[B_V_EMPTY + (g & 1)]);   // V consumed
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&cx.bars[B_V_EMPTY + (g & 1)]);   // V consumed
+            gtot *= gC;
 
             // X = vg - beta (S K^T), split and staged as the A operand of U^T = X^T T^T
             if (!(ok = warp_wait(cx, B_SKQ_DONE, g & 1))) break;
@@ -832,10 +910,12 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                     x[j + 1] = xx.y;
                 }
                 if (last) {
+                    if (st_row >= 0) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(p.S_T + srow + 32 * q + j) =
-                            make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(st_base + stoff + 32 * q + j) =
+                                make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    }
                 } else {
                     stage_state_piece(lane_addr, h, q, x);
                 }
@@ -846,8 +926,15 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
             }
+            if (SPLIT && last && p.g_out && !rg.pk && h == 0)
+                p.g_out[((size_t)it.n * p.H + it.h) * p.d_v + ch] = gtot;
             // O = Gamma * (Q S^T + P U); leaves after the state has been handed back
             if (!(ok = warp_wait(cx, B_O_DONE, g & 1))) break;
+            if (rg.pk) {   // transition items have no output
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
+                continue;
+            }
             tc_fence_after();
             uint32_t opk[16];
             {
@@ -895,6 +982,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
 }
 
 // ------------------------------------------------------------------ kernel
+template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p) {
     if (*p.status != 0) return;   // planner rejected cu_seqlens
     extern __shared__ uint8_t smem_raw[];
@@ -932,13 +1020,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     cx.tmem = *tslot;
 
     if (warp == 0) {
-        run_producer(p, cx, lane);
+        run_producer<SPLIT>(p, cx, lane);
     } else if (warp == 1) {
-        run_mma(p, cx);
+        run_mma<SPLIT>(p, cx);
     } else if (warp >= 2 && warp < 6) {
-        run_token_group(p, cx, tid - 64, warp, lane);
+        run_token_group<SPLIT>(p, cx, tid - 64, warp, lane);
     } else {
-        run_row_group(p, cx, tid - 192, warp, lane);
+        run_row_group<SPLIT>(p, cx, tid - 192, warp, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -975,6 +1063,53 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t e
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps and the fields every launch shares; a plain launch over the
+// real sequences unless the caller changes the split fields.
+bool init_params(const PrefillArgs& a, TcParams& p) {
+    if (!make_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, DK, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, DK, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, a.d_v,
+                  DVB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&p.tm_a, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.total_tokens, a.H,
+                  a.d_v, DVB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    p.beta = a.beta;
+    p.S0 = a.S0;
+    p.S_T = a.S_T;
+    p.o = static_cast<__nv_bfloat16*>(a.o);
+    p.cu = a.cu_seqlens;
+    p.order = a.order;
+    p.status = a.status;
+    p.H = a.H;
+    p.d_v = a.d_v;
+    p.nvb = a.d_v / DVB;
+    p.num_items = a.num_seqs * a.H * p.nvb;
+    p.vt0 = nullptr;
+    p.vlen = nullptr;
+    p.n_base = 0;
+    p.n_base_p = 0;
+    p.s0_lo = 0;
+    p.s0_hi = a.num_seqs;
+    p.st_lo = 0;
+    p.st_hi = a.num_seqs;
+    p.num_items_p = 0;
+    p.g_out = nullptr;
+    p.P_out = nullptr;
+    return true;
+}
+
+template <bool SPLIT>
+cudaError_t launch(TcParams& p, int grid, cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(kda_prefill_tc_kernel<SPLIT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    kda_prefill_tc_kernel<SPLIT><<<grid, kThreads, SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool prefill_tc_supports(const PrefillArgs& a) {
@@ -988,35 +1123,61 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     // nothing to load: the portable kernel copies S0 to S_T
     if (a.total_tokens == 0) return launch_prefill_simt(a, stream);
     TcParams p;
-    if (!make_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, DK, 64,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, DK, 64,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, a.d_v,
-                  DVB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&p.tm_a, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.total_tokens, a.H,
-                  a.d_v, DVB, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    p.beta = a.beta;
-    p.S0 = a.S0;
-    p.S_T = a.S_T;
-    p.o = static_cast<__nv_bfloat16*>(a.o);
-    p.cu = a.cu_seqlens;
-    p.order = a.order;
-    p.status = a.status;
-    p.H = a.H;
-    p.d_v = a.d_v;
-    p.nvb = a.d_v / DVB;
-    p.num_items = a.num_seqs * a.H * p.nvb;
+    if (!init_params(a, p)) return cudaErrorInvalidValue;
     if (p.num_items == 0) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(kda_prefill_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)SMEM_BYTES);
-    if (err != cudaSuccess) return err;
     const int sms = sm_count();
     const int grid = p.num_items < sms ? p.num_items : sms;
-    kda_prefill_tc_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    p.a_ctas = grid;
+    return launch<false>(p, grid, stream);
+}
+
+cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, char* ws,
+                                    cudaStream_t stream) {
+    if (!prefill_tc_supports(a) || L.M < 3) return cudaErrorInvalidValue;
+    if (a.total_tokens == 0 || a.num_seqs == 0) return launch_prefill_tc(a, stream);
+    TcParams p;
+    if (!init_params(a, p)) return cudaErrorInvalidValue;
+    const int M = L.M, N = a.num_seqs;
+    cudaError_t err = launch_split_plan(a, L, ws, stream);
+    if (err != cudaSuccess) return err;
+    p.vt0 = reinterpret_cast<const int64_t*>(ws + L.vt0);
+    p.vlen = reinterpret_cast<const int32_t*>(ws + L.vlen);
+    const int sms = sm_count();
+    // pass 1: segment 0 from S0 and segments 1..M-2 from zero (final states
+    // and prod alpha kept), and the transitions P of segments 1..M-2
+    TcParams p1 = p;
+    p1.num_items = (M - 1) * N * a.H * p.nvb;
+    p1.S_T = reinterpret_cast<float*>(ws + L.sfin);
+    p1.st_hi = (M - 1) * N;
+    p1.g_out = reinterpret_cast<float*>(ws + L.gbuf);
+    p1.n_base_p = N;
+    p1.num_items_p = (M - 2) * N * a.H;
+    p1.P_out = reinterpret_cast<float*>(ws + L.pbuf);
+    // one CTA per plain chain when they fit, the rest to transitions
+    int a_ctas = p1.num_items < sms ? p1.num_items : sms;
+    int p_ctas = sms - a_ctas;
+    if (p_ctas > p1.num_items_p) p_ctas = p1.num_items_p;
+    if (p_ctas < 1) {   // more chains than SMs: split the grid evenly
+        a_ctas = sms / 2;
+        p_ctas = sms - a_ctas;
+    }
+    p1.a_ctas = a_ctas;
+    if ((err = launch<true>(p1, a_ctas + p_ctas, stream)) != cudaSuccess) return err;
+    // the scan of the segment maps: true initial states of segments 1..M-1
+    if ((err = launch_split_combine(a, L, ws, stream)) != cudaSuccess) return err;
+    // pass 2: segments 1..M-1 from their true initial states; the last one
+    // writes S_T
+    TcParams p2 = p;
+    p2.n_base = N;
+    p2.num_items = (M - 1) * N * a.H * p.nvb;
+    p2.S0 = reinterpret_cast<const float*>(ws + L.sst);
+    p2.s0_lo = N;
+    p2.s0_hi = M * N;
+    p2.st_lo = (M - 1) * N;
+    p2.st_hi = M * N;
+    const int grid2 = p2.num_items < sms ? p2.num_items : sms;
+    p2.a_ctas = grid2;
+    return launch<true>(p2, grid2, stream);
 }
 
 }  // namespace kda

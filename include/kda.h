@@ -64,21 +64,38 @@ typedef enum {
 
 /* Which prefill kernel runs.  AUTO picks the tensor-core kernel whenever the
  * shape qualifies (dtype KDA_BF16, d_k == 128, d_v a multiple of 128,
- * chunk == 64) and the portable chunk kernel otherwise. */
+ * chunk == 64) and the portable chunk kernel otherwise; with the tensor-core
+ * kernel it also splits the sequence axis (below) when the batch has fewer
+ * (sequence, head, 128-channel block) chains than a third of the SMs, the
+ * sequences average at least 2048 tokens per segment, and the workspace has
+ * room for it. */
 typedef enum {
     KDA_KERNEL_AUTO = 0,
     KDA_KERNEL_CHUNK_SIMT = 1,   /* fp32 CUDA-core chunk kernel: any supported shape */
-    KDA_KERNEL_CHUNK_TC = 2      /* tcgen05 / TMEM / TMA chunk kernel */
+    KDA_KERNEL_CHUNK_TC = 2,     /* tcgen05 / TMEM / TMA chunk kernel */
+    /* the tensor-core kernel with the sequence axis split into M >= 3
+     * segments of whole chunks: a first pass runs segment 0 of every sequence
+     * from S0 and, for segments 1..M-2, the state reached from zero, the
+     * product of alpha and the transition prod (I - beta k k^T); a scan
+     * chains these affine maps into each segment's initial state; a second
+     * pass runs segments 1..M-1 from those states.  Same results as
+     * KDA_KERNEL_CHUNK_TC up to rounding.  Only for batches with few chains
+     * (those for which kda_prefill_workspace_size includes the segment
+     * buffers), whatever the sequence lengths. */
+    KDA_KERNEL_CHUNK_TC_SPLIT = 3
 } kda_prefill_kernel;
 
 typedef void* kda_stream_t;   /* a cudaStream_t */
 
 /*
- * Bytes of device workspace kda_prefill needs for `num_seqs` sequences (the
- * other sizes are accepted for forward compatibility and do not change the
- * result today).  Returns 0 for num_seqs < 0.  The workspace holds the
- * varlen schedule (sequence order, work counter, device error word); its
- * contents need no initialisation and are overwritten by every call.
+ * Bytes of device workspace kda_prefill needs for `num_seqs` sequences of H
+ * heads with these sizes.  Returns 0 for num_seqs < 0.  The workspace holds
+ * the varlen schedule (sequence order, work counter, device error word) and,
+ * for batches with few (sequence, head, 128-channel block) chains on the
+ * current device, the buffers of the sequence-axis split: at most
+ * 8 x num_seqs x H x d_v x d_k x 12 bytes.  A smaller workspace of at least
+ * the schedule's size is accepted and never splits.  Its contents need no
+ * initialisation and are overwritten by every call.
  */
 size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
                                   int32_t chunk);
@@ -118,9 +135,11 @@ kda_status kda_prefill(const void* q, const void* k, const void* v,
                        void* o, float* S_T, void* workspace, size_t workspace_bytes,
                        kda_stream_t stream);
 
-/* kda_prefill with an explicit kernel choice (for testing both kernels on
- * one shape).  Requesting KDA_KERNEL_CHUNK_TC for a shape it does not cover
- * returns KDA_ERR_UNSUPPORTED. */
+/* kda_prefill with an explicit kernel choice (for testing the kernels on one
+ * shape).  Requesting KDA_KERNEL_CHUNK_TC or KDA_KERNEL_CHUNK_TC_SPLIT for a
+ * shape the tensor-core kernel does not cover returns KDA_ERR_UNSUPPORTED;
+ * KDA_KERNEL_CHUNK_TC_SPLIT with a workspace smaller than
+ * kda_prefill_workspace_size returns KDA_ERR_INVALID_ARG. */
 kda_status kda_prefill_ex(const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,
                           const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,

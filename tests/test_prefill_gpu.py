@@ -153,3 +153,65 @@ def test_bad_cu_seqlens_reported_and_nothing_written(bad):
             kda.device_status(ws)
         assert ei.value.status == kda.ERR_DEVICE_INPUT
         assert torch.all(o == 5.0) and torch.all(S_T == 5.0)
+
+
+def _split_case(lengths, H, d_v, s0_std, seed):
+    spec = synth.PrefillSpec(num_seqs=len(lengths), len_lo=1, len_hi=1, H=H, d_k=128, d_v=d_v,
+                             chunk=64, s0_std=s0_std, seed=seed)
+    d = synth.prefill_inputs(spec)
+    # replace the drawn lengths with the given ones (inputs are per token, so
+    # a longer draw is cut to size)
+    T = int(sum(lengths))
+    big = synth.PrefillSpec(num_seqs=1, len_lo=T, len_hi=T, H=H, d_k=128, d_v=d_v, chunk=64,
+                            s0_std=0.0, seed=seed)
+    db = synth.prefill_inputs(big)
+    for key in ("q", "k", "v", "alpha", "beta"):
+        d[key] = db[key]
+    d["cu_seqlens"] = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    d["lengths"] = list(lengths)
+    return spec, d
+
+
+@pytest.mark.parametrize("lengths,H,d_v,s0_std", [
+    ([1000, 60, 2500], 2, 128, 0.1),     # one single-chunk sequence: mostly empty segments
+    ([4096, 0, 3000], 1, 256, 0.1),      # an empty sequence, two value blocks
+    ([5000], 3, 128, 0.0),               # no initial state
+])
+def test_sequence_split_matches_oracle(lengths, H, d_v, s0_std):
+    """The split form (segment 0 from S0, segment maps from zero / identity,
+    their scan, then the other segments from their true initial states)
+    against the oracle, on every (sequence, head)."""
+    spec, d = _split_case(lengths, H, d_v, s0_std, seed=11)
+    if not kda.supported("tc_split", H, 128, d_v, torch.bfloat16, 64):
+        pytest.skip("tensor-core kernel not available for this shape")
+    dev = parity.to_device(d)
+    N = len(lengths)
+    ws_bytes = kda.workspace_size(N, H, 128, d_v, 64)
+    assert ws_bytes > kda.workspace_size(N, 1, 16, 16, 16)   # room for the segments
+    o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], chunk=64, kernel="tc_split",
+                         check_device_status=True)
+    ref = parity.oracle_pairs(d, [(n, h) for n in range(N) for h in range(H)])
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
+    # the unsplit kernel on the same inputs agrees to rounding
+    o2, S2 = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], chunk=64, kernel="tc", check_device_status=True)
+    assert parity.rel(S_T.cpu().numpy(), S2.cpu().numpy()) < 1e-4
+    assert parity.rel(o.float().cpu().numpy(), o2.float().cpu().numpy()) < 3e-3
+
+
+def test_sequence_split_in_place_state():
+    """S_T may alias S0 under the split form too."""
+    spec, d = _split_case([3000, 2000], 2, 128, 0.1, seed=12)
+    dev = parity.to_device(d)
+    S = dev["S0"].clone()
+    T = int(d["cu_seqlens"][-1])
+    o = torch.empty((T, 2, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(kda.workspace_size(2, 2, 128, 128, 64), dtype=torch.uint8, device="cuda")
+    kda.prefill_into(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], S,
+                     dev["cu_seqlens"], o, S, ws, kernel="tc_split")
+    kda.device_status(ws)
+    ref = parity.oracle_pairs(d, [(n, h) for n in range(2) for h in range(2)])
+    wo, wsr = parity.compare_pairs(d, o, S, ref)
+    assert wo <= parity.TOL_BF16 and wsr <= parity.TOL_BF16, (wo, wsr)
