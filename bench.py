@@ -133,10 +133,14 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
-def workload_bytes(spec, T: int, decode_steps: int):
-    """Algorithmic HBM bytes of one prefill launch and of one decode step."""
+def workload_bytes(spec, T: int, decode_steps: int, alpha_bytes: int | None = None):
+    """Algorithmic HBM bytes of one prefill launch and of one decode step
+    (alpha_bytes: bytes of the forget gate per token-head, fp32 per channel
+    by default)."""
     esz = 2 if spec.dtype == "bf16" else 4
-    per_token_head = 2 * spec.d_k * esz + spec.d_v * esz + spec.d_v * 4 + 4 + spec.d_v * esz
+    if alpha_bytes is None:
+        alpha_bytes = spec.d_v * 4
+    per_token_head = 2 * spec.d_k * esz + spec.d_v * esz + alpha_bytes + 4 + spec.d_v * esz
     state = spec.num_seqs * spec.H * spec.d_v * spec.d_k * 4
     prefill = T * spec.H * per_token_head + 2 * state + 4 * (spec.num_seqs + 1)
     bh = spec.num_seqs * spec.H
@@ -528,7 +532,10 @@ def run_component(args):
         units, unit = bh, "state-updates/s"
         desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
     else:
-        spec = synth.WORKLOADS["varlen" if args.workload == "varlen_prefill" else args.workload]
+        gate = {"prefill_head_gate": "head", "prefill_log_gate": "log_bf16"}.get(args.workload)
+        name = "varlen" if args.workload == "varlen_prefill" else \
+            "prefill" if gate else args.workload
+        spec = synth.WORKLOADS[name]
         d = synth.prefill_inputs(spec)
         g = {key: (d[key].to(dev) if d[key] is not None else None)
              for key in ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")}
@@ -538,13 +545,30 @@ def run_component(args):
         wsp = torch.empty(kda.workspace_size(spec.num_seqs, spec.H, spec.d_k, spec.d_v, spec.chunk),
                           dtype=torch.uint8, device=dev)
 
-        def launch():
-            kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
-                             g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
-        nbytes, _ = workload_bytes(spec, T, 0)
+        alpha_bytes = None
+        if gate is None:
+            def launch():
+                kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                                 g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
+        else:
+            # the same synthetic gates in the other layout: channel 0's gate for
+            # every channel, or log alpha rounded to bf16
+            if gate == "head":
+                ga = g["alpha"][:, :, 0].contiguous()
+                alpha_bytes = 4
+            else:
+                ga = torch.log(g["alpha"]).to(torch.bfloat16)
+                alpha_bytes = spec.d_v * 2
+
+            def launch():
+                kda.prefill_gates_into(g["q"], g["k"], g["v"], ga, g["beta"], g["S0"],
+                                       g["cu_seqlens"], o, S, wsp, gate=gate, chunk=spec.chunk,
+                                       stream=stream)
+        nbytes, _ = workload_bytes(spec, T, 0, alpha_bytes)
         units, unit = T, "tokens/s"
         desc = (f"{args.workload}: N={spec.num_seqs}, T={T}, H={spec.H}, d_k={spec.d_k}, "
-                f"d_v={spec.d_v}, chunk={spec.chunk}")
+                f"d_v={spec.d_v}, chunk={spec.chunk}"
+                + (f", gate layout {gate}" if gate else ""))
         lens = [int(x) for x in d["lengths"]]
         mma_flops = (MMA_FLOPS_PER_BLOCK_CHUNK * spec.H * (spec.d_v // 128)
                      * sum((n + spec.chunk - 1) // spec.chunk for n in lens))
@@ -600,12 +624,13 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload",
                    choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
-                            "l2_resident"],
+                            "l2_resident", "prefill_head_gate", "prefill_log_gate"],
                    default="varlen",
                    help="varlen (default): the full step; others time one kernel alone "
                         "(varlen_prefill: the varlen batch's prefill without the decode steps; "
                         "l2_resident: the chunk kernel with its inputs in L2, against the "
-                        "tensor-core peak)")
+                        "tensor-core peak; prefill_head_gate / prefill_log_gate: the prefill "
+                        "workload with a per-head fp32 gate / a bf16 log-alpha gate)")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)

@@ -41,12 +41,12 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
 
 namespace kda {
 
-kda_status prefill_impl(const void* q, const void* k, const void* v, const float* alpha,
+kda_status prefill_impl(const void* q, const void* k, const void* v, const void* alpha,
                         const float* beta, const float* S0, const int32_t* cu_seqlens,
                         int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                         int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
                         void* workspace, size_t workspace_bytes, kda_prefill_kernel kernel,
-                        kda_stream_t stream_) {
+                        kda_stream_t stream_, kda_gate_format gate) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1)
         return KDA_ERR_INVALID_ARG;
@@ -54,9 +54,15 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     if (kernel != KDA_KERNEL_AUTO && kernel != KDA_KERNEL_CHUNK_SIMT &&
         kernel != KDA_KERNEL_CHUNK_TC && kernel != KDA_KERNEL_CHUNK_TC_SPLIT)
         return KDA_ERR_INVALID_ARG;
+    if (gate != KDA_GATE_CHANNEL_F32 && gate != KDA_GATE_HEAD_F32 &&
+        gate != KDA_GATE_CHANNEL_LOG_BF16)
+        return KDA_ERR_INVALID_ARG;
     if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
     if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
     if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (gate != KDA_GATE_CHANNEL_F32 &&
+        (kernel == KDA_KERNEL_CHUNK_SIMT || kernel == KDA_KERNEL_CHUNK_TC_SPLIT))
+        return KDA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * H > (int64_t)INT32_MAX / 64) return KDA_ERR_UNSUPPORTED;
     if (!cu_seqlens || !workspace || (num_seqs > 0 && !S_T)) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !alpha || !beta || !o)) return KDA_ERR_INVALID_ARG;
@@ -71,7 +77,9 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     if (S0 && S_T != S0 && overlaps(S_T, n_s, S0, n_s)) return KDA_ERR_INVALID_ARG;
     const size_t n_qk = (size_t)total_tokens * H * d_k * esz;
     const size_t n_v = (size_t)total_tokens * H * d_v * esz;
-    const size_t n_a = (size_t)total_tokens * H * d_v * sizeof(float);
+    const size_t n_a = gate == KDA_GATE_HEAD_F32 ? (size_t)total_tokens * H * sizeof(float)
+                       : gate == KDA_GATE_CHANNEL_LOG_BF16 ? (size_t)total_tokens * H * d_v * 2
+                                                           : (size_t)total_tokens * H * d_v * sizeof(float);
     const void* ins[] = {q, k, v, alpha, beta};
     const size_t in_n[] = {n_qk, n_qk, n_v, n_a, (size_t)total_tokens * H * sizeof(float)};
     for (int i = 0; i < 5; ++i)
@@ -82,6 +90,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     kda::PrefillArgs a;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S0 = S0;
     a.cu_seqlens = cu_seqlens; a.num_seqs = num_seqs; a.total_tokens = total_tokens;
+    a.gate = gate;
     a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.chunk = chunk; a.o = o; a.S_T = S_T;
     char* ws = static_cast<char*>(workspace);
     a.status = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kStatus);
@@ -91,10 +100,12 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     const bool tc_ok = kda::prefill_tc_supports(a);
     const bool want_tc = kernel == KDA_KERNEL_CHUNK_TC || kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
     if (want_tc && !tc_ok) return KDA_ERR_UNSUPPORTED;
+    // the other gate layouts run on the tensor-core kernel only, unsplit
+    if (gate != KDA_GATE_CHANNEL_F32 && !tc_ok) return KDA_ERR_UNSUPPORTED;
     const bool use_tc = want_tc || (kernel == KDA_KERNEL_AUTO && tc_ok);
     // sequence-axis split: few chains, long sequences, room in the workspace
     kda::SplitLayout split;
-    if (use_tc && kernel != KDA_KERNEL_CHUNK_TC && num_seqs > 0) {
+    if (use_tc && kernel != KDA_KERNEL_CHUNK_TC && num_seqs > 0 && gate == KDA_GATE_CHANNEL_F32) {
         const int M = kda::split_segments(num_seqs, H, d_k, d_v, chunk);
         const bool forced = kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
         if (forced && M < 3) return KDA_ERR_UNSUPPORTED;
@@ -152,6 +163,18 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v, const flo
     return kda::prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
                              d_k, d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, kernel,
                              stream);
+}
+
+kda_status kda_prefill_gates(const void* q, const void* k, const void* v, const void* alpha,
+                             kda_gate_format gate_format, const float* beta, const float* S0,
+                             const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                             int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                             int32_t chunk, void* o, float* S_T, void* workspace,
+                             size_t workspace_bytes, kda_prefill_kernel kernel,
+                             kda_stream_t stream) {
+    return kda::prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
+                             d_k, d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, kernel,
+                             stream, gate_format);
 }
 
 kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d_k, int32_t d_v,

@@ -45,7 +45,7 @@ struct PrefillArgs {
     const void* q;
     const void* k;
     const void* v;
-    const float* alpha;
+    const void* alpha;   // layout by gate (kda_gate_format)
     const float* beta;
     const float* S0;
     const int32_t* cu_seqlens;
@@ -59,6 +59,7 @@ struct PrefillArgs {
     int32_t* status;    // device
     int32_t* counter;   // device
     int32_t* order;     // device, [num_seqs]
+    int32_t gate = 0;   // kda_gate_format
 };
 
 struct DecodeArgs {
@@ -91,12 +92,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 int sm_count();   // of the current device, cached per device
 
 // Validation and dispatch behind kda_prefill / kda_prefill_ex (kda_api.cu).
-kda_status prefill_impl(const void* q, const void* k, const void* v, const float* alpha,
+kda_status prefill_impl(const void* q, const void* k, const void* v, const void* alpha,
                         const float* beta, const float* S0, const int32_t* cu_seqlens,
                         int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                         int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
                         void* workspace, size_t workspace_bytes, kda_prefill_kernel kernel,
-                        kda_stream_t stream);
+                        kda_stream_t stream, kda_gate_format gate = KDA_GATE_CHANNEL_F32);
 
 // ---- small device helpers ------------------------------------------------
 

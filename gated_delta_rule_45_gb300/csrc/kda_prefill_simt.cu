@@ -142,7 +142,7 @@ kda_prefill_simt_kernel(PrefillArgs a) {
             if (t < nvalid && r < rows) {
                 const size_t gi = ((size_t)(c0 + t) * H + h) * d_v + r0 + r;
                 vx = Elem<T>::load(v + gi);
-                ax = a.alpha[gi];
+                ax = static_cast<const float*>(a.alpha)[gi];
             }
             s.Xs[t * kDVP + r] = vx;
             s.Gs[t * kDVP + r] = ax;

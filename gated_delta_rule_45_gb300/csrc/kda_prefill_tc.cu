@@ -131,12 +131,19 @@ struct TcParams {
     int32_t n_base, n_base_p, s0_lo, s0_hi, st_lo, st_hi, a_ctas, num_items_p;
     float* g_out;
     float* P_out;
+    const float* alpha_s;   // GATE_SCALAR: alpha [T][H]
 };
 
 struct ItemInfo {
     int n, h, vb, len, nc;
     int64_t t0;
 };
+
+// Gate formats (the GATE template parameter): per value channel fp32 alpha
+// [T][H][d_v]; one fp32 gate per (token, head) [T][H] (Gated DeltaNet's
+// scalar gate, broadcast over the value channels); per value channel log alpha
+// in bf16 [T][H][d_v] (half the bytes of the largest prefill input).
+enum { GATE_F32 = 0, GATE_SCALAR = 1, GATE_LOG_BF16 = 2 };
 
 // SPLIT: the kernel serves the split launches (virtual sequences, transition
 // items); the plain instantiation compiles none of that.
@@ -266,7 +273,7 @@ __device__ __forceinline__ uint32_t kq_addr(const Ctx& cx, int s) {
 }
 
 // ------------------------------------------------------------------ producer
-template <bool SPLIT>
+template <bool SPLIT, int GATE>
 __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
     ChunkCursor<SPLIT> cur(p);
     cur.init(p);
@@ -288,6 +295,11 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
         float* bst = const_cast<float*>(beta_st) + s * C;
         for (int j = lane; j < C; j += 32)
             bst[j] = j < nvalid ? p.beta[(tok0 + j) * p.H + h] : 0.f;
+        if (GATE == GATE_SCALAR) {   // one gate per token rides with beta
+            float* ast = reinterpret_cast<float*>(cx.smem + SM_ALPHA) + s * C;
+            for (int j = lane; j < C; j += 32)
+                ast[j] = j < nvalid ? p.alpha_s[(tok0 + j) * p.H + h] : 1.f;
+        }
         __syncwarp();
         if (lane == 0) {
             uint64_t* bar = &cx.bars[B_KQ_FULL + s];
@@ -305,18 +317,20 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
             continue;
         }
         // alpha: one buffer, free once the row group has read it into registers
-        if (g >= 1) {
-            int r = 1;
-            if (lane == 0) r = wait1(cx, B_A_EMPTY, (g - 1) & 1);
-            __syncwarp();
-            if (!__shfl_sync(0xffffffffu, r, 0)) break;
+        if (GATE != GATE_SCALAR) {
+            if (g >= 1) {
+                int r = 1;
+                if (lane == 0) r = wait1(cx, B_A_EMPTY, (g - 1) & 1);
+                __syncwarp();
+                if (!__shfl_sync(0xffffffffu, r, 0)) break;
+            }
+            if (lane == 0) {
+                uint64_t* bar = &cx.bars[B_A_FULL];
+                mbar_arrive_expect_tx(bar, 64 * DVB * (GATE == GATE_LOG_BF16 ? 2 : 4));
+                tma_load_3d(cx.smem + SM_ALPHA, &p.tm_a, bar, cur.info.vb * DVB, h, (int32_t)tok0);
+            }
+            ++a_issued;
         }
-        if (lane == 0) {
-            uint64_t* bar = &cx.bars[B_A_FULL];
-            mbar_arrive_expect_tx(bar, 64 * DVB * 4);
-            tma_load_3d(cx.smem + SM_ALPHA, &p.tm_a, bar, cur.info.vb * DVB, h, (int32_t)tok0);
-        }
-        ++a_issued;
         // V: two buffers
         if (g >= 2) {
             int r = 1;
@@ -696,7 +710,7 @@ __device__ __forceinline__ void stage_state_piece(uint32_t lane_addr, int h, int
     tmem_st16(lane_addr + TM_SLO + 32 * h + 16 * q, lo);
 }
 
-template <bool SPLIT>
+template <bool SPLIT, int GATE>
 __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp, int lane) {
     const int quarter = warp & 3;
     const int h = rt >> 7;                 // token half / key-channel half
@@ -772,43 +786,57 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
 #pragma unroll
                 for (int j = 0; j < 32; ++j) vg[j] = 0.f;
             } else {
-                if (!(ok = warp_wait(cx, B_A_FULL, g & 1))) break;
                 float* half_tot = reinterpret_cast<float*>(cx.smem + SM_HALF);
                 // The tiles always hold finite values (TMA fills rows past the tensor
                 // with zeros; rows past the sequence belong to the next one), so the
                 // loads are unconditional and padded tokens are masked afterwards.
-                float a[32];
+                float a[32], inv[32];
+                if (GATE == GATE_SCALAR) {
+                    // one gate per token (padded tokens: 1), from the beta stage
+                    const float* ast = reinterpret_cast<const float*>(cx.smem + SM_ALPHA) + (g & 1) * C;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) a[j] = al[(32 * h + j) * DVB + r];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&cx.bars[B_A_EMPTY]);   // alpha is in registers
-                float run = 1.f;
+                    for (int j = 0; j < 32; ++j) a[j] = ast[32 * h + j];
+                } else {
+                    if (!(ok = warp_wait(cx, B_A_FULL, g & 1))) break;
+                    if (GATE == GATE_LOG_BF16) {   // alpha = exp(log alpha)
+                        const uint16_t* la = reinterpret_cast<const uint16_t*>(al);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    a[j] = 32 * h + j < nvalid ? a[j] : 1.f;
-                    run *= a[j];
-                    gam[j] = run;
-                }
-                half_tot[h * DVB + r] = run;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&cx.bars[B_PAIR + quarter]);
-                if (!(ok = warp_wait(cx, B_PAIR + quarter, g & 1))) break;
-                const float other = half_tot[(1 - h) * DVB + r];
-                if (h == 1) {
+                        for (int j = 0; j < 32; ++j) a[j] = __expf(bf2f(la[(32 * h + j) * DVB + r]));
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float2 gg = __fmul2_rn(make_float2(gam[j], gam[j + 1]),
-                                                     make_float2(other, other));
-                        gam[j] = gg.x;
-                        gam[j + 1] = gg.y;
+                        for (int j = 0; j < 32; ++j) a[j] = al[(32 * h + j) * DVB + r];
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.bars[B_A_EMPTY]);   // alpha is in registers
                 }
-                gC = h == 0 ? run * other : gam[31];
-                // 1 / gamma_t from one reciprocal and the products of the later alphas
-                float inv[32];
-                inv[31] = __frcp_rn(gam[31]);
+                {
+                    float run = 1.f;
 #pragma unroll
-                for (int j = 30; j >= 0; --j) inv[j] = inv[j + 1] * a[j + 1];
+                    for (int j = 0; j < 32; ++j) {
+                        a[j] = 32 * h + j < nvalid ? a[j] : 1.f;
+                        run *= a[j];
+                        gam[j] = run;
+                    }
+                    half_tot[h * DVB + r] = run;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.bars[B_PAIR + quarter]);
+                    if (!(ok = warp_wait(cx, B_PAIR + quarter, g & 1))) break;
+                    const float other = half_tot[(1 - h) * DVB + r];
+                    if (h == 1) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            const float2 gg = __fmul2_rn(make_float2(gam[j], gam[j + 1]),
+                                                         make_float2(other, other));
+                            gam[j] = gg.x;
+                            gam[j + 1] = gg.y;
+                        }
+                    }
+                    gC = h == 0 ? run * other : gam[31];
+                    // 1 / gamma_t from one reciprocal and the products of the later alphas
+                    inv[31] = __frcp_rn(gam[31]);
+#pragma unroll
+                    for (int j = 30; j >= 0; --j) inv[j] = inv[j + 1] * a[j + 1];
+                }
                 if (!(ok = warp_wait(cx, B_V_FULL + (g & 1), (g >> 1) & 1))) break;
                 const uint16_t* vs =
                     reinterpret_cast<const uint16_t*>(cx.smem + ((g & 1) ? SM_V1 : SM_V));
@@ -982,7 +1010,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool SPLIT>
+template <bool SPLIT, int GATE>
 __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __grid_constant__ TcParams p) {
     if (*p.status != 0) return;   // planner rejected cu_seqlens
     extern __shared__ uint8_t smem_raw[];
@@ -1020,13 +1048,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     cx.tmem = *tslot;
 
     if (warp == 0) {
-        run_producer<SPLIT>(p, cx, lane);
+        run_producer<SPLIT, GATE>(p, cx, lane);
     } else if (warp == 1) {
         run_mma<SPLIT>(p, cx);
     } else if (warp >= 2 && warp < 6) {
         run_token_group<SPLIT>(p, cx, tid - 64, warp, lane);
     } else {
-        run_row_group<SPLIT>(p, cx, tid - 192, warp, lane);
+        run_row_group<SPLIT, GATE>(p, cx, tid - 192, warp, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -1072,9 +1100,15 @@ bool init_params(const PrefillArgs& a, TcParams& p) {
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, a.d_v,
                   DVB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&p.tm_a, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.total_tokens, a.H,
-                  a.d_v, DVB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        (a.gate == GATE_F32 &&
+         !make_map(&p.tm_a, a.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.total_tokens, a.H,
+                   a.d_v, DVB, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+        (a.gate == GATE_LOG_BF16 &&
+         !make_map(&p.tm_a, a.alpha, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H,
+                   a.d_v, DVB, CU_TENSOR_MAP_SWIZZLE_NONE)))
         return false;
+    if (a.gate == GATE_SCALAR) p.tm_a = p.tm_v;   // not read; a valid map to prefetch
+    p.alpha_s = static_cast<const float*>(a.alpha);
     p.beta = a.beta;
     p.S0 = a.S0;
     p.S_T = a.S_T;
@@ -1100,14 +1134,19 @@ bool init_params(const PrefillArgs& a, TcParams& p) {
     return true;
 }
 
-template <bool SPLIT>
-cudaError_t launch(TcParams& p, int grid, cudaStream_t stream) {
-    cudaError_t err = cudaFuncSetAttribute(kda_prefill_tc_kernel<SPLIT>,
+template <bool SPLIT, int GATE>
+cudaError_t launch_g(TcParams& p, int grid, cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(kda_prefill_tc_kernel<SPLIT, GATE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    kda_prefill_tc_kernel<SPLIT><<<grid, kThreads, SMEM_BYTES, stream>>>(p);
+    kda_prefill_tc_kernel<SPLIT, GATE><<<grid, kThreads, SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <bool SPLIT>
+cudaError_t launch(TcParams& p, int grid, cudaStream_t stream) {
+    return launch_g<SPLIT, GATE_F32>(p, grid, stream);
 }
 
 }  // namespace
@@ -1128,12 +1167,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     const int sms = sm_count();
     const int grid = p.num_items < sms ? p.num_items : sms;
     p.a_ctas = grid;
-    return launch<false>(p, grid, stream);
+    switch (a.gate) {
+        case GATE_F32: return launch_g<false, GATE_F32>(p, grid, stream);
+        case GATE_SCALAR: return launch_g<false, GATE_SCALAR>(p, grid, stream);
+        case GATE_LOG_BF16: return launch_g<false, GATE_LOG_BF16>(p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, char* ws,
                                     cudaStream_t stream) {
-    if (!prefill_tc_supports(a) || L.M < 3) return cudaErrorInvalidValue;
+    if (!prefill_tc_supports(a) || L.M < 3 || a.gate != GATE_F32) return cudaErrorInvalidValue;
     if (a.total_tokens == 0 || a.num_seqs == 0) return launch_prefill_tc(a, stream);
     TcParams p;
     if (!init_params(a, p)) return cudaErrorInvalidValue;

@@ -25,6 +25,11 @@ BF16, FP32 = 0, 1
 KERNEL_AUTO, KERNEL_CHUNK_SIMT, KERNEL_CHUNK_TC, KERNEL_CHUNK_TC_SPLIT = 0, 1, 2, 3
 _KERNELS = {"auto": KERNEL_AUTO, "simt": KERNEL_CHUNK_SIMT, "tc": KERNEL_CHUNK_TC,
             "tc_split": KERNEL_CHUNK_TC_SPLIT}
+GATE_CHANNEL_F32, GATE_HEAD_F32, GATE_CHANNEL_LOG_BF16 = 0, 1, 2
+# gate layout -> (code, dtype, alpha tensor rank)
+_GATES = {"channel": (GATE_CHANNEL_F32, torch.float32, 3),
+          "head": (GATE_HEAD_F32, torch.float32, 2),
+          "log_bf16": (GATE_CHANNEL_LOG_BF16, torch.bfloat16, 3)}
 
 _lib = None
 
@@ -54,6 +59,9 @@ def load(path: str | None = None):
     lib.kda_prefill.argtypes = prefill_args + [vp]
     lib.kda_prefill_ex.restype = ctypes.c_int
     lib.kda_prefill_ex.argtypes = prefill_args + [ctypes.c_int, vp]
+    lib.kda_prefill_gates.restype = ctypes.c_int
+    lib.kda_prefill_gates.argtypes = [vp, vp, vp, vp, ctypes.c_int] + prefill_args[4:] + \
+        [ctypes.c_int, vp]
     lib.kda_prefill_noalloc.restype = ctypes.c_int
     lib.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                         ctypes.c_int, i32, vp, vp, vp]
@@ -140,6 +148,51 @@ def prefill_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace, *, chu
                                _stream_ptr(stream))
     if st != OK:
         raise KdaError(st, "kda_prefill")
+
+
+def prefill_gates_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace, *,
+                       gate: str = "channel", chunk: int = 64, kernel: str = "auto",
+                       stream=None) -> None:
+    """Enqueue kda_prefill_gates: as prefill_into with the forget gate in layout `gate`:
+    "channel" alpha [T, H, d_v] fp32, "head" alpha [T, H] fp32 (one gate per head),
+    "log_bf16" log alpha [T, H, d_v] bf16."""
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace)
+    code, adt, arank = _GATES[gate]
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if alpha.dtype != adt or alpha.dim() != arank:
+        raise TypeError(f"gate layout {gate!r} wants a rank-{arank} {adt} tensor")
+    if cu_seqlens.dtype != torch.int32 or beta.dtype != torch.float32:
+        raise TypeError("cu_seqlens must be int32 and beta float32")
+    if S_T.dtype != torch.float32 or (S0 is not None and S0.dtype != torch.float32):
+        raise TypeError("states must be float32")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype:
+        raise TypeError("q, k, v and o must share one dtype")
+    st = load().kda_prefill_gates(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), code, _ptr(beta),
+                                  _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v, dt, chunk,
+                                  _ptr(o), _ptr(S_T), _ptr(workspace), workspace.numel(),
+                                  _KERNELS[kernel], _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_prefill_gates")
+
+
+def prefill_gates(q, k, v, alpha, beta, S0, cu_seqlens, *, gate: str = "channel",
+                  chunk: int = 64, kernel: str = "auto", stream=None,
+                  check_device_status: bool = False):
+    """Allocate outputs with PyTorch and run kda_prefill_gates; returns (o, S_T)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
+    S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=q.device)
+    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk), dtype=torch.uint8, device=q.device)
+    prefill_gates_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, ws, gate=gate, chunk=chunk,
+                       kernel=kernel, stream=stream)
+    if check_device_status:
+        device_status(ws, stream=stream)
+    return o, S_T
 
 
 def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64, kernel: str = "auto",

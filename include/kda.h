@@ -87,6 +87,16 @@ typedef enum {
 
 typedef void* kda_stream_t;   /* a cudaStream_t */
 
+/* Layout of the forget gate for kda_prefill_gates. */
+typedef enum {
+    KDA_GATE_CHANNEL_F32 = 0,   /* alpha [T][H][d_v] fp32 in (0, 1] (kda_prefill's) */
+    KDA_GATE_HEAD_F32 = 1,      /* alpha [T][H] fp32 in (0, 1]: one gate per token and
+                                   head, the same for every value channel (the scalar
+                                   gate of Gated DeltaNet) */
+    KDA_GATE_CHANNEL_LOG_BF16 = 2   /* log alpha [T][H][d_v] bfloat16, <= 0: half the
+                                       bytes of the fp32 gate */
+} kda_gate_format;
+
 /*
  * Bytes of device workspace kda_prefill needs for `num_seqs` sequences of H
  * heads with these sizes.  Returns 0 for num_seqs < 0.  The workspace holds
@@ -146,6 +156,24 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v,
                           int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype, int32_t chunk,
                           void* o, float* S_T, void* workspace, size_t workspace_bytes,
                           kda_prefill_kernel kernel, kda_stream_t stream);
+
+/*
+ * kda_prefill_ex with the forget gate in another layout (kda_gate_format):
+ * `alpha` points to the gate in that layout; everything else as kda_prefill_ex.
+ * The recurrence is the same with alpha_t[r] = alpha[t][h] (KDA_GATE_HEAD_F32)
+ * or exp(log_alpha[t][h][r]) (KDA_GATE_CHANNEL_LOG_BF16).  The two new
+ * layouts run on the tensor-core kernel only (without the sequence-axis
+ * split): other shapes, or kernel == KDA_KERNEL_CHUNK_SIMT or
+ * KDA_KERNEL_CHUNK_TC_SPLIT, return KDA_ERR_UNSUPPORTED.
+ * KDA_GATE_CHANNEL_F32 is exactly kda_prefill_ex.
+ */
+kda_status kda_prefill_gates(const void* q, const void* k, const void* v, const void* alpha,
+                             kda_gate_format gate_format, const float* beta, const float* S0,
+                             const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                             int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                             int32_t chunk, void* o, float* S_T, void* workspace,
+                             size_t workspace_bytes, kda_prefill_kernel kernel,
+                             kda_stream_t stream);
 
 /*
  * Whether `kernel` covers a prefill of this shape: KDA_OK if kda_prefill_ex

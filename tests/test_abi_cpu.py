@@ -144,3 +144,37 @@ def test_binding_fails_loudly_without_library(tmp_path):
     from gated_delta_rule_45_gb300 import kda
     with pytest.raises(RuntimeError, match="libkda.so not found"):
         kda.load(str(tmp_path / "missing.so"))
+
+
+def _prefill_gates(lib, **kw):
+    args = dict(q=_fake(0x10000), k=_fake(0x20000), v=_fake(0x30000), alpha=_fake(0x40000),
+                gate=1, beta=_fake(0x50000), S0=None, cu=_fake(0x60000), N=2, T=64, H=2,
+                d_k=128, d_v=128, dtype=0, chunk=64, o=_fake(0x700000), S_T=_fake(0x800000),
+                ws=_fake(0x900000), ws_bytes=4096, kernel=0)
+    args.update(kw)
+    return lib.kda_prefill_gates(args["q"], args["k"], args["v"], args["alpha"], args["gate"],
+                                 args["beta"], args["S0"], args["cu"], args["N"], args["T"],
+                                 args["H"], args["d_k"], args["d_v"], args["dtype"],
+                                 args["chunk"], args["o"], args["S_T"], args["ws"],
+                                 args["ws_bytes"], args["kernel"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(gate=7), 1),                      # unknown gate layout
+    (dict(gate=1, kernel=1), 2),            # other layouts: tensor-core kernel only
+    (dict(gate=2, kernel=1), 2),
+    (dict(gate=1, kernel=3), 2),            # ... and never split
+    (dict(gate=1, d_k=64), 2),              # not a tensor-core shape
+    (dict(gate=2, dtype=1), 2),             # fp32 storage: not a tensor-core shape
+    (dict(gate=1, alpha=None), 1),
+    (dict(gate=2, alpha=_fake(0x10002)), 1),   # misaligned
+    # o may not overlap the gate, whose size depends on its layout
+    (dict(gate=2, o=_fake(0x40000 + 16384)), 1),
+    (dict(gate=1, o=_fake(0x40000 + 256)), 1),
+])
+def test_prefill_gates_rejects_on_host(lib, kw, expect):
+    assert _prefill_gates(lib, **kw) == expect
+
+
+def test_prefill_ex_split_needs_a_tensor_core_shape(lib):
+    assert _prefill(lib, kernel=3, d_k=64) == 2

@@ -215,3 +215,30 @@ def test_sequence_split_in_place_state():
     ref = parity.oracle_pairs(d, [(n, h) for n in range(2) for h in range(2)])
     wo, wsr = parity.compare_pairs(d, o, S, ref)
     assert wo <= parity.TOL_BF16 and wsr <= parity.TOL_BF16, (wo, wsr)
+
+
+@pytest.mark.parametrize("gate,d_v", [("head", 256), ("log_bf16", 128), ("channel", 128)])
+def test_gate_layouts_match_oracle(gate, d_v):
+    """kda_prefill_gates: one gate per (token, head) broadcast over the value
+    channels (Gated DeltaNet's scalar gate), and log alpha in bf16; the oracle
+    gets the same gates as alpha[t][h][r] (exp taken in float64)."""
+    spec = synth.PrefillSpec(num_seqs=3, len_lo=60, len_hi=500, H=2, d_k=128, d_v=d_v,
+                             s0_std=0.1, seed=31)
+    d = synth.prefill_inputs(spec)
+    T = int(d["cu_seqlens"][-1])
+    gen = torch.Generator().manual_seed(32)
+    if gate == "head":
+        g_in = torch.sigmoid(torch.randn(T, spec.H, generator=gen) + 3.0)
+        d["alpha"] = g_in[:, :, None].expand(T, spec.H, d_v).contiguous()
+    elif gate == "log_bf16":
+        g_in = torch.log(torch.sigmoid(torch.randn(T, spec.H, d_v, generator=gen) + 3.0))
+        g_in = g_in.to(torch.bfloat16)
+        d["alpha"] = torch.exp(g_in.double()).float()
+    else:
+        g_in = d["alpha"]
+    dev = parity.to_device(d)
+    o, S_T = kda.prefill_gates(dev["q"], dev["k"], dev["v"], g_in.cuda(), dev["beta"], dev["S0"],
+                               dev["cu_seqlens"], gate=gate, check_device_status=True)
+    ref = parity.oracle_pairs(d, [(n, h) for n in range(spec.num_seqs) for h in range(spec.H)])
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (gate, wo, ws)
