@@ -60,8 +60,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_ERR_UNSUPPORTED;
     if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
     if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
-    if (gate != KDA_GATE_CHANNEL_F32 &&
-        (kernel == KDA_KERNEL_CHUNK_SIMT || kernel == KDA_KERNEL_CHUNK_TC_SPLIT))
+    if (gate != KDA_GATE_CHANNEL_F32 && kernel == KDA_KERNEL_CHUNK_TC_SPLIT)
         return KDA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * H > (int64_t)INT32_MAX / 64) return KDA_ERR_UNSUPPORTED;
     if (!cu_seqlens || !workspace || (num_seqs > 0 && !S_T)) return KDA_ERR_INVALID_ARG;
@@ -100,8 +99,6 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     const bool tc_ok = kda::prefill_tc_supports(a);
     const bool want_tc = kernel == KDA_KERNEL_CHUNK_TC || kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
     if (want_tc && !tc_ok) return KDA_ERR_UNSUPPORTED;
-    // the other gate layouts run on the tensor-core kernel only, unsplit
-    if (gate != KDA_GATE_CHANNEL_F32 && !tc_ok) return KDA_ERR_UNSUPPORTED;
     const bool use_tc = want_tc || (kernel == KDA_KERNEL_AUTO && tc_ok);
     // sequence-axis split: few chains, long sequences, room in the workspace
     kda::SplitLayout split;
@@ -204,10 +201,15 @@ kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream)
     return st == KDA_ERR_DEVICE_TIMEOUT ? KDA_ERR_DEVICE_TIMEOUT : KDA_ERR_DEVICE_INPUT;
 }
 
-kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* alpha,
-                           const float* beta, float* S, int32_t B, int32_t H, int32_t d_k,
-                           int32_t d_v, kda_dtype dtype, void* o, kda_stream_t stream) {
+// Validation and launch behind kda_decode_step / kda_decode_step_gates.
+static kda_status decode_impl(const void* q, const void* k, const void* v, const void* alpha,
+                              kda_gate_format gate, const float* beta, float* S, int32_t B,
+                              int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype, void* o,
+                              kda_stream_t stream) {
     if (B < 0 || H < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+    if (gate != KDA_GATE_CHANNEL_F32 && gate != KDA_GATE_HEAD_F32 &&
+        gate != KDA_GATE_CHANNEL_LOG_BF16)
+        return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (d_k != 16 && d_k != 32 && d_k != 64 && d_k != 128 && d_k != 256)
         return KDA_ERR_UNSUPPORTED;
@@ -222,9 +224,11 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const fl
     const size_t n_s = (size_t)B * H * d_v * d_k * sizeof(float);
     const size_t n_o = (size_t)B * H * d_v * esz;
     const void* ins[] = {q, k, v, alpha, beta};
+    const size_t n_a = gate == KDA_GATE_HEAD_F32 ? (size_t)B * H * sizeof(float)
+                       : gate == KDA_GATE_CHANNEL_LOG_BF16 ? (size_t)B * H * d_v * 2
+                                                           : (size_t)B * H * d_v * sizeof(float);
     const size_t in_n[] = {(size_t)B * H * d_k * esz, (size_t)B * H * d_k * esz,
-                           (size_t)B * H * d_v * esz, (size_t)B * H * d_v * sizeof(float),
-                           (size_t)B * H * sizeof(float)};
+                           (size_t)B * H * d_v * esz, n_a, (size_t)B * H * sizeof(float)};
     for (int i = 0; i < 5; ++i)
         if (overlaps(S, n_s, ins[i], in_n[i]) || overlaps(o, n_o, ins[i], in_n[i]))
             return KDA_ERR_INVALID_ARG;
@@ -232,10 +236,25 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const fl
 
     kda::DecodeArgs a;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S = S;
-    a.B = B; a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.o = o;
+    a.B = B; a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.o = o; a.gate = gate;
     return kda::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KDA_OK
                : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* alpha,
+                           const float* beta, float* S, int32_t B, int32_t H, int32_t d_k,
+                           int32_t d_v, kda_dtype dtype, void* o, kda_stream_t stream) {
+    return decode_impl(q, k, v, alpha, KDA_GATE_CHANNEL_F32, beta, S, B, H, d_k, d_v, dtype,
+                            o, stream);
+}
+
+kda_status kda_decode_step_gates(const void* q, const void* k, const void* v, const void* alpha,
+                                 kda_gate_format gate_format, const float* beta, float* S,
+                                 int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                                 void* o, kda_stream_t stream) {
+    return decode_impl(q, k, v, alpha, gate_format, beta, S, B, H, d_k, d_v, dtype, o,
+                            stream);
 }
 
 const char* kda_status_string(kda_status s) {

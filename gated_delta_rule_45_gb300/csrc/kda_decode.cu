@@ -37,10 +37,20 @@ __device__ __forceinline__ float group_sum(float x) {
     return x;
 }
 
-template <int DK, typename T>
+// GATE: the layout of the forget gate (kda_gate_format): alpha[b][h][r] fp32,
+// alpha[b][h] fp32 for every row, or exp(log_alpha[b][h][r]) from bf16.
+template <int GATE>
+__device__ __forceinline__ float gate_of(const void* alpha, int bh, size_t vi) {
+    if (GATE == KDA_GATE_HEAD_F32) return static_cast<const float*>(alpha)[bh];
+    if (GATE == KDA_GATE_CHANNEL_LOG_BF16)
+        return __expf(__bfloat162float(static_cast<const __nv_bfloat16*>(alpha)[vi]));
+    return static_cast<const float*>(alpha)[vi];
+}
+
+template <int DK, typename T, int GATE>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                  const float* __restrict__ alpha, const float* __restrict__ beta,
+                  const void* __restrict__ alpha, const float* __restrict__ beta,
                   float* __restrict__ S, int32_t H, int32_t d_v, T* __restrict__ o) {
     using Sh = DecodeShape<DK>;
     const int bh = blockIdx.x;                  // b * H + h
@@ -93,7 +103,7 @@ kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         pb = group_sum<Sh::LPR>(pb);
         if (r < d_v) {
             const size_t vi = (size_t)bh * d_v + r;
-            const float al = alpha[vi];
+            const float al = gate_of<GATE>(alpha, bh, vi);
             const float err = bt * (Elem<T>::load(v + vi) - al * pa);
             float4* dst = reinterpret_cast<float4*>(S + vi * DK);
 #pragma unroll
@@ -110,14 +120,25 @@ kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     }
 }
 
-template <int DK, typename T>
-cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+template <int DK, typename T, int GATE>
+cudaError_t launch_decode_g(const DecodeArgs& a, cudaStream_t stream) {
     using Sh = DecodeShape<DK>;
     dim3 grid(a.B * a.H, (a.d_v + Sh::ROWS_PER_CTA - 1) / Sh::ROWS_PER_CTA);
-    kda_decode_kernel<DK, T><<<grid, kDecodeWarps * 32, 0, stream>>>(
+    kda_decode_kernel<DK, T, GATE><<<grid, kDecodeWarps * 32, 0, stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         a.alpha, a.beta, a.S, a.H, a.d_v, static_cast<T*>(a.o));
     return cudaGetLastError();
+}
+
+template <int DK, typename T>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+    switch (a.gate) {
+        case KDA_GATE_CHANNEL_F32: return launch_decode_g<DK, T, KDA_GATE_CHANNEL_F32>(a, stream);
+        case KDA_GATE_HEAD_F32: return launch_decode_g<DK, T, KDA_GATE_HEAD_F32>(a, stream);
+        case KDA_GATE_CHANNEL_LOG_BF16:
+            return launch_decode_g<DK, T, KDA_GATE_CHANNEL_LOG_BF16>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <typename T>

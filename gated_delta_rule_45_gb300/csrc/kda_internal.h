@@ -66,12 +66,13 @@ struct DecodeArgs {
     const void* q;
     const void* k;
     const void* v;
-    const float* alpha;
+    const void* alpha;   // layout by gate (kda_gate_format)
     const float* beta;
     float* S;
     int32_t B, H, d_k, d_v;
     kda_dtype dtype;
     void* o;
+    int32_t gate = 0;    // kda_gate_format
 };
 
 // Launchers; each returns the CUDA error of its launch.

@@ -142,7 +142,12 @@ kda_prefill_simt_kernel(PrefillArgs a) {
             if (t < nvalid && r < rows) {
                 const size_t gi = ((size_t)(c0 + t) * H + h) * d_v + r0 + r;
                 vx = Elem<T>::load(v + gi);
-                ax = static_cast<const float*>(a.alpha)[gi];
+                if (a.gate == KDA_GATE_HEAD_F32)   // one gate per (token, head)
+                    ax = static_cast<const float*>(a.alpha)[(size_t)(c0 + t) * H + h];
+                else if (a.gate == KDA_GATE_CHANNEL_LOG_BF16)
+                    ax = __expf(__bfloat162float(static_cast<const __nv_bfloat16*>(a.alpha)[gi]));
+                else
+                    ax = static_cast<const float*>(a.alpha)[gi];
             }
             s.Xs[t * kDVP + r] = vx;
             s.Gs[t * kDVP + r] = ax;

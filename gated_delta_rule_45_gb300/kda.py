@@ -72,6 +72,9 @@ def load(path: str | None = None):
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
                                     vp, vp]
+    lib.kda_decode_step_gates.restype = ctypes.c_int
+    lib.kda_decode_step_gates.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, i32, i32, i32,
+                                          i32, ctypes.c_int, vp, vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_version.restype = i32
@@ -255,4 +258,26 @@ def decode_step(q, k, v, alpha, beta, S, o=None, *, stream=None):
                                 B, H, d_k, d_v, dt, _ptr(o), _stream_ptr(stream))
     if st != OK:
         raise KdaError(st, "kda_decode_step")
+    return o
+
+
+def decode_step_gates(q, k, v, alpha, beta, S, o=None, *, gate: str = "channel", stream=None):
+    """kda_decode_step_gates: decode_step with the forget gate in layout `gate`
+    ("channel" alpha [B, H, d_v] fp32, "head" alpha [B, H] fp32, "log_bf16" log
+    alpha [B, H, d_v] bf16); S updated in place; returns o [B, H, d_v]."""
+    code, adt, arank = _GATES[gate]
+    B, H, d_k = q.shape
+    d_v = v.shape[2]
+    if o is None:
+        o = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
+    _check_cuda(q, k, v, alpha, beta, S, o)
+    if alpha.dtype != adt or alpha.dim() != arank:
+        raise TypeError(f"gate layout {gate!r} wants a rank-{arank} {adt} tensor")
+    if S.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("S and beta must be float32")
+    dt = _dtype_code(q)
+    st = load().kda_decode_step_gates(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), code, _ptr(beta),
+                                      _ptr(S), B, H, d_k, d_v, dt, _ptr(o), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_decode_step_gates")
     return o

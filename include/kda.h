@@ -161,10 +161,9 @@ kda_status kda_prefill_ex(const void* q, const void* k, const void* v,
  * kda_prefill_ex with the forget gate in another layout (kda_gate_format):
  * `alpha` points to the gate in that layout; everything else as kda_prefill_ex.
  * The recurrence is the same with alpha_t[r] = alpha[t][h] (KDA_GATE_HEAD_F32)
- * or exp(log_alpha[t][h][r]) (KDA_GATE_CHANNEL_LOG_BF16).  The two new
- * layouts run on the tensor-core kernel only (without the sequence-axis
- * split): other shapes, or kernel == KDA_KERNEL_CHUNK_SIMT or
- * KDA_KERNEL_CHUNK_TC_SPLIT, return KDA_ERR_UNSUPPORTED.
+ * or exp(log_alpha[t][h][r]) (KDA_GATE_CHANNEL_LOG_BF16).  Every shape
+ * kda_prefill_ex supports; the sequence-axis split is not used with the two
+ * new layouts (KDA_KERNEL_CHUNK_TC_SPLIT returns KDA_ERR_UNSUPPORTED).
  * KDA_GATE_CHANNEL_F32 is exactly kda_prefill_ex.
  */
 kda_status kda_prefill_gates(const void* q, const void* k, const void* v, const void* alpha,
@@ -240,6 +239,15 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v,
                            const float* alpha, const float* beta, float* S,
                            int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
                            void* o, kda_stream_t stream);
+
+/* kda_decode_step with the forget gate in another layout (kda_gate_format):
+ * alpha [B][H] fp32 (KDA_GATE_HEAD_F32) or log alpha [B][H][d_v] bf16
+ * (KDA_GATE_CHANNEL_LOG_BF16); every shape kda_decode_step supports. */
+kda_status kda_decode_step_gates(const void* q, const void* k, const void* v,
+                                 const void* alpha, kda_gate_format gate_format,
+                                 const float* beta, float* S, int32_t B, int32_t H,
+                                 int32_t d_k, int32_t d_v, kda_dtype dtype, void* o,
+                                 kda_stream_t stream);
 
 /* Static description of a status code.  Never NULL. */
 const char* kda_status_string(kda_status s);

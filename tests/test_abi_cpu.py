@@ -161,11 +161,9 @@ def _prefill_gates(lib, **kw):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(gate=7), 1),                      # unknown gate layout
-    (dict(gate=1, kernel=1), 2),            # other layouts: tensor-core kernel only
-    (dict(gate=2, kernel=1), 2),
-    (dict(gate=1, kernel=3), 2),            # ... and never split
-    (dict(gate=1, d_k=64), 2),              # not a tensor-core shape
-    (dict(gate=2, dtype=1), 2),             # fp32 storage: not a tensor-core shape
+    (dict(gate=1, kernel=3), 2),            # the other layouts never split
+    (dict(gate=2, kernel=3), 2),
+    (dict(gate=1, d_k=130), 2),             # not a supported shape at all
     (dict(gate=1, alpha=None), 1),
     (dict(gate=2, alpha=_fake(0x10002)), 1),   # misaligned
     # o may not overlap the gate, whose size depends on its layout
@@ -178,3 +176,14 @@ def test_prefill_gates_rejects_on_host(lib, kw, expect):
 
 def test_prefill_ex_split_needs_a_tensor_core_shape(lib):
     assert _prefill(lib, kernel=3, d_k=64) == 2
+
+
+def test_decode_gates_rejects_on_host(lib):
+    def call(gate, alpha=_fake(0x40000), o=_fake(0x900000)):
+        return lib.kda_decode_step_gates(_fake(0x10000), _fake(0x20000), _fake(0x30000), alpha,
+                                         gate, _fake(0x50000), _fake(0x100000), 2, 2, 128, 128,
+                                         0, o, None)
+    assert call(9) == 1                          # unknown layout
+    assert call(1, alpha=None) == 1
+    assert call(2, alpha=_fake(0x40008)) == 1    # misaligned
+    assert call(1, o=_fake(0x40000)) == 1        # o overlaps the [B][H] gate

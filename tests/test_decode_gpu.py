@@ -68,3 +68,32 @@ def test_decode_state_only_in_place():
     torch.cuda.synchronize()
     assert torch.all(buf[:1024] == 7.0) and torch.all(buf[1024 + n_s:] == 7.0)
     assert torch.all(obuf[:128] == 3.0) and torch.all(obuf[128 + 192:] == 3.0)
+
+
+@pytest.mark.parametrize("gate,d_k,d_v", [("head", 128, 128), ("log_bf16", 128, 256),
+                                          ("head", 64, 80)])
+def test_decode_gate_layouts(gate, d_k, d_v):
+    """kda_decode_step_gates against the oracle with the gates expanded to
+    alpha[b][h][r] (exp taken in float64)."""
+    spec = synth.DecodeSpec(B=5, H=3, d_k=d_k, d_v=d_v, seed=41)
+    d = synth.decode_inputs(spec)
+    gen = torch.Generator().manual_seed(42)
+    if gate == "head":
+        g_in = torch.sigmoid(torch.randn(spec.B, spec.H, generator=gen) + 4.0)
+        alpha = g_in[:, :, None].expand(spec.B, spec.H, d_v).contiguous()
+    else:
+        g_in = torch.log(torch.sigmoid(torch.randn(spec.B, spec.H, d_v, generator=gen) + 4.0))
+        g_in = g_in.to(torch.bfloat16)
+        alpha = torch.exp(g_in.double()).float()
+    dev = parity.to_device(d)
+    S = dev["S"].clone()
+    o = kda.decode_step_gates(dev["q"], dev["k"], dev["v"], g_in.cuda(), dev["beta"], S,
+                              gate=gate)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.decode_step(*(parity._np(d[x]) for x in ("q", "k", "v")),
+                                      alpha.numpy(), d["beta"].numpy(), d["S"].double().numpy())
+    o_g, S_g = o.float().cpu().numpy(), S.cpu().numpy()
+    worst_o = max(max(parity.rel_gate(o_g[b, h], o_ref[b, h], torch.bfloat16)
+                      for b in range(spec.B) for h in range(spec.H)), parity.rel(o_g, o_ref))
+    worst_s = max(parity.rel(S_g[b, h], S_ref[b, h]) for b in range(spec.B) for h in range(spec.H))
+    assert worst_o <= parity.TOL_BF16 and worst_s <= parity.TOL_BF16, (worst_o, worst_s)

@@ -242,3 +242,27 @@ def test_gate_layouts_match_oracle(gate, d_v):
     ref = parity.oracle_pairs(d, [(n, h) for n in range(spec.num_seqs) for h in range(spec.H)])
     wo, ws = parity.compare_pairs(d, o, S_T, ref)
     assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (gate, wo, ws)
+
+
+@pytest.mark.parametrize("gate", ["head", "log_bf16"])
+def test_gate_layouts_on_the_portable_kernel(gate):
+    """The gate layouts on the fp32 CUDA-core kernel (d_k = 64, fp32 storage, chunk 32)."""
+    spec = synth.PrefillSpec(num_seqs=2, len_lo=40, len_hi=200, H=2, d_k=64, d_v=48,
+                             dtype="fp32", chunk=32, s0_std=0.1, seed=33)
+    d = synth.prefill_inputs(spec)
+    T = int(d["cu_seqlens"][-1])
+    gen = torch.Generator().manual_seed(34)
+    if gate == "head":
+        g_in = torch.sigmoid(torch.randn(T, spec.H, generator=gen) + 3.0)
+        d["alpha"] = g_in[:, :, None].expand(T, spec.H, spec.d_v).contiguous()
+    else:
+        g_in = torch.log(torch.sigmoid(torch.randn(T, spec.H, spec.d_v, generator=gen) + 3.0))
+        g_in = g_in.to(torch.bfloat16)
+        d["alpha"] = torch.exp(g_in.double()).float()
+    dev = parity.to_device(d)
+    o, S_T = kda.prefill_gates(dev["q"], dev["k"], dev["v"], g_in.cuda(), dev["beta"], dev["S0"],
+                               dev["cu_seqlens"], gate=gate, chunk=32, kernel="simt",
+                               check_device_status=True)
+    ref = parity.oracle_pairs(d, [(n, h) for n in range(spec.num_seqs) for h in range(spec.H)])
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    assert wo <= 1e-4 and ws <= 1e-4, (gate, wo, ws)
