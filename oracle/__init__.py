@@ -5,11 +5,14 @@ CPU-baseline / reference arm of ``bench.py`` may import this package.  The
 CUDA product path never imports, links or calls it, and it imports nothing
 from the product package.
 
-Two independent forms live here:
+Three forms live here, each written independently of the others:
 
 * ``prefill`` -- the C library ``kda_oracle.c``: the page's three-line update
   (forget gating, predict, memory updating) and o_t = S_t q_t, one token at a
   time in fp64 ("Kimi (AI)", section "Kimi Delta Attention (KDA)").
+* ``backward`` -- the same C library, reverse mode of that update: the
+  gradients of sum(dO * o) + sum(dS_T * S_T) with respect to q, k, v, alpha,
+  beta and S0, one token at a time in fp64.
 * ``dense_form.run`` -- numpy, tiny sizes only: the same recurrence expanded
   into one explicit matrix product per step,
   S_t = diag(alpha_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T.
@@ -60,6 +63,9 @@ def load(path: str | None = None):
     lib.kda_oracle_prefill.restype = ctypes.c_int
     lib.kda_oracle_prefill.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, i32, i64,
                                        i32, i32, i32, vp, vp, i32]
+    lib.kda_oracle_backward.restype = ctypes.c_int
+    lib.kda_oracle_backward.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, i32, i64,
+                                        i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32]
     lib.kda_oracle_max_threads.restype = ctypes.c_int
     lib.kda_oracle_max_threads.argtypes = []
     if path is None:
@@ -115,6 +121,58 @@ def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, nthreads: int = 0, lib=None
     if rc != 0:
         raise ValueError("kda_oracle_prefill failed with code %d" % rc)
     return o, S_T
+
+
+def backward(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, nthreads: int = 0,
+             lib=None):
+    """Gradients of L = sum(dO * o) + sum(dS_T * S_T) for the batch ``prefill`` runs.
+
+    Inputs as for ``prefill``; dO: [T_total, H, d_v] and dS_T: [N, H, d_v, d_k]
+    or None (zeros), any float type, widened to fp64.  Returns a dict of fp64
+    arrays: dq, dk [T_total, H, d_k]; dv, dalpha [T_total, H, d_v];
+    dbeta [T_total, H]; dS0 [N, H, d_v, d_k].  Reverse mode of the page's
+    three-line update, one token at a time ("Kimi (AI)", section "Kimi Delta
+    Attention (KDA)"); see ``kda_oracle_backward`` in ``kda_oracle.c``.
+    """
+    lib = lib or load()
+    q, kind = _as_qkv(q)
+    k, kind_k = _as_qkv(k)
+    v, kind_v = _as_qkv(v)
+    if not (kind == kind_k == kind_v):
+        raise TypeError("q, k and v must share one storage type")
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    alpha = np.ascontiguousarray(alpha, dtype=np.float32)
+    beta = np.ascontiguousarray(beta, dtype=np.float32)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    N = cu.shape[0] - 1
+    if k.shape != (T, H, d_k) or v.shape != (T, H, d_v) or alpha.shape != (T, H, d_v) \
+            or beta.shape != (T, H):
+        raise ValueError("inconsistent shapes")
+    dO = np.ascontiguousarray(dO, dtype=np.float64)
+    if dO.shape != (T, H, d_v):
+        raise ValueError("dO must be [T, H, d_v]")
+    if S0 is not None:
+        S0 = np.ascontiguousarray(S0, dtype=np.float64)
+        if S0.shape != (N, H, d_v, d_k):
+            raise ValueError("S0 must be [N, H, d_v, d_k]")
+    if dS_T is not None:
+        dS_T = np.ascontiguousarray(dS_T, dtype=np.float64)
+        if dS_T.shape != (N, H, d_v, d_k):
+            raise ValueError("dS_T must be [N, H, d_v, d_k]")
+    out = {
+        "dq": np.zeros((T, H, d_k)), "dk": np.zeros((T, H, d_k)),
+        "dv": np.zeros((T, H, d_v)), "dalpha": np.zeros((T, H, d_v)),
+        "dbeta": np.zeros((T, H)), "dS0": np.zeros((N, H, d_v, d_k)),
+    }
+    rc = lib.kda_oracle_backward(_ptr(q), _ptr(k), _ptr(v), kind, _ptr(alpha), _ptr(beta),
+                                 _ptr(S0), _ptr(cu), N, T, H, d_k, d_v, _ptr(dO), _ptr(dS_T),
+                                 _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                                 _ptr(out["dalpha"]), _ptr(out["dbeta"]), _ptr(out["dS0"]),
+                                 int(nthreads))
+    if rc != 0:
+        raise ValueError("kda_oracle_backward failed with code %d" % rc)
+    return out
 
 
 def decode_step(q, k, v, alpha, beta, S):

@@ -167,3 +167,252 @@ int kda_oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * ---------------------------------------------------------------------------
+ * Reverse mode of the same recurrence (gradients for training).
+ *
+ * The pages place the chunk-wise parallel form in training, which needs the
+ * gradients of a loss L with respect to every input.  Given dL/do_t and
+ * dL/dS_T, the chain rule through the three-line update taken backwards
+ * (memory updating, predict, forget gating, in that order) gives, with
+ * D = dL/dS_t accumulated from the later tokens and u = v_t - v~_t:
+ *
+ *     D       += do_t q_t^T                    (o_t = S_t q_t)
+ *     dq_t     = S_t^T do_t
+ *     g        = D k_t
+ *     dv_t     = beta_t g
+ *     dbeta_t  = u^T g
+ *     dk_t     = beta_t (D^T u - S~_t^T g)
+ *     dS~      = D - beta_t g k_t^T
+ *     dalpha_t = rowwise sum of dS~ (*) S_{t-1}
+ *     D        = diag(alpha_t) dS~             (dL/dS_{t-1})
+ *
+ * and dL/dS0 is the D left after the first token.  The states S_{t-1} are
+ * taken from a plain tape: the forward pass keeps every OR_SEG-th state, and
+ * the backward pass re-runs the forward step from the nearest kept state to
+ * refill the states of one segment at a time.  Re-running the same fp64
+ * step gives the same states bit for bit, so the tape only bounds memory.
+ * ---------------------------------------------------------------------------
+ */
+#define OR_SEG 64
+
+/* One forward step of one (sequence, head): S_prev -> S_next (the forget gating,
+ * predict and memory updating lines above, written out once more). */
+static void oracle_step(const double* S_prev, double* S_next, const double* kt,
+                        const double* vt, const double* at, double b, int32_t d_k,
+                        int32_t d_v)
+{
+    for (int32_t r = 0; r < d_v; ++r) {
+        const double* src = S_prev + (int64_t)r * d_k;
+        double* row = S_next + (int64_t)r * d_k;
+        for (int32_t c = 0; c < d_k; ++c) row[c] = at[r] * src[c];      /* S~ */
+        double pred = 0.0;
+        for (int32_t c = 0; c < d_k; ++c) pred += row[c] * kt[c];       /* v~ */
+        const double err = vt[r] - pred;
+        for (int32_t c = 0; c < d_k; ++c) row[c] += b * err * kt[c];
+    }
+}
+
+typedef struct {
+    double *tape, *kt, *qt, *vt, *at, *dot, *D, *Stl, *g, *u;
+} oracle_bwd_scratch;
+
+static void oracle_load_token(const void* q, const void* k, const void* v, int kind,
+                              const float* alpha, int64_t th, int32_t d_k, int32_t d_v,
+                              double* qt, double* kt, double* vt, double* at)
+{
+    for (int32_t c = 0; c < d_k; ++c) {
+        qt[c] = oracle_load(q, kind, th * d_k + c);
+        kt[c] = oracle_load(k, kind, th * d_k + c);
+    }
+    for (int32_t r = 0; r < d_v; ++r) {
+        vt[r] = oracle_load(v, kind, th * d_v + r);
+        at[r] = (double)alpha[th * d_v + r];
+    }
+}
+
+static void oracle_backward_pair(const void* q, const void* k, const void* v, int kind,
+                                 const float* alpha, const float* beta, const double* S0,
+                                 const double* dO, const double* dS_T,
+                                 int64_t t_begin, int64_t t_end, int32_t n, int32_t h,
+                                 int32_t H, int32_t d_k, int32_t d_v,
+                                 double* dq, double* dk, double* dv, double* dalpha,
+                                 double* dbeta, double* dS0, oracle_bwd_scratch* w)
+{
+    const int64_t sz = (int64_t)d_v * d_k;
+    const int64_t state_off = ((int64_t)n * H + h) * sz;
+    const int64_t L = t_end - t_begin;
+    const int64_t nseg = (L + OR_SEG - 1) / OR_SEG;
+    /* tape[0 .. nseg]: states at segment starts; tape[nseg + 1 + j]: state after
+     * token j of the segment being differentiated (j = 0 .. OR_SEG - 1) */
+    double* kept = w->tape;
+    double* seg = w->tape + (nseg + 1) * sz;
+
+    if (S0) memcpy(kept, S0 + state_off, sizeof(double) * (size_t)sz);
+    else memset(kept, 0, sizeof(double) * (size_t)sz);
+    for (int64_t s = 0; s < nseg; ++s) {
+        const double* cur = kept + s * sz;
+        double* nxt = kept + (s + 1) * sz;
+        memcpy(nxt, cur, sizeof(double) * (size_t)sz);
+        const int64_t a = t_begin + s * OR_SEG, e = a + OR_SEG < t_end ? a + OR_SEG : t_end;
+        for (int64_t t = a; t < e; ++t) {
+            const int64_t th = t * H + h;
+            oracle_load_token(q, k, v, kind, alpha, th, d_k, d_v, w->qt, w->kt, w->vt, w->at);
+            /* in place is safe: each row is read before it is written */
+            oracle_step(nxt, nxt, w->kt, w->vt, w->at, (double)beta[th], d_k, d_v);
+        }
+    }
+
+    /* D = dL/dS_T */
+    if (dS_T) memcpy(w->D, dS_T + state_off, sizeof(double) * (size_t)sz);
+    else memset(w->D, 0, sizeof(double) * (size_t)sz);
+
+    for (int64_t s = nseg - 1; s >= 0; --s) {
+        const int64_t a = t_begin + s * OR_SEG, e = a + OR_SEG < t_end ? a + OR_SEG : t_end;
+        /* refill the states after each token of this segment */
+        for (int64_t t = a; t < e; ++t) {
+            const int64_t th = t * H + h;
+            oracle_load_token(q, k, v, kind, alpha, th, d_k, d_v, w->qt, w->kt, w->vt, w->at);
+            const double* prev = t == a ? kept + s * sz : seg + (t - a - 1) * sz;
+            oracle_step(prev, seg + (t - a) * sz, w->kt, w->vt, w->at, (double)beta[th], d_k, d_v);
+        }
+        for (int64_t t = e - 1; t >= a; --t) {
+            const int64_t th = t * H + h;
+            oracle_load_token(q, k, v, kind, alpha, th, d_k, d_v, w->qt, w->kt, w->vt, w->at);
+            const double b = (double)(beta[th]);
+            const double* S_t = seg + (t - a) * sz;
+            const double* S_prev = t == a ? kept + s * sz : seg + (t - a - 1) * sz;
+            for (int32_t r = 0; r < d_v; ++r) w->dot[r] = dO[th * d_v + r];
+
+            /* output: D += do q^T, dq = S_t^T do */
+            for (int32_t r = 0; r < d_v; ++r) {
+                double* Dr = w->D + (int64_t)r * d_k;
+                for (int32_t c = 0; c < d_k; ++c) Dr[c] += w->dot[r] * w->qt[c];
+            }
+            for (int32_t c = 0; c < d_k; ++c) {
+                double acc = 0.0;
+                for (int32_t r = 0; r < d_v; ++r) acc += S_t[(int64_t)r * d_k + c] * w->dot[r];
+                dq[th * d_k + c] = acc;
+            }
+            /* forget gating and predict again: S~ and u = v - S~ k */
+            for (int32_t r = 0; r < d_v; ++r) {
+                const double* src = S_prev + (int64_t)r * d_k;
+                double* row = w->Stl + (int64_t)r * d_k;
+                double pred = 0.0;
+                for (int32_t c = 0; c < d_k; ++c) {
+                    row[c] = w->at[r] * src[c];
+                    pred += row[c] * w->kt[c];
+                }
+                w->u[r] = w->vt[r] - pred;
+            }
+            /* memory updating: g = D k, dv, dbeta, dk */
+            double db = 0.0;
+            for (int32_t r = 0; r < d_v; ++r) {
+                const double* Dr = w->D + (int64_t)r * d_k;
+                double acc = 0.0;
+                for (int32_t c = 0; c < d_k; ++c) acc += Dr[c] * w->kt[c];
+                w->g[r] = acc;
+                dv[th * d_v + r] = b * acc;
+                db += w->u[r] * acc;
+            }
+            dbeta[th] = db;
+            for (int32_t c = 0; c < d_k; ++c) {
+                double du = 0.0, sg = 0.0;
+                for (int32_t r = 0; r < d_v; ++r) {
+                    du += w->D[(int64_t)r * d_k + c] * w->u[r];
+                    sg += w->Stl[(int64_t)r * d_k + c] * w->g[r];
+                }
+                dk[th * d_k + c] = b * (du - sg);
+            }
+            /* dS~ = D - beta g k^T; dalpha = rowwise <dS~, S_{t-1}>; D = diag(alpha) dS~ */
+            for (int32_t r = 0; r < d_v; ++r) {
+                double* Dr = w->D + (int64_t)r * d_k;
+                const double* Pr = S_prev + (int64_t)r * d_k;
+                double da = 0.0;
+                for (int32_t c = 0; c < d_k; ++c) {
+                    Dr[c] = Dr[c] - b * w->g[r] * w->kt[c];
+                    da += Dr[c] * Pr[c];
+                }
+                dalpha[th * d_v + r] = da;
+                for (int32_t c = 0; c < d_k; ++c) Dr[c] = w->at[r] * Dr[c];
+            }
+        }
+    }
+    if (dS0) memcpy(dS0 + state_off, w->D, sizeof(double) * (size_t)sz);
+}
+
+/*
+ * Gradients of L = sum(dO * o) + sum(dS_T * S_T) for the packed batch that
+ * kda_oracle_prefill runs (same input layouts and checks, same return codes).
+ *   dO    [T_total][H][d_v] fp64          dS_T  [N][H][d_v][d_k] fp64 or NULL (zeros)
+ *   dq,dk [T_total][H][d_k] fp64 out      dv, dalpha [T_total][H][d_v] fp64 out
+ *   dbeta [T_total][H] fp64 out           dS0   [N][H][d_v][d_k] fp64 out or NULL
+ * Tokens past cu_seqlens[num_seqs] get zero gradients.
+ */
+int kda_oracle_backward(const void* q, const void* k, const void* v, int kind,
+                        const float* alpha, const float* beta, const double* S0,
+                        const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                        int32_t H, int32_t d_k, int32_t d_v,
+                        const double* dO, const double* dS_T,
+                        double* dq, double* dk, double* dv, double* dalpha, double* dbeta,
+                        double* dS0, int32_t nthreads)
+{
+    if (num_seqs < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || (kind != 0 && kind != 1)) return 1;
+    if (!cu_seqlens || (num_seqs > 0 && (!q || !k || !v || !alpha || !beta || !dO || !dq ||
+                                         !dk || !dv || !dalpha || !dbeta))) return 1;
+    if (cu_seqlens[0] != 0) return 2;
+    for (int32_t n = 0; n < num_seqs; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
+    if ((int64_t)cu_seqlens[num_seqs] > total_tokens) return 2;
+    if (num_seqs == 0) return 0;
+
+    memset(dq, 0, sizeof(double) * (size_t)total_tokens * H * d_k);
+    memset(dk, 0, sizeof(double) * (size_t)total_tokens * H * d_k);
+    memset(dv, 0, sizeof(double) * (size_t)total_tokens * H * d_v);
+    memset(dalpha, 0, sizeof(double) * (size_t)total_tokens * H * d_v);
+    memset(dbeta, 0, sizeof(double) * (size_t)total_tokens * H);
+
+    int64_t max_len = 0;
+    for (int32_t n = 0; n < num_seqs; ++n) {
+        const int64_t len = (int64_t)cu_seqlens[n + 1] - cu_seqlens[n];
+        if (len > max_len) max_len = len;
+    }
+    const int64_t sz = (int64_t)d_v * d_k;
+    const int64_t tape_states = (max_len + OR_SEG - 1) / OR_SEG + 1 + OR_SEG;
+    const int64_t pairs = (int64_t)num_seqs * H;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(|: failed)
+#endif
+    {
+        oracle_bwd_scratch w;
+        w.tape = (double*)malloc(sizeof(double) * (size_t)(tape_states * sz));
+        w.D = (double*)malloc(sizeof(double) * (size_t)sz);
+        w.Stl = (double*)malloc(sizeof(double) * (size_t)sz);
+        w.kt = (double*)malloc(sizeof(double) * (size_t)d_k);
+        w.qt = (double*)malloc(sizeof(double) * (size_t)d_k);
+        w.vt = (double*)malloc(sizeof(double) * (size_t)d_v);
+        w.at = (double*)malloc(sizeof(double) * (size_t)d_v);
+        w.dot = (double*)malloc(sizeof(double) * (size_t)d_v);
+        w.g = (double*)malloc(sizeof(double) * (size_t)d_v);
+        w.u = (double*)malloc(sizeof(double) * (size_t)d_v);
+        const int have = w.tape && w.D && w.Stl && w.kt && w.qt && w.vt && w.at && w.dot &&
+                         w.g && w.u;
+        if (!have) failed = 1;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t p = 0; p < pairs; ++p) {
+            if (!have) continue;
+            const int32_t n = (int32_t)(p / H), h = (int32_t)(p % H);
+            oracle_backward_pair(q, k, v, kind, alpha, beta, S0, dO, dS_T, cu_seqlens[n],
+                                 cu_seqlens[n + 1], n, h, H, d_k, d_v, dq, dk, dv, dalpha,
+                                 dbeta, dS0, &w);
+        }
+        free(w.tape); free(w.D); free(w.Stl); free(w.kt); free(w.qt); free(w.vt);
+        free(w.at); free(w.dot); free(w.g); free(w.u);
+    }
+    return failed ? 3 : 0;
+}
