@@ -257,6 +257,71 @@ kda_status kda_decode_step_gates(const void* q, const void* k, const void* v, co
                             stream);
 }
 
+size_t kda_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                   int32_t d_k, int32_t d_v, int32_t chunk) {
+    if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k != 128 || d_v < 64 || d_v % 64 != 0 ||
+        chunk != 64)
+        return 0;
+    return kda::backward_layout(num_seqs, total_tokens, H, d_v).end;
+}
+
+kda_status kda_backward(const void* q, const void* k, const void* v, const float* alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens,
+                        int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                        int32_t d_v, kda_dtype dtype, int32_t chunk, const void* d_o,
+                        const float* dS_T, float* dq, float* dk, float* dv, float* dalpha,
+                        float* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
+                        kda_stream_t stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 || d_k != 128 || d_v % 64 != 0 || d_v > 1024 || chunk != 64)
+        return KDA_ERR_UNSUPPORTED;
+    if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * H * (d_v / 64) > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (!cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !alpha || !beta || !d_o || !dq || !dk || !dv ||
+                             !dalpha || !dbeta))
+        return KDA_ERR_INVALID_ARG;
+    const kda::BackwardLayout L = kda::backward_layout(num_seqs, total_tokens, H, d_v);
+    if (workspace_bytes < L.end) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, alpha, beta, S0, cu_seqlens, d_o, dS_T, dq, dk, dv,
+                          dalpha, dbeta, dS0, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    // no output may overlap an input or another output
+    const size_t tq = (size_t)total_tokens * H * d_k, tv = (size_t)total_tokens * H * d_v;
+    const size_t ts = (size_t)total_tokens * H, ns = (size_t)num_seqs * H * d_v * d_k;
+    const void* ins[] = {q, k, v, alpha, beta, S0, d_o, dS_T, workspace};
+    const size_t in_n[] = {2 * tq, 2 * tq, 2 * tv, 4 * tv, 4 * ts, 4 * ns, 2 * tv, 4 * ns,
+                           workspace_bytes};
+    const void* outs[] = {dq, dk, dv, dalpha, dbeta, dS0};
+    const size_t out_n[] = {4 * tq, 4 * tq, 4 * tv, 4 * tv, 4 * ts, 4 * ns};
+    for (int o = 0; o < 6; ++o) {
+        for (int i = 0; i < 9; ++i)
+            if (overlaps(outs[o], out_n[o], ins[i], in_n[i])) return KDA_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 6; ++o2)
+            if (overlaps(outs[o], out_n[o], outs[o2], out_n[o2])) return KDA_ERR_INVALID_ARG;
+    }
+
+    char* ws = static_cast<char*>(workspace);
+    kda::PrefillArgs pa = {};
+    pa.cu_seqlens = cu_seqlens; pa.num_seqs = num_seqs; pa.total_tokens = total_tokens;
+    pa.H = H; pa.d_k = d_k; pa.d_v = d_v; pa.dtype = dtype; pa.chunk = chunk;
+    pa.status = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kStatus);
+    pa.counter = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kCounter);
+    pa.order = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kOrder);
+    if (kda::launch_planner(pa, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (num_seqs == 0) return KDA_OK;
+    kda::BackwardArgs a;
+    a.q = q; a.k = k; a.v = v; a.dO = d_o; a.alpha = alpha; a.beta = beta; a.S0 = S0;
+    a.dS_T = dS_T; a.cu_seqlens = cu_seqlens; a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens; a.H = H; a.d_v = d_v;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dalpha = dalpha; a.dbeta = dbeta; a.dS0 = dS0;
+    return kda::launch_backward(a, L, ws, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char* kda_status_string(kda_status s) {
     switch (s) {
         case KDA_OK: return "ok";

@@ -75,6 +75,27 @@ struct DecodeArgs {
     int32_t gate = 0;    // kda_gate_format
 };
 
+// Backward pass (kda_backward.cu).  Buffers appended to the base workspace:
+//   ckpt     fp32 [T / 64 + N][H][d_v][d_k]   chunk-start states; chunk c of
+//            sequence n (first token t0) in slot t0 / 64 + n + c
+//   dq_part  fp32 [d_v / 64][T][H][d_k]       dq of each 64-row block
+//   dk_part  fp32 [d_v / 64][T][H][d_k]
+//   db_part  fp32 [d_v / 64][T][H]
+struct BackwardLayout {
+    size_t ckpt = 0, dq_part = 0, dk_part = 0, db_part = 0, end = 0;
+};
+BackwardLayout backward_layout(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_v);
+
+struct BackwardArgs {
+    const void *q, *k, *v, *dO;   // bf16
+    const float *alpha, *beta, *S0, *dS_T;
+    const int32_t* cu_seqlens;
+    int32_t num_seqs;
+    int64_t total_tokens;
+    int32_t H, d_v;
+    float *dq, *dk, *dv, *dalpha, *dbeta, *dS0;
+};
+
 // Launchers; each returns the CUDA error of its launch.
 cudaError_t launch_planner(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
@@ -88,6 +109,10 @@ cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, char* 
 cudaError_t launch_split_combine(const PrefillArgs& a, const SplitLayout& L, char* ws,
                                  cudaStream_t stream);
 bool prefill_tc_supports(const PrefillArgs& a);
+// The chain kernel and the row-block reduction of the backward pass (ws: the
+// workspace base, planner already enqueued).
+cudaError_t launch_backward(const BackwardArgs& a, const BackwardLayout& L, char* ws,
+                            cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 int sm_count();   // of the current device, cached per device

@@ -7,8 +7,10 @@ library is missing or a call fails, an exception is raised.
 
 The names follow the C ABI: ``prefill`` / ``prefill_into`` wrap
 ``kda_prefill`` / ``kda_prefill_ex``, ``decode_step`` wraps
-``kda_decode_step``, ``workspace_size`` wraps ``kda_prefill_workspace_size``
-and ``device_status`` wraps ``kda_prefill_device_status``.
+``kda_decode_step``, ``workspace_size`` wraps ``kda_prefill_workspace_size``,
+``device_status`` wraps ``kda_prefill_device_status`` and ``backward`` /
+``backward_into`` / ``backward_workspace_size`` wrap ``kda_backward`` and
+``kda_backward_workspace_size``.
 """
 from __future__ import annotations
 
@@ -75,6 +77,11 @@ def load(path: str | None = None):
     lib.kda_decode_step_gates.restype = ctypes.c_int
     lib.kda_decode_step_gates.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, i32, i32, i32,
                                           i32, ctypes.c_int, vp, vp]
+    lib.kda_backward_workspace_size.restype = sz
+    lib.kda_backward_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32]
+    lib.kda_backward.restype = ctypes.c_int
+    lib.kda_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                 ctypes.c_int, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_version.restype = i32
@@ -281,3 +288,67 @@ def decode_step_gates(q, k, v, alpha, beta, S, o=None, *, gate: str = "channel",
     if st != OK:
         raise KdaError(st, "kda_decode_step_gates")
     return o
+
+
+def backward_workspace_size(num_seqs: int, total_tokens: int, H: int, d_k: int = 128,
+                            d_v: int = 128, chunk: int = 64) -> int:
+    """kda_backward_workspace_size: bytes of workspace (0: shape not supported)."""
+    return int(load().kda_backward_workspace_size(num_seqs, total_tokens, H, d_k, d_v, chunk))
+
+
+def backward_into(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T, grads, workspace, *,
+                  chunk: int = 64, stream=None) -> None:
+    """Enqueue kda_backward into preallocated fp32 gradients.
+
+    Inputs as ``prefill_into`` (bf16 q, k, v); dO: [T, H, d_v] bf16; dS_T:
+    [N, H, d_v, d_k] fp32 or None; grads: dict with "dq", "dk" [T, H, d_k],
+    "dv", "dalpha" [T, H, d_v], "dbeta" [T, H] and optionally "dS0"
+    [N, H, d_v, d_k], all fp32; workspace: uint8 device tensor of at least
+    ``backward_workspace_size`` bytes.
+    """
+    dS0 = grads.get("dS0")
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T, grads["dq"], grads["dk"],
+                grads["dv"], grads["dalpha"], grads["dbeta"], dS0, workspace)
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if dO.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v and dO must share one dtype")
+    for t in (alpha, beta, S0, dS_T, grads["dq"], grads["dk"], grads["dv"], grads["dalpha"],
+              grads["dbeta"], dS0):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("alpha, beta, states and gradients must be float32")
+    st = load().kda_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+                             _ptr(cu_seqlens), N, T, H, d_k, d_v, _dtype_code(q), chunk,
+                             _ptr(dO), _ptr(dS_T), _ptr(grads["dq"]), _ptr(grads["dk"]),
+                             _ptr(grads["dv"]), _ptr(grads["dalpha"]), _ptr(grads["dbeta"]),
+                             _ptr(dS0), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_backward")
+
+
+def backward(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, chunk: int = 64,
+             stream=None, check_device_status: bool = False):
+    """Allocate fp32 gradients with PyTorch and run kda_backward; returns a dict
+    with dq, dk, dv, dalpha, dbeta and dS0 (tokens past cu_seqlens[-1] zero)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    grads = {"dq": torch.zeros((T, H, d_k), dtype=torch.float32, device=dev),
+             "dk": torch.zeros((T, H, d_k), dtype=torch.float32, device=dev),
+             "dv": torch.zeros((T, H, d_v), dtype=torch.float32, device=dev),
+             "dalpha": torch.zeros((T, H, d_v), dtype=torch.float32, device=dev),
+             "dbeta": torch.zeros((T, H), dtype=torch.float32, device=dev),
+             "dS0": torch.zeros((N, H, d_v, d_k), dtype=torch.float32, device=dev)}
+    nbytes = backward_workspace_size(N, T, H, d_k, d_v, chunk)
+    if nbytes == 0:
+        raise KdaError(ERR_UNSUPPORTED, "kda_backward")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    backward_into(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T, grads, ws, chunk=chunk,
+                  stream=stream)
+    if check_device_status:
+        device_status(ws, stream=stream)
+    return grads

@@ -130,6 +130,19 @@ def prefill_inputs(spec: PrefillSpec, generator: torch.Generator | None = None) 
                 lengths=lengths, spec=spec, generator=gen)
 
 
+def backward_cotangents(d: dict, dS_T_std: float = 0.1) -> tuple:
+    """Draw the incoming gradients of a backward pass for the prefill problem `d`
+    (continuing its generator): dL/do ~ N(0, 1) in the storage dtype, and dL/dS_T
+    ~ N(0, dS_T_std^2) fp32, or None when dS_T_std == 0."""
+    spec, gen = d["spec"], d["generator"]
+    T = int(d["cu_seqlens"][-1])
+    dO = _normal(gen, (T, spec.H, spec.d_v)).to(_DTYPES[spec.dtype])
+    dS_T = None
+    if dS_T_std > 0:
+        dS_T = _normal(gen, (spec.num_seqs, spec.H, spec.d_v, spec.d_k), std=dS_T_std)
+    return dO, dS_T
+
+
 def decode_inputs(spec: DecodeSpec, generator: torch.Generator | None = None,
                   with_state: bool = True) -> dict:
     """Draw one decode step on the CPU: q, k [B,H,d_k]; v, alpha [B,H,d_v]; beta [B,H]; S."""

@@ -249,6 +249,52 @@ kda_status kda_decode_step_gates(const void* q, const void* k, const void* v,
                                  int32_t d_k, int32_t d_v, kda_dtype dtype, void* o,
                                  kda_stream_t stream);
 
+/*
+ * Bytes of device workspace kda_backward needs, or 0 for a shape it does not
+ * support.  About (total_tokens / 64 + num_seqs) x H x d_v x d_k x 4 bytes of
+ * chunk-start states plus 2 x d_v / 64 x total_tokens x H x d_k x 4 bytes of
+ * per-block partial sums.  Contents need no initialisation.
+ */
+size_t kda_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                   int32_t d_k, int32_t d_v, int32_t chunk);
+
+/*
+ * Backward pass of kda_prefill: given dO = dL/do and dS_T = dL/dS_T for some
+ * loss L of the outputs of kda_prefill on the same inputs, writes the
+ * gradients of L with respect to every input.  The chain rule is taken
+ * through the chunkwise form of the recurrence ("Kimi (AI)", section "Kimi
+ * Delta Attention (KDA)": the three-line update and o_t = S_t q_t).  The
+ * forward pass is recomputed inside the call: no state from kda_prefill is
+ * needed.
+ *
+ *   q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, d_k,
+ *   d_v, dtype, chunk     as for kda_prefill (channel fp32 gate)
+ *   d_o                   [T][H][d_v] (dtype): dL/do
+ *   dS_T                  [N][H][d_v][d_k] fp32 or NULL (zeros): dL/dS_T
+ *   dq, dk                outputs [T][H][d_k] fp32
+ *   dv, dalpha            outputs [T][H][d_v] fp32
+ *   dbeta                 output [T][H] fp32
+ *   dS0                   output [N][H][d_v][d_k] fp32, or NULL (not written);
+ *                         dL/dS0 (the gradient reaching S0 even when S0 is NULL)
+ *   workspace             kda_backward_workspace_size bytes, 16-byte aligned,
+ *                         not shared with calls that may run concurrently
+ *
+ * Gradients of tokens at or past cu_seqlens[num_seqs] are not written.  No
+ * output may overlap an input or another output.  kda_prefill_device_status
+ * on the same workspace reports device-detected input errors, which leave
+ * every output unwritten.  The result is deterministic (no atomics).
+ *
+ * Supported: dtype KDA_BF16, d_k == 128, d_v a multiple of 64 up to 1024,
+ * chunk == 64; alpha as for kda_prefill.  Arithmetic is fp32.
+ */
+kda_status kda_backward(const void* q, const void* k, const void* v, const float* alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens,
+                        int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                        int32_t d_v, kda_dtype dtype, int32_t chunk, const void* d_o,
+                        const float* dS_T, float* dq, float* dk, float* dv, float* dalpha,
+                        float* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
+                        kda_stream_t stream);
+
 /* Static description of a status code.  Never NULL. */
 const char* kda_status_string(kda_status s);
 

@@ -187,3 +187,51 @@ def test_decode_gates_rejects_on_host(lib):
     assert call(1, alpha=None) == 1
     assert call(2, alpha=_fake(0x40008)) == 1    # misaligned
     assert call(1, o=_fake(0x40000)) == 1        # o overlaps the [B][H] gate
+
+
+def _backward(lib, **kw):
+    M = 0x1000000   # 16 MB apart: no two fake buffers of this shape overlap
+    args = dict(q=_fake(1 * M), k=_fake(2 * M), v=_fake(3 * M), alpha=_fake(4 * M),
+                beta=_fake(5 * M), S0=None, cu=_fake(6 * M), N=2, T=64, H=2, d_k=128, d_v=128,
+                dtype=0, chunk=64, dO=_fake(7 * M), dS_T=None, dq=_fake(8 * M), dk=_fake(9 * M),
+                dv=_fake(10 * M), dalpha=_fake(11 * M), dbeta=_fake(12 * M), dS0=None,
+                ws=_fake(13 * M), ws_bytes=None)
+    args.update(kw)
+    if args["ws_bytes"] is None:
+        args["ws_bytes"] = lib.kda_backward_workspace_size(args["N"], args["T"], args["H"],
+                                                           128, 128, 64)
+    return lib.kda_backward(args["q"], args["k"], args["v"], args["alpha"], args["beta"],
+                            args["S0"], args["cu"], args["N"], args["T"], args["H"], args["d_k"],
+                            args["d_v"], args["dtype"], args["chunk"], args["dO"], args["dS_T"],
+                            args["dq"], args["dk"], args["dv"], args["dalpha"], args["dbeta"],
+                            args["dS0"], args["ws"], args["ws_bytes"], None)
+
+
+def test_backward_workspace_size(lib):
+    f = lib.kda_backward_workspace_size
+    assert f(2, 64, 2, 128, 128, 64) > 0
+    # chunk-start states: (T / 64 + N) slots of H d_v d_k fp32, plus 2 partial sums per block
+    assert f(8, 32768, 32, 128, 128, 64) >= (512 + 8) * 32 * 128 * 128 * 4 + \
+        2 * 2 * 32768 * 32 * 128 * 4
+    for bad in [(2, 64, 2, 64, 128, 64), (2, 64, 2, 128, 96, 64), (2, 64, 2, 128, 128, 32),
+                (-1, 64, 2, 128, 128, 64), (2, 64, 0, 128, 128, 64)]:
+        assert f(*bad) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=1), 2),                           # fp32 inputs: not implemented
+    (dict(d_k=64), 2),
+    (dict(d_v=96), 2),
+    (dict(chunk=32), 2),
+    (dict(dtype=5), 1),
+    (dict(ws_bytes=1024), 1),                     # workspace too small
+    (dict(dO=None), 1),
+    (dict(dq=None), 1),
+    (dict(dq=_fake(0x1000008)), 1),               # misaligned (and inside q)
+    (dict(dk=_fake(8 * 0x1000000 + 4096)), 1),    # dk overlaps dq
+    (dict(dv=_fake(3 * 0x1000000)), 1),           # dv is v
+    (dict(dS0=_fake(4 * 0x1000000 + 256)), 1),    # dS0 overlaps alpha
+    (dict(dalpha=_fake(13 * 0x1000000)), 1),      # dalpha inside the workspace
+])
+def test_backward_rejects_on_host(lib, kw, expect):
+    assert _backward(lib, **kw) == expect
