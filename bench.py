@@ -188,6 +188,18 @@ MMA_FLOPS_PER_BLOCK_CHUNK = (2 * 2 * 128 * 128 * 128 + 2 * 128 * 64 * 128
                              + 3 * 2 * 128 * 64 * 64)
 
 
+# Multiply-adds the backward kernel issues per (64-value-row block, 64-token
+# chunk), d_k = 128: the forward sweep (K K^T, Y, U, S update: 1,835,008) and
+# the backward sweep (K K^T, Q K^T, Y, U, E, dU, dT, dX, dT T^T, dA, dM, dq, dk,
+# D: 9,437,184), each a product of 64 x 64 x 128, 64 x 64 x 64 or 64 x 128 x 64.
+BWD_FMA_PER_BLOCK_CHUNK = 1_835_008 + 9_437_184
+
+
+def fp32_peak():
+    """fp32 CUDA-core peak (TFLOP/s): 152 SMs x 128 FMA lanes x 2 flops x 2.07 GHz."""
+    return 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 # ---------------------------------------------------------------- CPU oracle
 def time_oracle_sample(d, steps, pairs_wanted: int, budget_s: float, seed: int = 0):
     """Time the oracle on sampled (sequence, head) pairs of the workload (prefill
@@ -531,6 +543,33 @@ def run_component(args):
                        + 2 * spec.d_v * spec.d_k * 4)
         units, unit = bh, "state-updates/s"
         desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
+    elif args.workload == "backward":
+        spec = synth.PREFILL
+        d = synth.prefill_inputs(spec)
+        dO, dS_T = synth.backward_cotangents(d)
+        g = {key: (d[key].to(dev) if d[key] is not None else None)
+             for key in ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")}
+        dO, dS_T = dO.to(dev), dS_T.to(dev)
+        T = int(d["cu_seqlens"][-1])
+        N, H, d_k, d_v = spec.num_seqs, spec.H, spec.d_k, spec.d_v
+        grads = {"dq": torch.empty((T, H, d_k), device=dev),
+                 "dk": torch.empty((T, H, d_k), device=dev),
+                 "dv": torch.empty((T, H, d_v), device=dev),
+                 "dalpha": torch.empty((T, H, d_v), device=dev),
+                 "dbeta": torch.empty((T, H), device=dev),
+                 "dS0": torch.empty((N, H, d_v, d_k), device=dev)}
+        wsp = torch.empty(kda.backward_workspace_size(N, T, H, d_k, d_v, spec.chunk),
+                          dtype=torch.uint8, device=dev)
+
+        def launch():
+            kda.backward_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                              g["cu_seqlens"], dO, dS_T, grads, wsp, chunk=spec.chunk,
+                              stream=stream)
+        units, unit = T, "tokens/s"
+        nchunks = sum((n + spec.chunk - 1) // spec.chunk for n in d["lengths"])
+        bwd_flops = 2 * BWD_FMA_PER_BLOCK_CHUNK * nchunks * H * (d_v // 64)
+        desc = (f"backward of the prefill workload: N={N}, T={T}, H={H}, d_k={d_k}, d_v={d_v}, "
+                f"chunk={spec.chunk}; dO bf16, dS_T fp32; all six gradients fp32")
     else:
         gate = {"prefill_head_gate": "head", "prefill_log_gate": "log_bf16"}.get(args.workload)
         name = "varlen" if args.workload == "varlen_prefill" else \
@@ -594,6 +633,14 @@ def run_component(args):
                 "frac": achieved / hbm_peak, "traffic": None,
                 "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_src}
     l2 = "no flush: inputs exceed L2"
+    if args.workload == "backward":
+        # fp32 CUDA-core arithmetic bounds the backward kernel, not HBM
+        tflops = bwd_flops / (ms / 1e3) / 1e12
+        roofline = {"bound": "alu", "achieved": tflops, "peak": fp32_peak(), "unit": "TFLOP/s",
+                    "frac": tflops / fp32_peak(), "traffic": None,
+                    "fp32_flops_per_launch": bwd_flops,
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz"}
+        l2 = "no flush: inputs exceed L2"
     if args.workload == "l2_resident":
         # inputs stay in L2 between launches: the tensor pipe, not HBM, is the roofline
         tpeak, tsrc = bf16_peak()
@@ -624,13 +671,15 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload",
                    choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
-                            "l2_resident", "prefill_head_gate", "prefill_log_gate"],
+                            "l2_resident", "prefill_head_gate", "prefill_log_gate",
+                            "backward"],
                    default="varlen",
                    help="varlen (default): the full step; others time one kernel alone "
                         "(varlen_prefill: the varlen batch's prefill without the decode steps; "
                         "l2_resident: the chunk kernel with its inputs in L2, against the "
                         "tensor-core peak; prefill_head_gate / prefill_log_gate: the prefill "
-                        "workload with a per-head fp32 gate / a bf16 log-alpha gate)")
+                        "workload with a per-head fp32 gate / a bf16 log-alpha gate; "
+                        "backward: kda_backward on the prefill workload)")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)
