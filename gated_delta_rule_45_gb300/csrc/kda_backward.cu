@@ -15,7 +15,7 @@
 //             dT = dU (diag(beta) Y)^T,  sdA = strict_lower(-T^T dT T^T)
 //             dM = tril_incl(dP U^T)
 //             dq = dP S + dM K
-//             dk = dM^T Q + U dS^ - dY S + diag(beta) sdA K + sdA^T diag(beta) K
+//             dk = dM^T Q + U dS^ - dY S + diag(beta) sdA K + (diag(beta) sdA)^T K
 //             dv = dY / Gamma
 //             dbeta_r = sum_i dX_ri Y_ri + k_r . (sdA K)_r
 //             E = dP * P - dY * V / Gamma,  E[C-1] += rowsum(dS^ * (S + U^T K))
@@ -25,11 +25,18 @@
 // Value channels (rows of S) only interact through sums that end in dq, dk
 // and dbeta, so one CTA owns one (sequence, head, 64-row block) chain: a
 // forward sweep over its chunks writes the chunk-start states to the
-// workspace, a backward sweep walks the chunks in reverse carrying D in shared
-// memory.  dq, dk and dbeta are written per row block and summed by a second
-// kernel in a fixed order, so results are deterministic.  Arithmetic is fp32
-// on the CUDA cores: every product above is a shared-memory tile product of
-// at most 64 x 128 x 128.
+// workspace, a backward sweep walks the chunks in reverse.  dq, dk and dbeta
+// are written per row block and summed by a second kernel in a fixed order,
+// so results are deterministic.
+//
+// Every product is a warp-level bf16 tensor-core MMA (m16n8k16, fp32
+// accumulate) on shared-memory tiles loaded with ldmatrix.  Values that are
+// not bf16 already are carried as hi + lo bf16 pairs (hi = bf16(x),
+// lo = bf16(x - hi)) and multiplied as hi*hi + hi*lo + lo*hi, which keeps
+// about 16 bits of each operand: q, k, v and dO are bf16 inputs and need no
+// lo part.  The state S (forward sweep) and the state gradient D (backward
+// sweep) stay in fp32 accumulator registers across chunks; only their bf16
+// hi/lo copies go to shared memory as operands.
 #include "kda_internal.h"
 
 namespace kda {
@@ -38,22 +45,32 @@ namespace {
 constexpr int C = 64;      // tokens per chunk
 constexpr int DK = 128;    // key channels
 constexpr int R = 64;      // value rows per CTA
-constexpr int NTH = 256;   // threads: a 16 x 16 grid of 4 x 4 (or 4 x 8) output tiles
-constexpr int LDH = 130;   // bf16 row stride of K and Q (65 words: conflict-free columns)
-constexpr int LDS = 129;   // fp32 row stride of S and D
-constexpr int LDC = 65;    // fp32 row stride of the 64 x 64 tiles
+constexpr int NTH = 256;   // 8 warps
 
-// shared memory (bytes)
+// Shared memory.  bf16 tiles are row-major with their 16-byte chunks
+// XOR-swizzled by (row & 7), so ldmatrix rows and fragment stores hit
+// distinct banks.  64 x 128 tiles: K, Q, S hi/lo, D hi/lo.  64 x 64 tiles
+// come in hi/lo pairs; a pair's 16 KB also holds a 64 x 64 fp32 matrix while
+// T is being built.  G: fp32 64 x 64 (Gamma, later E).
+constexpr int BIG = 64 * 128 * 2;
+constexpr int SMALL = 64 * 64 * 2;
+constexpr int PAIR = 2 * SMALL;
 constexpr int OFF_K = 0;
-constexpr int OFF_Q = OFF_K + C * LDH * 2;
-constexpr int OFF_S = OFF_Q + C * LDH * 2;
-constexpr int OFF_D = OFF_S + R * LDS * 4;
-constexpr int OFF_T64 = OFF_D + R * LDS * 4;
-constexpr int T64_BYTES = 64 * LDC * 4;
-enum { T_G = 0, T_T, T_M, T_Y, T_U, T_P, T_W, N_T64 };
-constexpr int OFF_RED = OFF_T64 + N_T64 * T64_BYTES;        // fp32 [16][64]
-constexpr int OFF_MISC = OFF_RED + 16 * 64 * 4;             // beta, dbeta, e, gamma_C
+constexpr int OFF_Q = OFF_K + BIG;
+constexpr int OFF_SH = OFF_Q + BIG;
+constexpr int OFF_SL = OFF_SH + BIG;
+constexpr int OFF_DH = OFF_SL + BIG;
+constexpr int OFF_DL = OFF_DH + BIG;
+constexpr int OFF_PAIR = OFF_DL + BIG;
+enum { P_A = 0, P_T, P_X, P_U, P_P, P_W, N_PAIR };
+constexpr int OFF_G = OFF_PAIR + N_PAIR * PAIR;
+constexpr int OFF_RED = OFF_G + 64 * 64 * 4;     // fp32 [8][64]
+constexpr int OFF_MISC = OFF_RED + 8 * 64 * 4;   // beta, gamma_C, ecol, dbeta (64 each)
 constexpr int SMEM_BYTES = OFF_MISC + 4 * 64 * 4;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+__host__ __device__ constexpr int pair_hi(int p) { return OFF_PAIR + p * PAIR; }
+__host__ __device__ constexpr int pair_lo(int p) { return OFF_PAIR + p * PAIR + SMALL; }
 
 struct BwdParams {
     const __nv_bfloat16 *q, *k, *v, *dO;
@@ -68,83 +85,147 @@ struct BwdParams {
     float* dS0;               // [N][H][d_v][DK] or null
 };
 
-// acc[m][n] += sum_k A(ty + 16 m, k) B(k, tx + 16 n)
-template <int MT, int NT, int KD, class FA, class FB>
-__device__ __forceinline__ void mm(float (&acc)[MT][NT], FA A, FB B) {
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-#pragma unroll 4
-    for (int k = 0; k < KD; ++k) {
-        float a[MT], b[NT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) a[m] = A(ty + 16 * m, k);
-#pragma unroll
-        for (int n = 0; n < NT; ++n) b[n] = B(k, tx + 16 * n);
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int n = 0; n < NT; ++n) acc[m][n] = fmaf(a[m], b[n], acc[m][n]);
-    }
+// Byte offset of element (row, col) of a swizzled bf16 tile with `wb` bytes per row.
+__device__ __forceinline__ uint32_t swz(int row, int col, int wb) {
+    return (uint32_t)(row * wb + ((((col >> 3) ^ row) & 7) << 4) + (((col >> 3) & ~7) << 4) +
+                      ((col & 7) << 1));
 }
 
-template <int MT, int NT>
-__device__ __forceinline__ void zero(float (&acc)[MT][NT]) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int n = 0; n < NT; ++n) acc[m][n] = 0.f;
+// Index of (row, col) in a 64 x 64 fp32 matrix, 4-word groups XOR-swizzled by row.
+__device__ __forceinline__ int gidx(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+// A tile operand: shared-memory addresses of its hi and lo parts, bytes per row.
+struct Op {
+    uint32_t hi, lo;
+    int wb;
+};
 
-// Rows tok0 .. tok0 + 63 of a [T][H][DK] bf16 tensor into a [64][LDH] tile
-// (rows at or past nvalid are zero).
-__device__ void load_rows_bf16(__nv_bfloat16* dst, const __nv_bfloat16* src, int64_t tok0,
-                               int nvalid, int H, int h) {
-    const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
-    uint32_t* d = reinterpret_cast<uint32_t*>(dst + r * LDH + 32 * part);
-    if (r < nvalid) {
-        const uint4* s = reinterpret_cast<const uint4*>(src + ((tok0 + r) * H + h) * DK + 32 * part);
+// c[nt] += sum over k < 16 KS of A(m, k) B(k, n) for the warp's 16 x 8 NT
+// tile at (m0, n0).  TA: A(m, k) is stored at [k][m] (else [m][k]); TB: B(k, n)
+// is stored at [k][n] (else [n][k]).  ALO / BLO: the operand has a lo part.
+template <int NT, int KS, bool TA, bool TB, bool ALO, bool BLO>
+__device__ __forceinline__ void mma_tile(float (&c)[NT][4], const Op& A, const Op& B, int m0,
+                                         int n0) {
+    const int l = threadIdx.x & 31;
+    const int r8 = l & 7, j1 = (l >> 3) & 1, j2 = l >> 4;
+#pragma unroll 2
+    for (int ks = 0; ks < KS; ++ks) {
+        const int k = 16 * ks;
+        uint32_t ah[4], al[4];
+        const uint32_t aoff = TA ? swz(k + r8 + 8 * j2, m0 + 8 * j1, A.wb)
+                                 : swz(m0 + r8 + 8 * j1, k + 8 * j2, A.wb);
+        if (TA) ldsm4t(A.hi + aoff, ah); else ldsm4(A.hi + aoff, ah);
+        if (ALO) { if (TA) ldsm4t(A.lo + aoff, al); else ldsm4(A.lo + aoff, al); }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 x = s[j];
-            d[4 * j] = x.x; d[4 * j + 1] = x.y; d[4 * j + 2] = x.z; d[4 * j + 3] = x.w;
+        for (int np = 0; np < NT / 2; ++np) {
+            const int n = n0 + 16 * np;
+            const uint32_t boff = TB ? swz(k + r8 + 8 * j1, n + 8 * j2, B.wb)
+                                     : swz(n + r8 + 8 * j2, k + 8 * j1, B.wb);
+            uint32_t bh[4], bl[4];
+            if (TB) ldsm4t(B.hi + boff, bh); else ldsm4(B.hi + boff, bh);
+            if (BLO) { if (TB) ldsm4t(B.lo + boff, bl); else ldsm4(B.lo + boff, bl); }
+            mma16816(c[2 * np], ah, bh[0], bh[1]);
+            mma16816(c[2 * np + 1], ah, bh[2], bh[3]);
+            if (BLO) {
+                mma16816(c[2 * np], ah, bl[0], bl[1]);
+                mma16816(c[2 * np + 1], ah, bl[2], bl[3]);
+            }
+            if (ALO) {
+                mma16816(c[2 * np], al, bh[0], bh[1]);
+                mma16816(c[2 * np + 1], al, bh[2], bh[3]);
+            }
         }
-    } else {
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero(float (&c)[NT][4]) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) d[j] = 0u;
+    for (int i = 0; i < NT; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+}
+
+// (x0, x1) at (row, col), col even, as hi and lo bf16 pairs into a swizzled tile.
+__device__ __forceinline__ void st_pair(char* sm, int off_hi, int off_lo, int wb, int row,
+                                        int col, float x0, float x1) {
+    const uint32_t o = swz(row, col, wb);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    *reinterpret_cast<__nv_bfloat162*>(sm + off_hi + o) = h;
+    *reinterpret_cast<__nv_bfloat162*>(sm + off_lo + o) =
+        __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+}
+
+__device__ __forceinline__ float2 ld_pair(const char* sm, int off_hi, int off_lo, int wb, int row,
+                                          int col) {
+    const uint32_t o = swz(row, col, wb);
+    const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + off_hi + o));
+    const float2 l = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + off_lo + o));
+    return make_float2(h.x + l.x, h.y + l.y);
+}
+
+__device__ __forceinline__ float2 ld_bf2(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+// Rows tok0 .. tok0 + 63 of a [T][H][DK] bf16 tensor into a swizzled 64 x 128
+// tile (rows at or past nvalid are zero).
+__device__ void load_rows(char* sm, int off, const __nv_bfloat16* src, int64_t tok0, int nvalid,
+                          int H, int h) {
+    for (int e = threadIdx.x; e < 64 * 16; e += NTH) {
+        const int row = e >> 4, c = e & 15;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (row < nvalid)
+            x = *reinterpret_cast<const uint4*>(src + ((tok0 + row) * H + h) * DK + 8 * c);
+        *reinterpret_cast<uint4*>(sm + off + swz(row, 8 * c, 256)) = x;
     }
 }
 
-// A 64 x 128 fp32 block, rows contiguous in global memory, into a [64][LDS] tile.
-__device__ void load_state(float* dst, const float* src) {
-    for (int e = 4 * threadIdx.x; e < R * DK; e += 4 * NTH) {
-        float4 x = src ? *reinterpret_cast<const float4*>(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float* d = dst + (e / DK) * LDS + e % DK;
-        d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
+// Fragment coordinates of the calling thread: a 64 x 64 output is tiled by the
+// 8 warps as 4 (rows) x 2 (32 columns), a 64 x 128 output as 4 x 2 (64 columns).
+struct Frag {
+    int m0, n64, n128, g, t;
+    __device__ Frag() {
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        m0 = 16 * (w & 3);
+        n64 = 32 * (w >> 2);
+        n128 = 64 * (w >> 2);
+        g = l >> 2;
+        t = l & 3;
     }
-}
+    __device__ int row(int e) const { return m0 + g + 8 * (e >> 1); }
+    __device__ int col64(int nt) const { return n64 + 8 * nt + 2 * t; }
+    __device__ int col128(int nt) const { return n128 + 8 * nt + 2 * t; }
+};
 
-__device__ void store_state(float* dst, const float* src) {
-    for (int e = 4 * threadIdx.x; e < R * DK; e += 4 * NTH) {
-        const float* s = src + (e / DK) * LDS + e % DK;
-        *reinterpret_cast<float4*>(dst + e) = make_float4(s[0], s[1], s[2], s[3]);
-    }
-}
-
-// Per-chunk inputs shared by both sweeps: K (and Q), beta, Gamma and gamma_C,
-// then T = (I + diag(beta) strict_lower(K K^T))^-1 by forward substitution.
+// Per-chunk inputs shared by both sweeps: K (and Q), beta, Gamma, gamma_C and
+// T = (I + diag(beta) strict_lower(K K^T))^-1 as a hi/lo pair.
 __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nvalid, int h,
-                            int row0, bool with_q) {
-    __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + OFF_K);
-    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + OFF_Q);
-    float* tG = reinterpret_cast<float*>(sm + OFF_T64 + T_G * T64_BYTES);
-    float* tT = reinterpret_cast<float*>(sm + OFF_T64 + T_T * T64_BYTES);
-    float* tW = reinterpret_cast<float*>(sm + OFF_T64 + T_W * T64_BYTES);
+                            int row0, bool with_q, const Frag& f) {
+    float* G = reinterpret_cast<float*>(sm + OFF_G);
+    float* Lf = reinterpret_cast<float*>(sm + pair_hi(P_A));
+    float* Tf = reinterpret_cast<float*>(sm + pair_hi(P_T));
     float* bet = reinterpret_cast<float*>(sm + OFF_MISC);
-    float* gC = bet + 192;
+    float* gC = bet + 64;
     const int tid = threadIdx.x;
-    load_rows_bf16(Ks, p.k, tok0, nvalid, p.H, h);
-    if (with_q) load_rows_bf16(Qs, p.q, tok0, nvalid, p.H, h);
+    load_rows(sm, OFF_K, p.k, tok0, nvalid, p.H, h);
+    if (with_q) load_rows(sm, OFF_Q, p.q, tok0, nvalid, p.H, h);
     if (tid < C) bet[tid] = tid < nvalid ? p.beta[(tok0 + tid) * p.H + h] : 0.f;
     if (tid >= 64 && tid < 128) {   // Gamma, one value channel per thread
         const int i = tid - 64;
@@ -153,25 +234,24 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
         float run = 1.f;
         for (int r = 0; r < C; ++r) {
             if (r < nvalid) run *= al[r * stride];
-            tG[r * LDC + i] = run;
+            G[gidx(r, i)] = run;
         }
         gC[i] = run;
     }
-    // T starts as the identity
-    for (int e = tid; e < C * C; e += NTH) tT[(e >> 6) * LDC + (e & 63)] = (e >> 6) == (e & 63) ? 1.f : 0.f;
+    for (int e = tid; e < C * C; e += NTH) Tf[gidx(e >> 6, e & 63)] = (e >> 6) == (e & 63) ? 1.f : 0.f;
     __syncthreads();
-    {   // L' = diag(beta) strict_lower(K K^T)
-        float acc[4][4];
-        zero(acc);
-        mm<4, 4, DK>(acc, [&](int r, int c) { return bf(Ks + r * LDH + c); },
-                     [&](int c, int s) { return bf(Ks + s * LDH + c); });
-        const int tx = tid & 15, ty = tid >> 4;
+    {   // L' = diag(beta) strict_lower(K K^T), fp32
+        float c[4][4];
+        zero(c);
+        const Op K{(uint32_t)__cvta_generic_to_shared(sm + OFF_K), 0u, 256};
+        mma_tile<4, 8, false, false, false, false>(c, K, K, f.m0, f.n64);
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int r = ty + 16 * m, s = tx + 16 * n;
-                tW[r * LDC + s] = s < r ? bet[r] * acc[m][n] : 0.f;
+            for (int e = 0; e < 4; e += 2) {
+                const int r = f.row(e), s = f.col64(nt);
+                Lf[gidx(r, s)] = s < r ? bet[r] * c[nt][e] : 0.f;
+                Lf[gidx(r, s + 1)] = s + 1 < r ? bet[r] * c[nt][e + 1] : 0.f;
             }
     }
     __syncthreads();
@@ -179,11 +259,26 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
         const int j = tid >> 2, part = tid & 3;
         for (int r = 1; r < C; ++r) {
             float acc = 0.f;
-            for (int s = part; s < r; s += 4) acc = fmaf(tW[r * LDC + s], tT[s * LDC + j], acc);
+            for (int s = part; s < r; s += 4) acc = fmaf(Lf[gidx(r, s)], Tf[gidx(s, j)], acc);
             acc += __shfl_xor_sync(0xffffffffu, acc, 1);
             acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (part == 0 && j < r) tT[r * LDC + j] = -acc;
+            if (part == 0 && j < r) Tf[gidx(r, j)] = -acc;
             __syncwarp();
+        }
+    }
+    __syncthreads();
+    {   // T as a hi/lo pair over its own fp32 storage
+        float2 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + NTH * q;
+            v[q] = *reinterpret_cast<const float2*>(Tf + gidx(e >> 5, 2 * (e & 31)));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + NTH * q;
+            st_pair(sm, pair_hi(P_T), pair_lo(P_T), 128, e >> 5, 2 * (e & 31), v[q].x, v[q].y);
         }
     }
     __syncthreads();
@@ -191,25 +286,19 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
 
 __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p) {
     if (*p.status != 0) return;
-    extern __shared__ __align__(16) char sm[];
-    const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_K);
-    const __nv_bfloat16* Qs = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_Q);
-    float* Ss = reinterpret_cast<float*>(sm + OFF_S);
-    float* Ds = reinterpret_cast<float*>(sm + OFF_D);
-    float* tG = reinterpret_cast<float*>(sm + OFF_T64 + T_G * T64_BYTES);
-    float* tT = reinterpret_cast<float*>(sm + OFF_T64 + T_T * T64_BYTES);
-    float* tM = reinterpret_cast<float*>(sm + OFF_T64 + T_M * T64_BYTES);
-    float* tY = reinterpret_cast<float*>(sm + OFF_T64 + T_Y * T64_BYTES);
-    float* tU = reinterpret_cast<float*>(sm + OFF_T64 + T_U * T64_BYTES);
-    float* tP = reinterpret_cast<float*>(sm + OFF_T64 + T_P * T64_BYTES);
-    float* tW = reinterpret_cast<float*>(sm + OFF_T64 + T_W * T64_BYTES);
+    extern __shared__ __align__(128) char sm[];
+    const uint32_t sb = (uint32_t)__cvta_generic_to_shared(sm);
+    float* G = reinterpret_cast<float*>(sm + OFF_G);
+    // red rows: 0-3 column sums of U * K dS^^T (one per row group of warps), later
+    // 0-1 the rowsums of dS^ * S; 4-5 and 6-7 the two parts of dbeta (one per column half)
     float* red = reinterpret_cast<float*>(sm + OFF_RED);
     float* bet = reinterpret_cast<float*>(sm + OFF_MISC);
-    float* dbr = bet + 64;
+    float* gC = bet + 64;
     float* ecol = bet + 128;
-    float* gC = bet + 192;
+    float* dbr = bet + 192;
+    const Frag f;
+    const int tid = threadIdx.x, w = tid >> 5;
 
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int rb = blockIdx.x % p.nrb;
     const int h = (blockIdx.x / p.nrb) % p.H;
     const int n = p.order[blockIdx.x / (p.nrb * p.H)];
@@ -219,324 +308,389 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
     const int row0 = rb * R;
     const int64_t slot0 = t0 / C + n;
     const size_t st_rows = (size_t)p.d_v * DK;   // one head's state
+    const size_t head_state = ((size_t)n * p.H + h) * st_rows + (size_t)row0 * DK;
     auto ckpt_at = [&](int c) {
         return p.ckpt + ((size_t)(slot0 + c) * p.H + h) * st_rows + (size_t)row0 * DK;
     };
     const int64_t vstride = (int64_t)p.H * p.d_v;
     auto vidx = [&](int64_t tok, int i) { return tok * vstride + (int64_t)h * p.d_v + row0 + i; };
 
+    const Op opK{sb + OFF_K, 0u, 256}, opQ{sb + OFF_Q, 0u, 256};
+    const Op opS{sb + OFF_SH, sb + OFF_SL, 256}, opD{sb + OFF_DH, sb + OFF_DL, 256};
+    auto pop = [&](int pi) { return Op{sb + pair_hi(pi), sb + pair_lo(pi), 128}; };
+    const Op opA = pop(P_A), opT = pop(P_T), opX = pop(P_X), opU = pop(P_U), opP = pop(P_P),
+             opW = pop(P_W);
+
     // ---- forward sweep: chunk-start states into the workspace ----
-    load_state(Ss, p.S0 ? p.S0 + ((size_t)n * p.H + h) * st_rows + (size_t)row0 * DK : nullptr);
-    __syncthreads();
-    for (int c = 0; c < nc; ++c) {
-        const int64_t tok0 = t0 + (int64_t)c * C;
-        const int nvalid = min(C, len - c * C);
-        store_state(ckpt_at(c), Ss);
-        chunk_setup(p, sm, tok0, nvalid, h, row0, false);
-        {   // Y = V / Gamma - K S^T
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, DK>(acc, [&](int r, int c2) { return bf(Ks + r * LDH + c2); },
-                         [&](int c2, int i) { return Ss[i * LDS + c2]; });
+    {
+        float Sm[8][4];   // this block's rows of S, fp32, in accumulator layout
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+        for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) {
-                    const int r = ty + 16 * m, i = tx + 16 * n2;
-                    const float v = r < nvalid ? bf(p.v + vidx(tok0 + r, i)) : 0.f;
-                    tY[r * LDC + i] = v / tG[r * LDC + i] - acc[m][n2];
+            for (int e = 0; e < 4; e += 2) {
+                const int r = f.row(e), col = f.col128(nt);
+                float2 x = make_float2(0.f, 0.f);
+                if (p.S0) x = *reinterpret_cast<const float2*>(p.S0 + head_state + r * DK + col);
+                Sm[nt][e] = x.x;
+                Sm[nt][e + 1] = x.y;
+                st_pair(sm, OFF_SH, OFF_SL, 256, r, col, x.x, x.y);
+            }
+        __syncthreads();
+        for (int c = 0; c < nc; ++c) {
+            const int64_t tok0 = t0 + (int64_t)c * C;
+            const int nvalid = min(C, len - c * C);
+            float* ck = ckpt_at(c);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2)
+                    *reinterpret_cast<float2*>(ck + f.row(e) * DK + f.col128(nt)) =
+                        make_float2(Sm[nt][e], Sm[nt][e + 1]);
+            chunk_setup(p, sm, tok0, nvalid, h, row0, false, f);
+            {   // X = diag(beta) (V / Gamma - K S^T)
+                float cY[4][4];
+                zero(cY);
+                mma_tile<4, 8, false, false, false, true>(cY, opK, opS, f.m0, f.n64);
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const int r = f.row(e), i = f.col64(nt);
+                        const float2 vv = r < nvalid ? ld_bf2(p.v + vidx(tok0 + r, i))
+                                                     : make_float2(0.f, 0.f);
+                        const float y0 = vv.x / G[gidx(r, i)] - cY[nt][e];
+                        const float y1 = vv.y / G[gidx(r, i + 1)] - cY[nt][e + 1];
+                        st_pair(sm, pair_hi(P_X), pair_lo(P_X), 128, r, i, bet[r] * y0, bet[r] * y1);
+                    }
+            }
+            __syncthreads();
+            {   // U = T X
+                float cU[4][4];
+                zero(cU);
+                mma_tile<4, 4, false, true, true, true>(cU, opT, opX, f.m0, f.n64);
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2)
+                        st_pair(sm, pair_hi(P_U), pair_lo(P_U), 128, f.row(e), f.col64(nt),
+                                cU[nt][e], cU[nt][e + 1]);
+            }
+            __syncthreads();
+            // S <- diag(gamma_C) (S + U^T K)
+            mma_tile<8, 4, true, true, true, false>(Sm, opU, opK, f.m0, f.n128);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e), col = f.col128(nt);
+                    Sm[nt][e] *= gC[r];
+                    Sm[nt][e + 1] *= gC[r];
+                    st_pair(sm, OFF_SH, OFF_SL, 256, r, col, Sm[nt][e], Sm[nt][e + 1]);
                 }
+            __syncthreads();
         }
-        __syncthreads();
-        {   // U = T diag(beta) Y
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, C>(acc, [&](int r, int s) { return tT[r * LDC + s]; },
-                        [&](int s, int i) { return bet[s] * tY[s * LDC + i]; });
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) tU[(ty + 16 * m) * LDC + tx + 16 * n2] = acc[m][n2];
-        }
-        __syncthreads();
-        {   // S <- diag(gamma_C) (S + U^T K)
-            float acc[4][8];
-            zero(acc);
-            mm<4, 8, C>(acc, [&](int i, int s) { return tU[s * LDC + i]; },
-                        [&](int s, int c2) { return bf(Ks + s * LDH + c2); });
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int n2 = 0; n2 < 8; ++n2) {
-                    const int i = ty + 16 * m, c2 = tx + 16 * n2;
-                    Ss[i * LDS + c2] = gC[i] * (Ss[i * LDS + c2] + acc[m][n2]);
-                }
-        }
-        __syncthreads();
     }
 
     // ---- backward sweep ----
-    load_state(Ds, p.dS_T ? p.dS_T + ((size_t)n * p.H + h) * st_rows + (size_t)row0 * DK : nullptr);
-    __syncthreads();
+    float Dm[8][4];   // this block's rows of D (dL/d state at the chunk's end), fp32
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+            float2 x = make_float2(0.f, 0.f);
+            if (p.dS_T)
+                x = *reinterpret_cast<const float2*>(p.dS_T + head_state + f.row(e) * DK + f.col128(nt));
+            Dm[nt][e] = x.x;
+            Dm[nt][e + 1] = x.y;
+        }
     for (int c = nc - 1; c >= 0; --c) {
         const int64_t tok0 = t0 + (int64_t)c * C;
         const int nvalid = min(C, len - c * C);
-        load_state(Ss, ckpt_at(c));
-        chunk_setup(p, sm, tok0, nvalid, h, row0, true);
-        {   // M = tril_incl(Q K^T)
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, DK>(acc, [&](int r, int c2) { return bf(Qs + r * LDH + c2); },
-                         [&](int c2, int s) { return bf(Ks + s * LDH + c2); });
+        {   // the chunk-start state as hi/lo tiles
+            const float* ck = ckpt_at(c);
+            for (int e = tid; e < 64 * 32; e += NTH) {
+                const int r = e >> 5, col = 4 * (e & 31);
+                const float4 x = *reinterpret_cast<const float4*>(ck + r * DK + col);
+                st_pair(sm, OFF_SH, OFF_SL, 256, r, col, x.x, x.y);
+                st_pair(sm, OFF_SH, OFF_SL, 256, r, col + 2, x.z, x.w);
+            }
+        }
+        chunk_setup(p, sm, tok0, nvalid, h, row0, true, f);
+        {   // M = tril_incl(Q K^T) into pair A
+            float cM[4][4];
+            zero(cM);
+            mma_tile<4, 8, false, false, false, false>(cM, opQ, opK, f.m0, f.n64);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) {
-                    const int r = ty + 16 * m, s = tx + 16 * n2;
-                    tM[r * LDC + s] = s <= r ? acc[m][n2] : 0.f;
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e), s = f.col64(nt);
+                    st_pair(sm, pair_hi(P_A), pair_lo(P_A), 128, r, s, s <= r ? cM[nt][e] : 0.f,
+                            s + 1 <= r ? cM[nt][e + 1] : 0.f);
                 }
         }
-        {   // Y = V / Gamma - K S^T and dP = Gamma * dO
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, DK>(acc, [&](int r, int c2) { return bf(Ks + r * LDH + c2); },
-                         [&](int c2, int i) { return Ss[i * LDS + c2]; });
+        float Y[4][4], dP[4][4];
+        {   // Y = V / Gamma - K S^T, X = diag(beta) Y into pair X, dP = Gamma * dO into pair P
+            zero(Y);
+            mma_tile<4, 8, false, false, false, true>(Y, opK, opS, f.m0, f.n64);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) {
-                    const int r = ty + 16 * m, i = tx + 16 * n2;
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e), i = f.col64(nt);
                     const bool ok = r < nvalid;
-                    const float v = ok ? bf(p.v + vidx(tok0 + r, i)) : 0.f;
-                    const float d = ok ? bf(p.dO + vidx(tok0 + r, i)) : 0.f;
-                    const float g = tG[r * LDC + i];
-                    tY[r * LDC + i] = v / g - acc[m][n2];
-                    tP[r * LDC + i] = g * d;
+                    const float2 vv = ok ? ld_bf2(p.v + vidx(tok0 + r, i)) : make_float2(0.f, 0.f);
+                    const float2 dd = ok ? ld_bf2(p.dO + vidx(tok0 + r, i)) : make_float2(0.f, 0.f);
+                    const float g0 = G[gidx(r, i)], g1 = G[gidx(r, i + 1)];
+                    Y[nt][e] = vv.x / g0 - Y[nt][e];
+                    Y[nt][e + 1] = vv.y / g1 - Y[nt][e + 1];
+                    st_pair(sm, pair_hi(P_X), pair_lo(P_X), 128, r, i, bet[r] * Y[nt][e],
+                            bet[r] * Y[nt][e + 1]);
+                    dP[nt][e] = g0 * dd.x;
+                    dP[nt][e + 1] = g1 * dd.y;
+                    st_pair(sm, pair_hi(P_P), pair_lo(P_P), 128, r, i, dP[nt][e], dP[nt][e + 1]);
                 }
         }
         __syncthreads();
-        {   // U = T diag(beta) Y; dS^ = diag(gamma_C) D
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, C>(acc, [&](int r, int s) { return tT[r * LDC + s]; },
-                        [&](int s, int i) { return bet[s] * tY[s * LDC + i]; });
+        float U[4][4];
+        {   // U = T X into pair U; dS^ = diag(gamma_C) D as hi/lo tiles
+            zero(U);
+            mma_tile<4, 4, false, true, true, true>(U, opT, opX, f.m0, f.n64);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) tU[(ty + 16 * m) * LDC + tx + 16 * n2] = acc[m][n2];
-            for (int e = tid; e < R * DK; e += NTH) {
-                const int i = e >> 7;
-                Ds[i * LDS + (e & 127)] *= gC[i];
-            }
+                for (int e = 0; e < 4; e += 2)
+                    st_pair(sm, pair_hi(P_U), pair_lo(P_U), 128, f.row(e), f.col64(nt), U[nt][e],
+                            U[nt][e + 1]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e);
+                    Dm[nt][e] *= gC[r];
+                    Dm[nt][e + 1] *= gC[r];
+                    st_pair(sm, OFF_DH, OFF_DL, 256, r, f.col128(nt), Dm[nt][e], Dm[nt][e + 1]);
+                }
         }
         __syncthreads();
-        // E = dP * P with P = Q S^T + M U, kept in registers (same tiles as dX below)
         float E[4][4];
-        zero(E);
-        mm<4, 4, DK>(E, [&](int r, int c2) { return bf(Qs + r * LDH + c2); },
-                     [&](int c2, int i) { return Ss[i * LDS + c2]; });
-        mm<4, 4, C>(E, [&](int r, int s) { return tM[r * LDC + s]; },
-                    [&](int s, int i) { return tU[s * LDC + i]; });
+        {   // E = dP * (Q S^T + M U)
+            zero(E);
+            mma_tile<4, 8, false, false, false, true>(E, opQ, opS, f.m0, f.n64);
+            mma_tile<4, 4, false, true, true, true>(E, opA, opU, f.m0, f.n64);
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int n2 = 0; n2 < 4; ++n2) E[m][n2] *= tP[(ty + 16 * m) * LDC + tx + 16 * n2];
-        {   // dU = K dS^^T + M^T dP; the first term also gives sum_r U_ri (K dS^^T)_ri
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, DK>(acc, [&](int r, int c2) { return bf(Ks + r * LDH + c2); },
-                         [&](int c2, int i) { return Ds[i * LDS + c2]; });
-#pragma unroll
-            for (int n2 = 0; n2 < 4; ++n2) {
-                float s = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) s = fmaf(tU[(ty + 16 * m) * LDC + tx + 16 * n2], acc[m][n2], s);
-                red[ty * 64 + tx + 16 * n2] = s;
-            }
-            mm<4, 4, C>(acc, [&](int r, int s) { return tM[s * LDC + r]; },
-                        [&](int s, int i) { return tP[s * LDC + i]; });
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) tW[(ty + 16 * m) * LDC + tx + 16 * n2] = acc[m][n2];
+                for (int e = 0; e < 4; ++e) E[nt][e] *= dP[nt][e];
         }
-        __syncthreads();
-        {   // dT = dU (diag(beta) Y)^T into M's tile; finish the column sums
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, R>(acc, [&](int r, int i) { return tW[r * LDC + i]; },
-                        [&](int i, int s) { return bet[s] * tY[s * LDC + i]; });
+        {   // Z = K dS^^T; column sums of U * Z; dU = Z + M^T dP into pair W
+            float Z[4][4];
+            zero(Z);
+            mma_tile<4, 8, false, false, false, true>(Z, opK, opD, f.m0, f.n64);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) tM[(ty + 16 * m) * LDC + tx + 16 * n2] = acc[m][n2];
-            if (tid < 64) {
-                float s = 0.f;
-                for (int j = 0; j < 16; ++j) s += red[j * 64 + tid];
-                ecol[tid] = s;
-            }
-        }
-        __syncthreads();
-        {   // dX = T^T dU: dbeta (first part), dY (over Y), dv, E -= dY V / Gamma
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, C>(acc, [&](int r, int s) { return tT[s * LDC + r]; },
-                        [&](int s, int i) { return tW[s * LDC + i]; });
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = ty + 16 * m;
-                const bool ok = r < nvalid;
-                float part = 0.f;
-#pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) {
-                    const int i = tx + 16 * n2;
-                    const float dx = acc[m][n2];
-                    part = fmaf(dx, tY[r * LDC + i], part);
-                    const float dy = bet[r] * dx;
-                    tY[r * LDC + i] = dy;
-                    const float g = tG[r * LDC + i];
-                    const float v = ok ? bf(p.v + vidx(tok0 + r, i)) : 0.f;
-                    E[m][n2] -= dy * v / g;
-                    if (ok) p.dv[vidx(tok0 + r, i)] = dy / g;
+                for (int q = 0; q < 2; ++q) {
+                    float s = fmaf(U[nt][q], Z[nt][q], U[nt][q + 2] * Z[nt][q + 2]);
+                    s += __shfl_xor_sync(0xffffffffu, s, 4);
+                    s += __shfl_xor_sync(0xffffffffu, s, 8);
+                    s += __shfl_xor_sync(0xffffffffu, s, 16);
+                    if (f.g == 0) red[(w & 3) * 64 + f.col64(nt) + q] = s;
                 }
-                red[tx * 64 + r] = part;
+            mma_tile<4, 4, true, true, true, true>(Z, opA, opP, f.m0, f.n64);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2)
+                    st_pair(sm, pair_hi(P_W), pair_lo(P_W), 128, f.row(e), f.col64(nt), Z[nt][e],
+                            Z[nt][e + 1]);
+        }
+        __syncthreads();
+        {   // dT = dU X^T into pair A; finish the column sums
+            float c2[4][4];
+            zero(c2);
+            mma_tile<4, 4, false, false, true, true>(c2, opW, opX, f.m0, f.n64);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2)
+                    st_pair(sm, pair_hi(P_A), pair_lo(P_A), 128, f.row(e), f.col64(nt), c2[nt][e],
+                            c2[nt][e + 1]);
+            if (tid < 64) ecol[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+        }
+        __syncthreads();
+        {   // dX = T^T dU: dbeta (first part), -dY into pair X, dv, E -= dY V / Gamma
+            float c2[4][4];
+            zero(c2);
+            mma_tile<4, 4, true, true, true, true>(c2, opT, opW, f.m0, f.n64);
+            float part[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e), i = f.col64(nt);
+                    const bool ok = r < nvalid;
+                    part[e >> 1] = fmaf(c2[nt][e], Y[nt][e], fmaf(c2[nt][e + 1], Y[nt][e + 1], part[e >> 1]));
+                    const float dy0 = bet[r] * c2[nt][e], dy1 = bet[r] * c2[nt][e + 1];
+                    st_pair(sm, pair_hi(P_X), pair_lo(P_X), 128, r, i, -dy0, -dy1);
+                    const float g0 = G[gidx(r, i)], g1 = G[gidx(r, i + 1)];
+                    const float2 vv = ok ? ld_bf2(p.v + vidx(tok0 + r, i)) : make_float2(0.f, 0.f);
+                    E[nt][e] -= dy0 * vv.x / g0;
+                    E[nt][e + 1] -= dy1 * vv.y / g1;
+                    if (ok)
+                        *reinterpret_cast<float2*>(p.dv + vidx(tok0 + r, i)) = make_float2(dy0 / g0, dy1 / g1);
+                }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float s = part[q];
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (f.t == 0) red[(4 + (w >> 2)) * 64 + f.m0 + f.g + 8 * q] = s;
             }
         }
         __syncthreads();
-        {   // tmp = dT T^T over dU's tile; finish the dbeta row sums
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, C>(acc, [&](int r, int s) { return tM[r * LDC + s]; },
-                        [&](int s, int j) { return tT[j * LDC + s]; });
+        {   // dT T^T into pair W; finish the first dbeta part
+            float c2[4][4];
+            zero(c2);
+            mma_tile<4, 4, false, false, true, true>(c2, opA, opT, f.m0, f.n64);
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) tW[(ty + 16 * m) * LDC + tx + 16 * n2] = acc[m][n2];
-            if (tid < 64) {
-                float s = 0.f;
-                for (int j = 0; j < 16; ++j) s += red[j * 64 + tid];
-                dbr[tid] = s;
+                for (int e = 0; e < 4; e += 2)
+                    st_pair(sm, pair_hi(P_W), pair_lo(P_W), 128, f.row(e), f.col64(nt), c2[nt][e],
+                            c2[nt][e + 1]);
+            if (tid < 64) dbr[tid] = red[256 + tid] + red[320 + tid];
+        }
+        __syncthreads();
+        {   // sdA = strict_lower(-T^T (dT T^T)) into pair A
+            float c2[4][4];
+            zero(c2);
+            mma_tile<4, 4, true, true, true, true>(c2, opT, opW, f.m0, f.n64);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e), j = f.col64(nt);
+                    st_pair(sm, pair_hi(P_A), pair_lo(P_A), 128, r, j, j < r ? -c2[nt][e] : 0.f,
+                            j + 1 < r ? -c2[nt][e + 1] : 0.f);
+                }
+        }
+        __syncthreads();
+        {   // dM = tril_incl(dP U^T) into pair W; diag(beta) sdA into pair T
+            float c2[4][4];
+            zero(c2);
+            mma_tile<4, 4, false, false, true, true>(c2, opP, opU, f.m0, f.n64);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e), s = f.col64(nt);
+                    st_pair(sm, pair_hi(P_W), pair_lo(P_W), 128, r, s, s <= r ? c2[nt][e] : 0.f,
+                            s + 1 <= r ? c2[nt][e + 1] : 0.f);
+                }
+            for (int e2 = tid; e2 < 64 * 32; e2 += NTH) {
+                const int r = e2 >> 5, s = 2 * (e2 & 31);
+                const float2 a = ld_pair(sm, pair_hi(P_A), pair_lo(P_A), 128, r, s);
+                st_pair(sm, pair_hi(P_T), pair_lo(P_T), 128, r, s, bet[r] * a.x, bet[r] * a.y);
             }
-        }
-        __syncthreads();
-        {   // sdA = strict_lower(-T^T tmp) over M's tile
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, C>(acc, [&](int r, int s) { return tT[s * LDC + r]; },
-                        [&](int s, int j) { return tW[s * LDC + j]; });
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) {
-                    const int r = ty + 16 * m, j = tx + 16 * n2;
-                    tM[r * LDC + j] = j < r ? -acc[m][n2] : 0.f;
-                }
-        }
-        __syncthreads();
-        {   // dM = tril_incl(dP U^T) over the tmp tile
-            float acc[4][4];
-            zero(acc);
-            mm<4, 4, R>(acc, [&](int r, int i) { return tP[r * LDC + i]; },
-                        [&](int i, int s) { return tU[s * LDC + i]; });
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int n2 = 0; n2 < 4; ++n2) {
-                    const int r = ty + 16 * m, s = tx + 16 * n2;
-                    tW[r * LDC + s] = s <= r ? acc[m][n2] : 0.f;
-                }
         }
         __syncthreads();
         const size_t part_base = (size_t)rb * p.T;
-        auto qk_idx = [&](int r, int c2) {
-            return ((part_base + tok0 + r) * p.H + h) * DK + c2;
-        };
+        auto qk_idx = [&](int r, int col) { return ((part_base + tok0 + r) * p.H + h) * DK + col; };
         {   // dq = dP S + dM K
-            float acc[4][8];
-            zero(acc);
-            mm<4, 8, R>(acc, [&](int r, int i) { return tP[r * LDC + i]; },
-                        [&](int i, int c2) { return Ss[i * LDS + c2]; });
-            mm<4, 8, C>(acc, [&](int r, int s) { return tW[r * LDC + s]; },
-                        [&](int s, int c2) { return bf(Ks + s * LDH + c2); });
+            float c8[8][4];
+            zero(c8);
+            mma_tile<8, 4, false, true, true, true>(c8, opP, opS, f.m0, f.n128);
+            mma_tile<8, 4, false, true, true, false>(c8, opW, opK, f.m0, f.n128);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = ty + 16 * m;
-                if (r < nvalid)
+            for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-                    for (int n2 = 0; n2 < 8; ++n2) p.dq_part[qk_idx(r, tx + 16 * n2)] = acc[m][n2];
-            }
-        }
-        {   // dk = beta sdA K + dM^T Q + U dS^ - dY S + sdA^T beta K; dbeta += k . (sdA K)
-            float acc[4][8];
-            zero(acc);
-            mm<4, 8, C>(acc, [&](int r, int s) { return tM[r * LDC + s]; },
-                        [&](int s, int c2) { return bf(Ks + s * LDH + c2); });
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = ty + 16 * m;
-                float part = 0.f;
-#pragma unroll
-                for (int n2 = 0; n2 < 8; ++n2) {
-                    part = fmaf(bf(Ks + r * LDH + tx + 16 * n2), acc[m][n2], part);
-                    acc[m][n2] *= bet[r];
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e);
+                    if (r < nvalid)
+                        *reinterpret_cast<float2*>(p.dq_part + qk_idx(r, f.col128(nt))) =
+                            make_float2(c8[nt][e], c8[nt][e + 1]);
                 }
-                red[tx * 64 + r] = part;
-            }
-            mm<4, 8, C>(acc, [&](int r, int s) { return tW[s * LDC + r]; },
-                        [&](int s, int c2) { return bf(Qs + s * LDH + c2); });
-            mm<4, 8, R>(acc, [&](int r, int i) { return tU[r * LDC + i]; },
-                        [&](int i, int c2) { return Ds[i * LDS + c2]; });
-            mm<4, 8, R>(acc, [&](int r, int i) { return -tY[r * LDC + i]; },
-                        [&](int i, int c2) { return Ss[i * LDS + c2]; });
-            mm<4, 8, C>(acc, [&](int r, int s) { return tM[s * LDC + r]; },
-                        [&](int s, int c2) { return bet[s] * bf(Ks + s * LDH + c2); });
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = ty + 16 * m;
-                if (r < nvalid)
-#pragma unroll
-                    for (int n2 = 0; n2 < 8; ++n2) p.dk_part[qk_idx(r, tx + 16 * n2)] = acc[m][n2];
-            }
         }
-        {   // ecol += rowsum(dS^ * S), four lanes per row
-            const int i = tid >> 2, part = tid & 3;
-            float s = 0.f;
-            for (int c2 = part; c2 < DK; c2 += 4) s = fmaf(Ds[i * LDS + c2], Ss[i * LDS + c2], s);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (part == 0) ecol[i] += s;
+        {   // dk = diag(beta) sdA K + dM^T Q + U dS^ - dY S + (diag(beta) sdA)^T K;
+            // dbeta second part k_r . (sdA K)_r
+            float c8[8][4];
+            zero(c8);
+            mma_tile<8, 4, false, true, true, false>(c8, opA, opK, f.m0, f.n128);
+            float part[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e), col = f.col128(nt);
+                    const float2 kk = __bfloat1622float2(
+                        *reinterpret_cast<const __nv_bfloat162*>(sm + OFF_K + swz(r, col, 256)));
+                    part[e >> 1] = fmaf(kk.x, c8[nt][e], fmaf(kk.y, c8[nt][e + 1], part[e >> 1]));
+                    c8[nt][e] *= bet[r];
+                    c8[nt][e + 1] *= bet[r];
+                }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float s = part[q];
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (f.t == 0) red[(6 + (w >> 2)) * 64 + f.m0 + f.g + 8 * q] = s;
+            }
+            mma_tile<8, 4, true, true, true, false>(c8, opW, opQ, f.m0, f.n128);
+            mma_tile<8, 4, false, true, true, true>(c8, opU, opD, f.m0, f.n128);
+            mma_tile<8, 4, false, true, true, true>(c8, opX, opS, f.m0, f.n128);
+            mma_tile<8, 4, true, true, true, false>(c8, opT, opK, f.m0, f.n128);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int r = f.row(e);
+                    if (r < nvalid)
+                        *reinterpret_cast<float2*>(p.dk_part + qk_idx(r, f.col128(nt))) =
+                            make_float2(c8[nt][e], c8[nt][e + 1]);
+                }
+        }
+        {   // rowsum(dS^ * S) per value channel, into red rows 0-1
+            float part[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const float2 s2 = ld_pair(sm, OFF_SH, OFF_SL, 256, f.row(e), f.col128(nt));
+                    part[e >> 1] = fmaf(Dm[nt][e], s2.x, fmaf(Dm[nt][e + 1], s2.y, part[e >> 1]));
+                }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float s = part[q];
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (f.t == 0) red[(w >> 2) * 64 + f.m0 + f.g + 8 * q] = s;
+            }
         }
         __syncthreads();
-        // E (with the state term on the last token) over Gamma's tile; dbeta out
+        // E with the state term on the chunk's last token, into G; dbeta out
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int n2 = 0; n2 < 4; ++n2) {
-                const int r = ty + 16 * m, i = tx + 16 * n2;
-                tG[r * LDC + i] = E[m][n2] + (r == C - 1 ? ecol[i] : 0.f);
+            for (int e = 0; e < 4; e += 2) {
+                const int r = f.row(e), i = f.col64(nt);
+                float a0 = E[nt][e], a1 = E[nt][e + 1];
+                if (r == C - 1) {
+                    a0 += ecol[i] + red[i] + red[64 + i];
+                    a1 += ecol[i + 1] + red[i + 1] + red[64 + i + 1];
+                }
+                *reinterpret_cast<float2*>(G + gidx(r, i)) = make_float2(a0, a1);
             }
-        if (tid < 64 && tid < nvalid) {
-            float s = dbr[tid];
-            for (int j = 0; j < 16; ++j) s += red[j * 64 + tid];
-            p.db_part[(part_base + tok0 + tid) * p.H + h] = s;
-        }
-        {   // D <- dS^ + dP^T Q - dY^T K
-            float acc[4][8];
-            zero(acc);
-            mm<4, 8, C>(acc, [&](int i, int r) { return tP[r * LDC + i]; },
-                        [&](int r, int c2) { return bf(Qs + r * LDH + c2); });
-            mm<4, 8, C>(acc, [&](int i, int r) { return -tY[r * LDC + i]; },
-                        [&](int r, int c2) { return bf(Ks + r * LDH + c2); });
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int n2 = 0; n2 < 8; ++n2) Ds[(ty + 16 * m) * LDS + tx + 16 * n2] += acc[m][n2];
-        }
+        if (tid < nvalid)
+            p.db_part[(part_base + tok0 + tid) * p.H + h] = dbr[tid] + red[384 + tid] + red[448 + tid];
+        // D <- dS^ + dP^T Q - dY^T K
+        mma_tile<8, 4, true, true, true, false>(Dm, opP, opQ, f.m0, f.n128);
+        mma_tile<8, 4, true, true, true, false>(Dm, opX, opK, f.m0, f.n128);
         __syncthreads();
         if (tid < 64) {   // dalpha = reverse cumulative sum of E over tokens / alpha
             float run = 0.f;
             for (int r = C - 1; r >= 0; --r) {
-                run += tG[r * LDC + tid];
+                run += G[gidx(r, tid)];
                 if (r < nvalid) {
                     const int64_t at = vidx(tok0 + r, tid);
                     p.dalpha[at] = run / p.alpha[at];
@@ -545,10 +699,16 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
         }
         __syncthreads();
     }
-    if (p.dS0) store_state(p.dS0 + ((size_t)n * p.H + h) * st_rows + (size_t)row0 * DK, Ds);
+    if (p.dS0) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; e += 2)
+                *reinterpret_cast<float2*>(p.dS0 + head_state + f.row(e) * DK + f.col128(nt)) =
+                    make_float2(Dm[nt][e], Dm[nt][e + 1]);
+    }
 }
 
-// dq, dk and dbeta: sums over the row blocks, in block order.
 __global__ void kda_backward_reduce(const BwdParams p, float* __restrict__ dq,
                                     float* __restrict__ dk, float* __restrict__ dbeta) {
     if (*p.status != 0) return;
