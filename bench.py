@@ -188,16 +188,15 @@ MMA_FLOPS_PER_BLOCK_CHUNK = (2 * 2 * 128 * 128 * 128 + 2 * 128 * 64 * 128
                              + 3 * 2 * 128 * 64 * 64)
 
 
-# Multiply-adds the backward kernel issues per (64-value-row block, 64-token
-# chunk), d_k = 128: the forward sweep (K K^T, Y, U, S update: 1,835,008) and
-# the backward sweep (K K^T, Q K^T, Y, U, E, dU, dT, dX, dT T^T, dA, dM, dq, dk,
-# D: 9,437,184), each a product of 64 x 64 x 128, 64 x 64 x 64 or 64 x 128 x 64.
+# Multiply-adds of the chunkwise backward per (64-value-row block, 64-token
+# chunk), d_k = 128, each product counted once: the forward sweep (K K^T, Y,
+# U, S update: 1,835,008) and the backward sweep (K K^T, Q K^T, Y, U, E, dU,
+# dT, dX, dT T^T, dA, dM, dq, dk, D: 9,437,184).
 BWD_FMA_PER_BLOCK_CHUNK = 1_835_008 + 9_437_184
-
-
-def fp32_peak():
-    """fp32 CUDA-core peak (TFLOP/s): 152 SMs x 128 FMA lanes x 2 flops x 2.07 GHz."""
-    return 152 * 128 * 2 * 2.07e9 / 1e12
+# The same products as the kernel issues them on the tensor cores: a product
+# with one hi/lo-split operand runs twice, with two split operands three
+# times (forward sweep 3,407,872, backward sweep 21,495,808).
+BWD_MMA_FMA_PER_BLOCK_CHUNK = 3_407_872 + 21_495_808
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -543,8 +542,11 @@ def run_component(args):
                        + 2 * spec.d_v * spec.d_k * 4)
         units, unit = bh, "state-updates/s"
         desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
-    elif args.workload == "backward":
+    elif args.workload in ("backward", "backward_small"):
         spec = synth.PREFILL
+        if args.workload == "backward_small":   # the profiling case: 512 tokens per sequence
+            import dataclasses
+            spec = dataclasses.replace(spec, len_lo=512, len_hi=512)
         d = synth.prefill_inputs(spec)
         dO, dS_T = synth.backward_cotangents(d)
         g = {key: (d[key].to(dev) if d[key] is not None else None)
@@ -567,8 +569,14 @@ def run_component(args):
                               stream=stream)
         units, unit = T, "tokens/s"
         nchunks = sum((n + spec.chunk - 1) // spec.chunk for n in d["lengths"])
+        # HBM bytes the gradients need at the least: inputs and dO, dS_T read once,
+        # the six gradients written once (the workspace traffic is extra)
+        state = N * H * d_v * d_k * 4
+        nbytes = T * H * (2 * d_k * 2 + 2 * d_v * 2 + d_v * 4 + 4 + 2 * d_k * 4
+                          + 2 * d_v * 4 + 4) + 3 * state
         bwd_flops = 2 * BWD_FMA_PER_BLOCK_CHUNK * nchunks * H * (d_v // 64)
-        desc = (f"backward of the prefill workload: N={N}, T={T}, H={H}, d_k={d_k}, d_v={d_v}, "
+        bwd_mma_flops = 2 * BWD_MMA_FMA_PER_BLOCK_CHUNK * nchunks * H * (d_v // 64)
+        desc = (f"{args.workload}: kda_backward, N={N}, T={T}, H={H}, d_k={d_k}, d_v={d_v}, "
                 f"chunk={spec.chunk}; dO bf16, dS_T fp32; all six gradients fp32")
     else:
         gate = {"prefill_head_gate": "head", "prefill_log_gate": "log_bf16"}.get(args.workload)
@@ -633,14 +641,17 @@ def run_component(args):
                 "frac": achieved / hbm_peak, "traffic": None,
                 "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_src}
     l2 = "no flush: inputs exceed L2"
-    if args.workload == "backward":
-        # fp32 CUDA-core arithmetic bounds the backward kernel, not HBM
-        tflops = bwd_flops / (ms / 1e3) / 1e12
-        roofline = {"bound": "alu", "achieved": tflops, "peak": fp32_peak(), "unit": "TFLOP/s",
-                    "frac": tflops / fp32_peak(), "traffic": None,
-                    "fp32_flops_per_launch": bwd_flops,
-                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2.07 GHz"}
-        l2 = "no flush: inputs exceed L2"
+    if args.workload in ("backward", "backward_small"):
+        # the products run on the tensor cores (bf16 mma.sync): that pipe, not HBM,
+        # is the roofline; the algorithmic fp32-equivalent rate is reported beside it
+        tpeak, tsrc = bf16_peak()
+        tflops = bwd_mma_flops / (ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": tflops / tpeak, "traffic": None,
+                    "mma_flops_per_launch": bwd_mma_flops, "peak_source": tsrc,
+                    "algorithmic_flops_per_launch": bwd_flops,
+                    "algorithmic_tflops": bwd_flops / (ms / 1e3) / 1e12,
+                    "hbm_equivalent_gbs": achieved}
     if args.workload == "l2_resident":
         # inputs stay in L2 between launches: the tensor pipe, not HBM, is the roofline
         tpeak, tsrc = bf16_peak()
@@ -672,14 +683,15 @@ def main(argv=None):
     p.add_argument("--workload",
                    choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
                             "l2_resident", "prefill_head_gate", "prefill_log_gate",
-                            "backward"],
+                            "backward", "backward_small"],
                    default="varlen",
                    help="varlen (default): the full step; others time one kernel alone "
                         "(varlen_prefill: the varlen batch's prefill without the decode steps; "
                         "l2_resident: the chunk kernel with its inputs in L2, against the "
                         "tensor-core peak; prefill_head_gate / prefill_log_gate: the prefill "
                         "workload with a per-head fp32 gate / a bf16 log-alpha gate; "
-                        "backward: kda_backward on the prefill workload)")
+                        "backward: kda_backward on the prefill workload; backward_small: "
+                        "the same with 512 tokens per sequence, for profiling)")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)

@@ -66,7 +66,9 @@ enum { P_A = 0, P_T, P_X, P_U, P_P, P_W, N_PAIR };
 constexpr int OFF_G = OFF_PAIR + N_PAIR * PAIR;
 constexpr int OFF_RED = OFF_G + 64 * 64 * 4;     // fp32 [8][64]
 constexpr int OFF_MISC = OFF_RED + 8 * 64 * 4;   // beta, gamma_C, ecol, dbeta (64 each)
-constexpr int SMEM_BYTES = OFF_MISC + 4 * 64 * 4;
+constexpr int OFF_V = OFF_MISC + 4 * 64 * 4;     // the chunk's V and dO, swizzled 64 x 64 bf16
+constexpr int OFF_DO = OFF_V + SMALL;
+constexpr int SMEM_BYTES = OFF_DO + SMALL;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 __host__ __device__ constexpr int pair_hi(int p) { return OFF_PAIR + p * PAIR; }
@@ -79,6 +81,7 @@ struct BwdParams {
     int32_t N, H, d_v, nrb;
     int64_t T;
     float* ckpt;              // [slots][H][d_v][DK], slot = t0 / C + n + chunk
+    uint4* tbuf;              // [slots][H][nrb] the chunk's T pair (PAIR bytes)
     float *dq_part, *dk_part; // [nrb][T][H][DK]
     float* db_part;           // [nrb][T][H]
     float *dv, *dalpha;       // [T][H][d_v]
@@ -180,14 +183,39 @@ __device__ __forceinline__ float2 ld_pair(const char* sm, int off_hi, int off_lo
     return make_float2(h.x + l.x, h.y + l.y);
 }
 
-__device__ __forceinline__ float2 ld_bf2(const __nv_bfloat16* p) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+// (row, col) and (row, col + 1) of a swizzled 64 x 64 bf16 tile, as floats.
+__device__ __forceinline__ float2 ld_tile2(const char* sm, int off, int row, int col) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + off + swz(row, col, 128)));
 }
+
+// Asynchronous copy of this block's 64 channels of V (and dO) for tokens
+// tok0 .. tok0 + 63 into swizzled tiles; rows at or past nvalid are zero-filled.
+__device__ void prefetch_vd(const BwdParams& p, char* sm, int64_t tok0, int nvalid, int h,
+                            int row0, bool with_do) {
+    const int64_t vstride = (int64_t)p.H * p.d_v;
+#pragma unroll
+    for (int e = threadIdx.x; e < 2 * 64 * 8; e += NTH) {
+        const int which = e >> 9, row = (e >> 3) & 63, c = e & 7;
+        if (which == 1 && !with_do) break;
+        const __nv_bfloat16* base = which ? p.dO : p.v;
+        const bool ok = row < nvalid;
+        const __nv_bfloat16* src = ok ? base + (tok0 + row) * vstride + (int64_t)h * p.d_v + row0 + 8 * c
+                                      : base;
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(sm + (which ? OFF_DO : OFF_V) +
+                                                                swz(row, 8 * c, 128));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+                     :: "r"(dst), "l"(src), "r"(ok ? 16 : 0) : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_vd() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // Rows tok0 .. tok0 + 63 of a [T][H][DK] bf16 tensor into a swizzled 64 x 128
 // tile (rows at or past nvalid are zero).
 __device__ void load_rows(char* sm, int off, const __nv_bfloat16* src, int64_t tok0, int nvalid,
                           int H, int h) {
+#pragma unroll
     for (int e = threadIdx.x; e < 64 * 16; e += NTH) {
         const int row = e >> 4, c = e & 15;
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
@@ -214,10 +242,12 @@ struct Frag {
     __device__ int col128(int nt) const { return n128 + 8 * nt + 2 * t; }
 };
 
-// Per-chunk inputs shared by both sweeps: K (and Q), beta, Gamma, gamma_C and
-// T = (I + diag(beta) strict_lower(K K^T))^-1 as a hi/lo pair.
+// Per-chunk inputs shared by both sweeps: K (and Q in the backward sweep), beta,
+// Gamma, gamma_C and T = (I + diag(beta) strict_lower(K K^T))^-1 as a hi/lo pair.
+// The forward sweep builds T and keeps a copy at `tglob`; the backward sweep
+// loads it from there.
 __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nvalid, int h,
-                            int row0, bool with_q, const Frag& f) {
+                            int row0, bool backward, uint4* tglob, const Frag& f) {
     float* G = reinterpret_cast<float*>(sm + OFF_G);
     float* Lf = reinterpret_cast<float*>(sm + pair_hi(P_A));
     float* Tf = reinterpret_cast<float*>(sm + pair_hi(P_T));
@@ -225,18 +255,35 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
     float* gC = bet + 64;
     const int tid = threadIdx.x;
     load_rows(sm, OFF_K, p.k, tok0, nvalid, p.H, h);
-    if (with_q) load_rows(sm, OFF_Q, p.q, tok0, nvalid, p.H, h);
+    if (backward) load_rows(sm, OFF_Q, p.q, tok0, nvalid, p.H, h);
     if (tid < C) bet[tid] = tid < nvalid ? p.beta[(tok0 + tid) * p.H + h] : 0.f;
-    if (tid >= 64 && tid < 128) {   // Gamma, one value channel per thread
-        const int i = tid - 64;
-        const float* al = p.alpha + (tok0 * p.H + h) * (int64_t)p.d_v + row0 + i;
+    {   // Gamma: four threads per value channel, 16 tokens each, products scanned across them
+        const int i = tid >> 2, part = tid & 3;
         const int64_t stride = (int64_t)p.H * p.d_v;
-        float run = 1.f;
-        for (int r = 0; r < C; ++r) {
-            if (r < nvalid) run *= al[r * stride];
-            G[gidx(r, i)] = run;
-        }
-        gC[i] = run;
+        const float* al = p.alpha + ((tok0 + 16 * part) * p.H + h) * (int64_t)p.d_v + row0 + i;
+        float a[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a[j] = 16 * part + j < nvalid ? al[j * stride] : 1.f;
+#pragma unroll
+        for (int j = 1; j < 16; ++j) a[j] *= a[j - 1];
+        float s = a[15], y;
+        y = __shfl_up_sync(0xffffffffu, s, 1);
+        if (part >= 1) s *= y;
+        y = __shfl_up_sync(0xffffffffu, s, 2);
+        if (part >= 2) s *= y;
+        float before = __shfl_up_sync(0xffffffffu, s, 1);
+        if (part == 0) before = 1.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) G[gidx(16 * part + j, i)] = before * a[j];
+        if (part == 3) gC[i] = s;
+    }
+    uint4* tsm = reinterpret_cast<uint4*>(sm + pair_hi(P_T));
+    if (backward) {
+#pragma unroll
+        for (int e = tid; e < PAIR / 16; e += NTH) tsm[e] = tglob[e];
+        wait_vd();
+        __syncthreads();
+        return;
     }
     for (int e = tid; e < C * C; e += NTH) Tf[gidx(e >> 6, e & 63)] = (e >> 6) == (e & 63) ? 1.f : 0.f;
     __syncthreads();
@@ -281,7 +328,10 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
             st_pair(sm, pair_hi(P_T), pair_lo(P_T), 128, e >> 5, 2 * (e & 31), v[q].x, v[q].y);
         }
     }
+    wait_vd();
     __syncthreads();
+#pragma unroll
+    for (int e = tid; e < PAIR / 16; e += NTH) tglob[e] = tsm[e];
 }
 
 __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p) {
@@ -311,6 +361,9 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
     const size_t head_state = ((size_t)n * p.H + h) * st_rows + (size_t)row0 * DK;
     auto ckpt_at = [&](int c) {
         return p.ckpt + ((size_t)(slot0 + c) * p.H + h) * st_rows + (size_t)row0 * DK;
+    };
+    auto tbuf_at = [&](int c) {
+        return p.tbuf + (((size_t)(slot0 + c) * p.H + h) * p.nrb + rb) * (PAIR / 16);
     };
     const int64_t vstride = (int64_t)p.H * p.d_v;
     auto vidx = [&](int64_t tok, int i) { return tok * vstride + (int64_t)h * p.d_v + row0 + i; };
@@ -346,7 +399,8 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
                 for (int e = 0; e < 4; e += 2)
                     *reinterpret_cast<float2*>(ck + f.row(e) * DK + f.col128(nt)) =
                         make_float2(Sm[nt][e], Sm[nt][e + 1]);
-            chunk_setup(p, sm, tok0, nvalid, h, row0, false, f);
+            prefetch_vd(p, sm, tok0, nvalid, h, row0, false);
+            chunk_setup(p, sm, tok0, nvalid, h, row0, false, tbuf_at(c), f);
             {   // X = diag(beta) (V / Gamma - K S^T)
                 float cY[4][4];
                 zero(cY);
@@ -356,8 +410,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
 #pragma unroll
                     for (int e = 0; e < 4; e += 2) {
                         const int r = f.row(e), i = f.col64(nt);
-                        const float2 vv = r < nvalid ? ld_bf2(p.v + vidx(tok0 + r, i))
-                                                     : make_float2(0.f, 0.f);
+                        const float2 vv = ld_tile2(sm, OFF_V, r, i);
                         const float y0 = vv.x / G[gidx(r, i)] - cY[nt][e];
                         const float y1 = vv.y / G[gidx(r, i + 1)] - cY[nt][e + 1];
                         st_pair(sm, pair_hi(P_X), pair_lo(P_X), 128, r, i, bet[r] * y0, bet[r] * y1);
@@ -408,6 +461,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
         const int nvalid = min(C, len - c * C);
         {   // the chunk-start state as hi/lo tiles
             const float* ck = ckpt_at(c);
+#pragma unroll
             for (int e = tid; e < 64 * 32; e += NTH) {
                 const int r = e >> 5, col = 4 * (e & 31);
                 const float4 x = *reinterpret_cast<const float4*>(ck + r * DK + col);
@@ -415,7 +469,8 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
                 st_pair(sm, OFF_SH, OFF_SL, 256, r, col + 2, x.z, x.w);
             }
         }
-        chunk_setup(p, sm, tok0, nvalid, h, row0, true, f);
+        prefetch_vd(p, sm, tok0, nvalid, h, row0, true);
+        chunk_setup(p, sm, tok0, nvalid, h, row0, true, tbuf_at(c), f);
         {   // M = tril_incl(Q K^T) into pair A
             float cM[4][4];
             zero(cM);
@@ -438,9 +493,8 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
 #pragma unroll
                 for (int e = 0; e < 4; e += 2) {
                     const int r = f.row(e), i = f.col64(nt);
-                    const bool ok = r < nvalid;
-                    const float2 vv = ok ? ld_bf2(p.v + vidx(tok0 + r, i)) : make_float2(0.f, 0.f);
-                    const float2 dd = ok ? ld_bf2(p.dO + vidx(tok0 + r, i)) : make_float2(0.f, 0.f);
+                    const float2 vv = ld_tile2(sm, OFF_V, r, i);
+                    const float2 dd = ld_tile2(sm, OFF_DO, r, i);
                     const float g0 = G[gidx(r, i)], g1 = G[gidx(r, i + 1)];
                     Y[nt][e] = vv.x / g0 - Y[nt][e];
                     Y[nt][e + 1] = vv.y / g1 - Y[nt][e + 1];
@@ -534,7 +588,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
                     const float dy0 = bet[r] * c2[nt][e], dy1 = bet[r] * c2[nt][e + 1];
                     st_pair(sm, pair_hi(P_X), pair_lo(P_X), 128, r, i, -dy0, -dy1);
                     const float g0 = G[gidx(r, i)], g1 = G[gidx(r, i + 1)];
-                    const float2 vv = ok ? ld_bf2(p.v + vidx(tok0 + r, i)) : make_float2(0.f, 0.f);
+                    const float2 vv = ld_tile2(sm, OFF_V, r, i);
                     E[nt][e] -= dy0 * vv.x / g0;
                     E[nt][e + 1] -= dy1 * vv.y / g1;
                     if (ok)
@@ -687,14 +741,29 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
         mma_tile<8, 4, true, true, true, false>(Dm, opP, opQ, f.m0, f.n128);
         mma_tile<8, 4, true, true, true, false>(Dm, opX, opK, f.m0, f.n128);
         __syncthreads();
-        if (tid < 64) {   // dalpha = reverse cumulative sum of E over tokens / alpha
-            float run = 0.f;
-            for (int r = C - 1; r >= 0; --r) {
-                run += G[gidx(r, tid)];
-                if (r < nvalid) {
-                    const int64_t at = vidx(tok0 + r, tid);
-                    p.dalpha[at] = run / p.alpha[at];
-                }
+        {   // dalpha = reverse cumulative sum of E over tokens / alpha; four threads per
+            // value channel, 16 tokens each, sums scanned across them
+            const int i = tid >> 2, part = tid & 3;
+            float e[16], a[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int r = 16 * part + j;
+                e[j] = G[gidx(r, i)];
+                a[j] = r < nvalid ? p.alpha[vidx(tok0 + r, i)] : 1.f;
+            }
+#pragma unroll
+            for (int j = 14; j >= 0; --j) e[j] += e[j + 1];
+            float s = e[0], y;
+            y = __shfl_down_sync(0xffffffffu, s, 1);
+            if (part <= 2) s += y;
+            y = __shfl_down_sync(0xffffffffu, s, 2);
+            if (part <= 1) s += y;
+            float after = __shfl_down_sync(0xffffffffu, s, 1);
+            if (part == 3) after = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int r = 16 * part + j;
+                if (r < nvalid) p.dalpha[vidx(tok0 + r, i)] = (e[j] + after) / a[j];
             }
         }
         __syncthreads();
@@ -749,6 +818,7 @@ BackwardLayout backward_layout(int32_t num_seqs, int64_t total_tokens, int32_t H
     const size_t nrb = (size_t)(d_v > 0 ? d_v : 0) / R;
     const size_t slots = (T + C - 1) / C + N;
     L.ckpt = take(slots * H * (size_t)d_v * DK * sizeof(float));
+    L.tbuf = take(slots * H * nrb * (size_t)PAIR);
     L.dq_part = take(nrb * T * H * DK * sizeof(float));
     L.dk_part = take(nrb * T * H * DK * sizeof(float));
     L.db_part = take(nrb * T * H * sizeof(float));
@@ -770,6 +840,7 @@ cudaError_t launch_backward(const BackwardArgs& a, const BackwardLayout& L, char
     p.N = a.num_seqs; p.H = a.H; p.d_v = a.d_v; p.nrb = a.d_v / R;
     p.T = a.total_tokens;
     p.ckpt = reinterpret_cast<float*>(ws + L.ckpt);
+    p.tbuf = reinterpret_cast<uint4*>(ws + L.tbuf);
     p.dq_part = reinterpret_cast<float*>(ws + L.dq_part);
     p.dk_part = reinterpret_cast<float*>(ws + L.dk_part);
     p.db_part = reinterpret_cast<float*>(ws + L.db_part);

@@ -78,11 +78,12 @@ struct DecodeArgs {
 // Backward pass (kda_backward.cu).  Buffers appended to the base workspace:
 //   ckpt     fp32 [T / 64 + N][H][d_v][d_k]   chunk-start states; chunk c of
 //            sequence n (first token t0) in slot t0 / 64 + n + c
+//   tbuf     [T / 64 + N][H][d_v / 64] x 16 KB  each chunk's T as bf16 hi/lo
 //   dq_part  fp32 [d_v / 64][T][H][d_k]       dq of each 64-row block
 //   dk_part  fp32 [d_v / 64][T][H][d_k]
 //   db_part  fp32 [d_v / 64][T][H]
 struct BackwardLayout {
-    size_t ckpt = 0, dq_part = 0, dk_part = 0, db_part = 0, end = 0;
+    size_t ckpt = 0, tbuf = 0, dq_part = 0, dk_part = 0, db_part = 0, end = 0;
 };
 BackwardLayout backward_layout(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_v);
 

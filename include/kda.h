@@ -251,9 +251,10 @@ kda_status kda_decode_step_gates(const void* q, const void* k, const void* v,
 
 /*
  * Bytes of device workspace kda_backward needs, or 0 for a shape it does not
- * support.  About (total_tokens / 64 + num_seqs) x H x d_v x d_k x 4 bytes of
- * chunk-start states plus 2 x d_v / 64 x total_tokens x H x d_k x 4 bytes of
- * per-block partial sums.  Contents need no initialisation.
+ * support: for d_k = 128, about (total_tokens / 64 + num_seqs) x H x d_v x 768
+ * bytes of per-chunk states and triangular factors, plus
+ * 2 x d_v / 64 x total_tokens x H x d_k x 4 bytes of per-block partial sums.
+ * Contents need no initialisation.
  */
 size_t kda_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
                                    int32_t d_k, int32_t d_v, int32_t chunk);
