@@ -128,10 +128,10 @@ __device__ __forceinline__ void mma_tile(float (&c)[NT][4], const Op& A, const O
                                          int n0) {
     const int l = threadIdx.x & 31;
     const int r8 = l & 7, j1 = (l >> 3) & 1, j2 = l >> 4;
-#pragma unroll 2
+#pragma unroll 1
     for (int ks = 0; ks < KS; ++ks) {
         const int k = 16 * ks;
-        uint32_t ah[4], al[4];
+        uint32_t ah[4], al[4], bh[NT / 2][4], bl[NT / 2][4];
         const uint32_t aoff = TA ? swz(k + r8 + 8 * j2, m0 + 8 * j1, A.wb)
                                  : swz(m0 + r8 + 8 * j1, k + 8 * j2, A.wb);
         if (TA) ldsm4t(A.hi + aoff, ah); else ldsm4(A.hi + aoff, ah);
@@ -141,19 +141,19 @@ __device__ __forceinline__ void mma_tile(float (&c)[NT][4], const Op& A, const O
             const int n = n0 + 16 * np;
             const uint32_t boff = TB ? swz(k + r8 + 8 * j1, n + 8 * j2, B.wb)
                                      : swz(n + r8 + 8 * j2, k + 8 * j1, B.wb);
-            uint32_t bh[4], bl[4];
-            if (TB) ldsm4t(B.hi + boff, bh); else ldsm4(B.hi + boff, bh);
-            if (BLO) { if (TB) ldsm4t(B.lo + boff, bl); else ldsm4(B.lo + boff, bl); }
-            mma16816(c[2 * np], ah, bh[0], bh[1]);
-            mma16816(c[2 * np + 1], ah, bh[2], bh[3]);
-            if (BLO) {
-                mma16816(c[2 * np], ah, bl[0], bl[1]);
-                mma16816(c[2 * np + 1], ah, bl[2], bl[3]);
-            }
-            if (ALO) {
-                mma16816(c[2 * np], al, bh[0], bh[1]);
-                mma16816(c[2 * np + 1], al, bh[2], bh[3]);
-            }
+            if (TB) ldsm4t(B.hi + boff, bh[np]); else ldsm4(B.hi + boff, bh[np]);
+            if (BLO) { if (TB) ldsm4t(B.lo + boff, bl[np]); else ldsm4(B.lo + boff, bl[np]); }
+        }
+        // pass by pass over all n-tiles, so that dependent MMAs are NT apart
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(c[nt], ah, bh[nt >> 1][2 * (nt & 1)], bh[nt >> 1][2 * (nt & 1) + 1]);
+        if (BLO) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(c[nt], ah, bl[nt >> 1][2 * (nt & 1)], bl[nt >> 1][2 * (nt & 1) + 1]);
+        }
+        if (ALO) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(c[nt], al, bh[nt >> 1][2 * (nt & 1)], bh[nt >> 1][2 * (nt & 1) + 1]);
         }
     }
 }
@@ -188,41 +188,48 @@ __device__ __forceinline__ float2 ld_tile2(const char* sm, int off, int row, int
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm + off + swz(row, col, 128)));
 }
 
-// Asynchronous copy of this block's 64 channels of V (and dO) for tokens
-// tok0 .. tok0 + 63 into swizzled tiles; rows at or past nvalid are zero-filled.
-__device__ void prefetch_vd(const BwdParams& p, char* sm, int64_t tok0, int nvalid, int h,
-                            int row0, bool with_do) {
-    const int64_t vstride = (int64_t)p.H * p.d_v;
-#pragma unroll
-    for (int e = threadIdx.x; e < 2 * 64 * 8; e += NTH) {
-        const int which = e >> 9, row = (e >> 3) & 63, c = e & 7;
-        if (which == 1 && !with_do) break;
-        const __nv_bfloat16* base = which ? p.dO : p.v;
-        const bool ok = row < nvalid;
-        const __nv_bfloat16* src = ok ? base + (tok0 + row) * vstride + (int64_t)h * p.d_v + row0 + 8 * c
-                                      : base;
-        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(sm + (which ? OFF_DO : OFF_V) +
-                                                                swz(row, 8 * c, 128));
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
-                     :: "r"(dst), "l"(src), "r"(ok ? 16 : 0) : "memory");
-    }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
+__device__ __forceinline__ void cp16(char* dst, const void* src, bool ok) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+                 :: "r"(d), "l"(src), "r"(ok ? 16 : 0) : "memory");
 }
 
-__device__ __forceinline__ void wait_vd() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-
-// Rows tok0 .. tok0 + 63 of a [T][H][DK] bf16 tensor into a swizzled 64 x 128
-// tile (rows at or past nvalid are zero).
-__device__ void load_rows(char* sm, int off, const __nv_bfloat16* src, int64_t tok0, int nvalid,
-                          int H, int h) {
+// Asynchronous copies of one chunk's inputs into shared memory: K and this
+// block's 64 channels of V and alpha (alpha into G), plus Q, dO and the
+// chunk's T (from `tglob`) in the backward sweep.  Rows at or past nvalid are
+// zero-filled.
+__device__ void prefetch_chunk(const BwdParams& p, char* sm, int64_t tok0, int nvalid, int h,
+                               int row0, bool backward, const uint4* tglob) {
+    const int tid = threadIdx.x;
+    const int64_t vstride = (int64_t)p.H * p.d_v;
 #pragma unroll
-    for (int e = threadIdx.x; e < 64 * 16; e += NTH) {
+    for (int e = tid; e < 64 * 16; e += NTH) {   // K, Q: 64 rows of 16 pieces
         const int row = e >> 4, c = e & 15;
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (row < nvalid)
-            x = *reinterpret_cast<const uint4*>(src + ((tok0 + row) * H + h) * DK + 8 * c);
-        *reinterpret_cast<uint4*>(sm + off + swz(row, 8 * c, 256)) = x;
+        const bool ok = row < nvalid;
+        const int64_t off = ok ? ((tok0 + row) * p.H + h) * DK + 8 * c : 0;
+        cp16(sm + OFF_K + swz(row, 8 * c, 256), p.k + off, ok);
+        if (backward) cp16(sm + OFF_Q + swz(row, 8 * c, 256), p.q + off, ok);
     }
+#pragma unroll
+    for (int e = tid; e < 64 * 8; e += NTH) {    // V, dO: 64 rows of 8 pieces
+        const int row = e >> 3, c = e & 7;
+        const bool ok = row < nvalid;
+        const int64_t off = ok ? (tok0 + row) * vstride + (int64_t)h * p.d_v + row0 + 8 * c : 0;
+        cp16(sm + OFF_V + swz(row, 8 * c, 128), p.v + off, ok);
+        if (backward) cp16(sm + OFF_DO + swz(row, 8 * c, 128), p.dO + off, ok);
+    }
+#pragma unroll
+    for (int e = tid; e < 64 * 16; e += NTH) {   // alpha: 64 rows of 16 groups of 4 channels
+        const int row = e >> 4, c = 4 * (e & 15);
+        const bool ok = row < nvalid;
+        const int64_t off = ok ? (tok0 + row) * vstride + (int64_t)h * p.d_v + row0 + c : 0;
+        cp16(sm + OFF_G + 4 * gidx(row, c), p.alpha + off, ok);
+    }
+    if (backward) {
+#pragma unroll
+        for (int e = tid; e < PAIR / 16; e += NTH) cp16(sm + pair_hi(P_T) + 16 * e, tglob + e, true);
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 
 // Fragment coordinates of the calling thread: a 64 x 64 output is tiled by the
@@ -254,16 +261,18 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
     float* bet = reinterpret_cast<float*>(sm + OFF_MISC);
     float* gC = bet + 64;
     const int tid = threadIdx.x;
-    load_rows(sm, OFF_K, p.k, tok0, nvalid, p.H, h);
-    if (backward) load_rows(sm, OFF_Q, p.q, tok0, nvalid, p.H, h);
     if (tid < C) bet[tid] = tid < nvalid ? p.beta[(tok0 + tid) * p.H + h] : 0.f;
-    {   // Gamma: four threads per value channel, 16 tokens each, products scanned across them
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    __syncthreads();
+    {   // Gamma over alpha in G: four threads per value channel, 16 tokens each,
+        // products scanned across them
         const int i = tid >> 2, part = tid & 3;
-        const int64_t stride = (int64_t)p.H * p.d_v;
-        const float* al = p.alpha + ((tok0 + 16 * part) * p.H + h) * (int64_t)p.d_v + row0 + i;
         float a[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) a[j] = 16 * part + j < nvalid ? al[j * stride] : 1.f;
+        for (int j = 0; j < 16; ++j) {
+            const int r = 16 * part + j;
+            a[j] = r < nvalid ? G[gidx(r, i)] : 1.f;
+        }
 #pragma unroll
         for (int j = 1; j < 16; ++j) a[j] *= a[j - 1];
         float s = a[15], y;
@@ -277,11 +286,7 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
         for (int j = 0; j < 16; ++j) G[gidx(16 * part + j, i)] = before * a[j];
         if (part == 3) gC[i] = s;
     }
-    uint4* tsm = reinterpret_cast<uint4*>(sm + pair_hi(P_T));
     if (backward) {
-#pragma unroll
-        for (int e = tid; e < PAIR / 16; e += NTH) tsm[e] = tglob[e];
-        wait_vd();
         __syncthreads();
         return;
     }
@@ -328,8 +333,8 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
             st_pair(sm, pair_hi(P_T), pair_lo(P_T), 128, e >> 5, 2 * (e & 31), v[q].x, v[q].y);
         }
     }
-    wait_vd();
     __syncthreads();
+    const uint4* tsm = reinterpret_cast<const uint4*>(sm + pair_hi(P_T));
 #pragma unroll
     for (int e = tid; e < PAIR / 16; e += NTH) tglob[e] = tsm[e];
 }
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
                 for (int e = 0; e < 4; e += 2)
                     *reinterpret_cast<float2*>(ck + f.row(e) * DK + f.col128(nt)) =
                         make_float2(Sm[nt][e], Sm[nt][e + 1]);
-            prefetch_vd(p, sm, tok0, nvalid, h, row0, false);
+            prefetch_chunk(p, sm, tok0, nvalid, h, row0, false, nullptr);
             chunk_setup(p, sm, tok0, nvalid, h, row0, false, tbuf_at(c), f);
             {   // X = diag(beta) (V / Gamma - K S^T)
                 float cY[4][4];
@@ -459,6 +464,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
     for (int c = nc - 1; c >= 0; --c) {
         const int64_t tok0 = t0 + (int64_t)c * C;
         const int nvalid = min(C, len - c * C);
+        prefetch_chunk(p, sm, tok0, nvalid, h, row0, true, tbuf_at(c));
         {   // the chunk-start state as hi/lo tiles
             const float* ck = ckpt_at(c);
 #pragma unroll
@@ -469,7 +475,6 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
                 st_pair(sm, OFF_SH, OFF_SL, 256, r, col + 2, x.z, x.w);
             }
         }
-        prefetch_vd(p, sm, tok0, nvalid, h, row0, true);
         chunk_setup(p, sm, tok0, nvalid, h, row0, true, tbuf_at(c), f);
         {   // M = tril_incl(Q K^T) into pair A
             float cM[4][4];
