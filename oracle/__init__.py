@@ -16,6 +16,10 @@ Three forms live here, each written independently of the others:
 * ``dense_form.run`` -- numpy, tiny sizes only: the same recurrence expanded
   into one explicit matrix product per step,
   S_t = diag(alpha_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T.
+
+``attnres`` (numpy, fp64) is the reference of a second workload on the same
+page, Attention Residuals, plain and blocked ("Kimi (AI)", section
+"Attention Residuals").
 """
 from __future__ import annotations
 
