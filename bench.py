@@ -542,6 +542,47 @@ def run_component(args):
                        + 2 * spec.d_v * spec.d_k * 4)
         units, unit = bh, "state-updates/s"
         desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
+    elif args.workload == "attnres":
+        # Blocked Attention Residuals over a 64-layer network (8 blocks of 8),
+        # 16384 tokens of width 2048, bf16; synthetic layer outputs stand in
+        # for the layers.  One step = the 64 layers' inputs, called as a model
+        # would: block sums stored as they complete, an in-place running sum.
+        spec = synth.ATTNRES
+        x = synth.attnres_inputs(spec, device=dev)
+        T, d = spec.T, spec.d
+        nblk = len(spec.block_sizes)
+        blocks = torch.empty((nblk + 1, T, d), dtype=torch.bfloat16, device=dev)
+        blocks[0] = x["h0"]
+        running = torch.empty((T, d), device=dev)
+        hbuf = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        outs, qs = x["outs"], x["queries"]
+        calls = []   # (nb, partial, h_last, partial_out, block_out) per layer
+        layer = 0
+        for n, size in enumerate(spec.block_sizes, start=1):
+            for i in range(size):
+                if i == 0 and n == 1:
+                    calls.append((1, None, None, None, None))
+                elif i == 0:
+                    calls.append((n - 1, running, outs[layer - 1], None, blocks[n - 1]))
+                elif i == 1:
+                    calls.append((n, None, outs[layer - 1], running, None))
+                else:
+                    calls.append((n, running, outs[layer - 1], running, None))
+                layer += 1
+
+        def launch():
+            for li, (nb, part, last, pout, bout) in enumerate(calls):
+                kda.attnres_layer(blocks[:nb], qs[li], partial=part, h_last=last,
+                                  partial_out=pout, block_out=bout, h=hbuf, stream=stream)
+        row = T * d
+        nbytes = 0
+        for nb, part, last, pout, bout in calls:
+            nbytes += nb * row * 2 + row * 2 + d * 4          # sources, h, q
+            nbytes += (row * 4 if part is not None else 0) + (row * 2 if last is not None else 0)
+            nbytes += (row * 4 if pout is not None else 0) + (row * 2 if bout is not None else 0)
+        units, unit = T, "tokens/s"
+        desc = (f"attnres: Blocked Attention Residuals, 64 layers in 8 blocks of 8, T={T}, d={d}, "
+                f"bf16 sources and outputs, fp32 running sum; one step = 64 attnres_layer calls")
     elif args.workload in ("backward", "backward_small"):
         spec = synth.PREFILL
         if args.workload == "backward_small":   # the profiling case: 512 tokens per sequence
@@ -683,7 +724,7 @@ def main(argv=None):
     p.add_argument("--workload",
                    choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
                             "l2_resident", "prefill_head_gate", "prefill_log_gate",
-                            "backward", "backward_small"],
+                            "backward", "backward_small", "attnres"],
                    default="varlen",
                    help="varlen (default): the full step; others time one kernel alone "
                         "(varlen_prefill: the varlen batch's prefill without the decode steps; "
@@ -691,7 +732,8 @@ def main(argv=None):
                         "tensor-core peak; prefill_head_gate / prefill_log_gate: the prefill "
                         "workload with a per-head fp32 gate / a bf16 log-alpha gate; "
                         "backward: kda_backward on the prefill workload; backward_small: "
-                        "the same with 512 tokens per sequence, for profiling)")
+                        "the same with 512 tokens per sequence, for profiling; attnres: "
+                        "Blocked Attention Residuals over a 64-layer network)")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)

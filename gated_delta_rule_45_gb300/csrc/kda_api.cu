@@ -1,5 +1,6 @@
 // C ABI of libkda: argument validation, workspace layout and kernel dispatch.
 // Every entry point is declared and documented in include/kda.h.
+#include "attnres.h"
 #include "kda_internal.h"
 
 #include <mutex>
@@ -320,6 +321,43 @@ kda_status kda_backward(const void* q, const void* k, const void* v, const float
     a.total_tokens = total_tokens; a.H = H; a.d_v = d_v;
     a.dq = dq; a.dk = dk; a.dv = dv; a.dalpha = dalpha; a.dbeta = dbeta; a.dS0 = dS0;
     return kda::launch_backward(a, L, ws, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status attnres_layer(const void* blocks, int32_t num_blocks, const float* partial,
+                         const void* h_last, float* partial_out, void* block_out,
+                         const float* q, float scale, int64_t T, int32_t d, kda_dtype dtype,
+                         void* h, kda_stream_t stream) {
+    if (num_blocks < 0 || T < 0 || d < 1) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    const bool has_p = partial || h_last;
+    const int64_t m = (int64_t)num_blocks + (has_p ? 1 : 0);
+    if (m < 1) return KDA_ERR_INVALID_ARG;
+    if ((partial_out || block_out) && !has_p) return KDA_ERR_INVALID_ARG;
+    if (d % 8 != 0 || m > 64) return KDA_ERR_UNSUPPORTED;
+    if (T == 0) return KDA_OK;
+    if (!q || !h || (num_blocks > 0 && !blocks)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {blocks, partial, h_last, partial_out, block_out, q, h};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+    const size_t row = (size_t)T * d;
+    const void* ins[] = {blocks, partial, h_last, q};
+    const size_t in_n[] = {(size_t)num_blocks * row * esz, row * 4, row * esz, (size_t)d * 4};
+    const void* outs[] = {h, partial_out, block_out};
+    const size_t out_n[] = {row * esz, row * 4, row * esz};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 4; ++i) {
+            if (o == 1 && i == 1 && partial_out == partial) continue;   // in place
+            if (overlaps(outs[o], out_n[o], ins[i], in_n[i])) return KDA_ERR_INVALID_ARG;
+        }
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlaps(outs[o], out_n[o], outs[o2], out_n[o2])) return KDA_ERR_INVALID_ARG;
+    }
+    return kda::launch_attnres(blocks, num_blocks, partial, h_last, partial_out, block_out, q,
+                               scale, T, d, dtype, h, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
 }
 
 const char* kda_status_string(kda_status s) {

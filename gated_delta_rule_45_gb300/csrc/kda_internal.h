@@ -115,6 +115,11 @@ bool prefill_tc_supports(const PrefillArgs& a);
 cudaError_t launch_backward(const BackwardArgs& a, const BackwardLayout& L, char* ws,
                             cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// Blocked Attention Residuals, one layer (attnres.cu; arguments as attnres_layer).
+cudaError_t launch_attnres(const void* blocks, int32_t nb, const float* partial,
+                           const void* h_last, float* partial_out, void* block_out,
+                           const float* q, float scale, int64_t T, int32_t d, kda_dtype dtype,
+                           void* h, cudaStream_t stream);
 
 int sm_count();   // of the current device, cached per device
 

@@ -10,7 +10,8 @@ The names follow the C ABI: ``prefill`` / ``prefill_into`` wrap
 ``kda_decode_step``, ``workspace_size`` wraps ``kda_prefill_workspace_size``,
 ``device_status`` wraps ``kda_prefill_device_status`` and ``backward`` /
 ``backward_into`` / ``backward_workspace_size`` wrap ``kda_backward`` and
-``kda_backward_workspace_size``.
+``kda_backward_workspace_size``; ``attnres_layer`` wraps the Blocked Attention
+Residuals call of ``include/attnres.h``.
 """
 from __future__ import annotations
 
@@ -82,6 +83,9 @@ def load(path: str | None = None):
     lib.kda_backward.restype = ctypes.c_int
     lib.kda_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                  ctypes.c_int, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.attnres_layer.restype = ctypes.c_int
+    lib.attnres_layer.argtypes = [vp, i32, vp, vp, vp, vp, vp, ctypes.c_float, i64, i32,
+                                  ctypes.c_int, vp, vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_version.restype = i32
@@ -352,3 +356,34 @@ def backward(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, chunk: int 
     if check_device_status:
         device_status(ws, stream=stream)
     return grads
+
+
+def attnres_layer(blocks, q, *, partial=None, h_last=None, partial_out=None, block_out=None,
+                  scale=None, h=None, stream=None):
+    """Enqueue attnres_layer: one layer's input under Blocked Attention Residuals.
+
+    blocks: [nb, T, d] (bf16 or fp32; nb may be 0 when partial or h_last is
+    given); q: [d] fp32; partial: [T, d] fp32 or None; h_last: [T, d] like
+    blocks or None; partial_out: [T, d] fp32 or None (may be partial);
+    block_out: [T, d] like blocks or None; scale: default 1/sqrt(d).
+    Returns h [T, d] (allocated when not given)."""
+    nb, T, d = blocks.shape
+    if h is None:
+        h = torch.empty((T, d), dtype=blocks.dtype, device=blocks.device)
+    _check_cuda(blocks, q, partial, h_last, partial_out, block_out, h)
+    if q.dtype != torch.float32:
+        raise TypeError("q must be float32")
+    for t in (partial, partial_out):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("the running sum is float32")
+    for t in (h_last, block_out, h):
+        if t is not None and t.dtype != blocks.dtype:
+            raise TypeError("h_last, block_out and h share the dtype of blocks")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    st = load().attnres_layer(_ptr(blocks) if nb > 0 else None, nb, _ptr(partial), _ptr(h_last),
+                              _ptr(partial_out), _ptr(block_out), _ptr(q), float(scale), T, d,
+                              _dtype_code(blocks), _ptr(h), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "attnres_layer")
+    return h

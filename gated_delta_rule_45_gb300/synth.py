@@ -143,6 +143,38 @@ def backward_cotangents(d: dict, dS_T_std: float = 0.1) -> tuple:
     return dO, dS_T
 
 
+@dataclasses.dataclass(frozen=True)
+class AttnResSpec:
+    """A network of Blocked Attention Residuals: T tokens of width d, layers in
+    blocks of the given sizes (the network input is block 0)."""
+    T: int
+    d: int
+    block_sizes: tuple
+    dtype: str = "bf16"
+    seed: int = 0
+
+
+# 64 layers in 8 blocks of 8 (blocks of sqrt(L) layers), 16384 tokens of width 2048
+ATTNRES = AttnResSpec(T=16384, d=2048, block_sizes=(8,) * 8)
+
+
+def attnres_inputs(spec: AttnResSpec, device="cpu") -> dict:
+    """Draw a network's inputs: h0 [T, d] and every layer's output [L, T, d]
+    ~ N(0, 1) in the storage dtype (stand-ins for the layers, which are outside
+    the library), queries [L, d] ~ N(0, 1) fp32."""
+    gen = torch.Generator(device=device).manual_seed(spec.seed)
+    L = sum(spec.block_sizes)
+    store = _DTYPES[spec.dtype]
+    def normal(shape):
+        x = torch.empty(shape, dtype=torch.float32, device=device)
+        x.normal_(generator=gen)
+        return x
+    h0 = normal((spec.T, spec.d)).to(store)
+    outs = normal((L, spec.T, spec.d)).to(store)
+    queries = normal((L, spec.d))
+    return dict(h0=h0, outs=outs, queries=queries, spec=spec)
+
+
 def decode_inputs(spec: DecodeSpec, generator: torch.Generator | None = None,
                   with_state: bool = True) -> dict:
     """Draw one decode step on the CPU: q, k [B,H,d_k]; v, alpha [B,H,d_v]; beta [B,H]; S."""

@@ -8,7 +8,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "kda.h")
+HEADERS = [os.path.join(ROOT, "include", n) for n in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if n.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -19,9 +20,9 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)
+    names = re.findall(r"\b((?:kda|attnres)_[a-z_0-9]+)\s*\(", text)
     return sorted(set(names))
 
 
@@ -235,3 +236,35 @@ def test_backward_workspace_size(lib):
 ])
 def test_backward_rejects_on_host(lib, kw, expect):
     assert _backward(lib, **kw) == expect
+
+
+def _attnres(lib, **kw):
+    M = 0x1000000
+    args = dict(blocks=_fake(1 * M), nb=3, partial=None, h_last=None, partial_out=None,
+                block_out=None, q=_fake(2 * M), scale=0.1, T=64, d=256, dtype=0, h=_fake(3 * M))
+    args.update(kw)
+    return lib.attnres_layer(args["blocks"], args["nb"], args["partial"], args["h_last"],
+                             args["partial_out"], args["block_out"], args["q"], args["scale"],
+                             args["T"], args["d"], args["dtype"], args["h"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=12), 2),                                   # d not a multiple of 8
+    (dict(nb=65), 2),                                  # more than 64 sources
+    (dict(nb=64, h_last=_fake(4 * 0x1000000)), 2),     # 64 blocks + the running sum
+    (dict(nb=0), 1),                                   # no source at all
+    (dict(nb=-1), 1),
+    (dict(dtype=7), 1),
+    (dict(partial_out=_fake(5 * 0x1000000)), 1),       # running sum out without one in
+    (dict(q=None), 1),
+    (dict(h=_fake(3 * 0x1000000 + 8)), 1),             # misaligned
+    (dict(h=_fake(1 * 0x1000000 + 4096)), 1),          # h inside blocks
+    (dict(h_last=_fake(4 * 0x1000000), block_out=_fake(4 * 0x1000000)), 1),   # block_out is h_last
+])
+def test_attnres_rejects_on_host(lib, kw, expect):
+    assert _attnres(lib, **kw) == expect
+
+
+def test_attnres_empty_is_a_no_op(lib):
+    # T == 0 returns before any CUDA call
+    assert _attnres(lib, T=0) == 0
