@@ -542,12 +542,15 @@ def run_component(args):
                        + 2 * spec.d_v * spec.d_k * 4)
         units, unit = bh, "state-updates/s"
         desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
-    elif args.workload == "attnres":
+    elif args.workload in ("attnres", "attnres_small"):
         # Blocked Attention Residuals over a 64-layer network (8 blocks of 8),
         # 16384 tokens of width 2048, bf16; synthetic layer outputs stand in
         # for the layers.  One step = the 64 layers' inputs, called as a model
         # would: block sums stored as they complete, an in-place running sum.
         spec = synth.ATTNRES
+        if args.workload == "attnres_small":   # the profiling case: 4096 tokens
+            import dataclasses
+            spec = dataclasses.replace(spec, T=4096)
         x = synth.attnres_inputs(spec, device=dev)
         T, d = spec.T, spec.d
         nblk = len(spec.block_sizes)
@@ -581,7 +584,7 @@ def run_component(args):
             nbytes += (row * 4 if part is not None else 0) + (row * 2 if last is not None else 0)
             nbytes += (row * 4 if pout is not None else 0) + (row * 2 if bout is not None else 0)
         units, unit = T, "tokens/s"
-        desc = (f"attnres: Blocked Attention Residuals, 64 layers in 8 blocks of 8, T={T}, d={d}, "
+        desc = (f"{args.workload}: Blocked Attention Residuals, 64 layers in 8 blocks of 8, T={T}, d={d}, "
                 f"bf16 sources and outputs, fp32 running sum; one step = 64 attnres_layer calls")
     elif args.workload in ("backward", "backward_small"):
         spec = synth.PREFILL
@@ -724,7 +727,7 @@ def main(argv=None):
     p.add_argument("--workload",
                    choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
                             "l2_resident", "prefill_head_gate", "prefill_log_gate",
-                            "backward", "backward_small", "attnres"],
+                            "backward", "backward_small", "attnres", "attnres_small"],
                    default="varlen",
                    help="varlen (default): the full step; others time one kernel alone "
                         "(varlen_prefill: the varlen batch's prefill without the decode steps; "
@@ -733,7 +736,8 @@ def main(argv=None):
                         "workload with a per-head fp32 gate / a bf16 log-alpha gate; "
                         "backward: kda_backward on the prefill workload; backward_small: "
                         "the same with 512 tokens per sequence, for profiling; attnres: "
-                        "Blocked Attention Residuals over a 64-layer network)")
+                        "Blocked Attention Residuals over a 64-layer network; attnres_small: "
+                        "the same with 4096 tokens, for profiling)")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)

@@ -9,10 +9,11 @@
 // block just finished), formed on the fly in fp32 and optionally written back
 // in fp32 and in the storage type.
 //
-// HBM-bound: each source is read once per token (a second read for the
-// weighted sum comes from L1).  One CTA per token at a time, every thread a
-// 16-byte piece of the hidden vector; per-source dot products are reduced
-// with warp shuffles, then across warps in shared memory; the softmax is fp32.
+// HBM-bound: each source is read once per token (the second read, for the
+// weighted sum, is served by L1/L2).  One CTA per token at a time, every
+// thread a 16-byte piece of the hidden vector, the pieces of up to four
+// stored blocks in flight together; per-source dot products are reduced with
+// warp shuffles, then across warps in shared memory; the softmax is fp32.
 #include "attnres.h"
 #include "kda_internal.h"
 
@@ -22,8 +23,8 @@ namespace {
 constexpr int kMaxSources = 64;
 constexpr int kThreads = 256;
 
-// One 16-byte piece of a row as floats, through the read-only path (load) or
-// stored (store).
+// One 16-byte piece of a row: loaded raw through the read-only path, then
+// unpacked to floats; stored from floats.
 template <typename T>
 struct Vec;
 template <>
@@ -36,9 +37,6 @@ struct Vec<__nv_bfloat16> {
             x[2 * i] = __uint_as_float(w[i] << 16);
             x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
         }
-    }
-    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[8]) {
-        unpack(__ldg(reinterpret_cast<const uint4*>(p)), x);
     }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&x)[8]) {
         uint32_t w[4];
@@ -53,14 +51,19 @@ struct Vec<__nv_bfloat16> {
 template <>
 struct Vec<float> {
     static constexpr int N = 4;
-    static __device__ __forceinline__ void load(const float* p, float (&x)[4]) {
-        const float4 u = __ldg(reinterpret_cast<const float4*>(p));
-        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    static __device__ __forceinline__ void unpack(const uint4 u, float (&x)[4]) {
+        x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
     }
     static __device__ __forceinline__ void store(float* p, const float (&x)[4]) {
         *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
     }
 };
+
+template <typename T>
+__device__ __forceinline__ uint4 ld_raw(const T* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
 
 // V fp32 values of the running sum: plain accesses, since the kernel may write
 // where it reads (partial_out == partial).
@@ -92,15 +95,19 @@ struct AttnResParams {
     float scale;
 };
 
+constexpr int kBatch = 4;   // stored blocks whose pieces are in flight together
+constexpr int kCtasPerSm = 4;   // resident CTAs: 64 registers a thread
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads) attnres_kernel(const AttnResParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) attnres_kernel(const AttnResParams p) {
     constexpr int V = Vec<T>::N;
     __shared__ float red[kThreads / 32][kMaxSources];
     __shared__ float wgt[kMaxSources];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     const bool has_p = p.partial || p.h_last;
-    const int m = p.nb + (has_p ? 1 : 0);
+    const int nb = p.nb;
+    const int m = nb + (has_p ? 1 : 0);
     const int pieces = p.d / V;
     const T* blocks = static_cast<const T*>(p.blocks);
     const float* partial = p.partial;
@@ -123,34 +130,62 @@ __global__ void __launch_bounds__(kThreads) attnres_kernel(const AttnResParams p
                 for (int e = 0; e < V; ++e) x[e] += y[e];
             }
             if (h_last) {
-                Vec<T>::load(h_last + row + (size_t)c * V, y);
+                Vec<T>::unpack(ld_raw(h_last + row + (size_t)c * V), y);
 #pragma unroll
                 for (int e = 0; e < V; ++e) x[e] += y[e];
             }
         };
-        // pass 1: q . s_j for every source; the running sum is stored on the way
-        for (int j = 0; j < m; ++j) {
+        auto qpiece = [&](int c, float (&qv)[V]) {
+#pragma unroll
+            for (int e = 0; e < V; e += 4) {
+                const float4 qq = __ldg(reinterpret_cast<const float4*>(p.q + (size_t)c * V + e));
+                qv[e] = qq.x; qv[e + 1] = qq.y; qv[e + 2] = qq.z; qv[e + 3] = qq.w;
+            }
+        };
+        // pass 1: q . s_j, kBatch stored blocks at a time with their loads in flight together
+        for (int j0 = 0; j0 < nb; j0 += kBatch) {
+            float acc[kBatch];
+#pragma unroll
+            for (int jj = 0; jj < kBatch; ++jj) acc[jj] = 0.f;
+            for (int c = tid; c < pieces; c += blockDim.x) {
+                uint4 raw[kBatch];
+#pragma unroll
+                for (int jj = 0; jj < kBatch; ++jj)
+                    if (j0 + jj < nb) raw[jj] = ld_raw(blocks + (size_t)(j0 + jj) * plane + row + (size_t)c * V);
+                float qv[V];
+                qpiece(c, qv);
+#pragma unroll
+                for (int jj = 0; jj < kBatch; ++jj) {
+                    if (j0 + jj < nb) {
+                        float x[V];
+                        Vec<T>::unpack(raw[jj], x);
+#pragma unroll
+                        for (int e = 0; e < V; ++e) acc[jj] = fmaf(x[e], qv[e], acc[jj]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < kBatch; ++jj) {
+                float a = acc[jj];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                if (lane == 0 && j0 + jj < nb) red[warp][j0 + jj] = a;
+            }
+        }
+        if (has_p) {   // the running sum, stored on the way
             float acc = 0.f;
             for (int c = tid; c < pieces; c += blockDim.x) {
                 float x[V], qv[V];
-                if (j < p.nb) {
-                    Vec<T>::load(blocks + (size_t)j * plane + row + (size_t)c * V, x);
-                } else {
-                    running(c, x);
-                    if (partial_out) st_f32<V>(partial_out + row + (size_t)c * V, x);
-                    if (block_out) Vec<T>::store(block_out + row + (size_t)c * V, x);
-                }
-#pragma unroll
-                for (int e = 0; e < V; e += 4) {
-                    const float4 qq = __ldg(reinterpret_cast<const float4*>(p.q + (size_t)c * V + e));
-                    qv[e] = qq.x; qv[e + 1] = qq.y; qv[e + 2] = qq.z; qv[e + 3] = qq.w;
-                }
+                running(c, x);
+                if (partial_out) st_f32<V>(partial_out + row + (size_t)c * V, x);
+                if (block_out) Vec<T>::store(block_out + row + (size_t)c * V, x);
+                qpiece(c, qv);
 #pragma unroll
                 for (int e = 0; e < V; ++e) acc = fmaf(x[e], qv[e], acc);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) red[warp][j] = acc;
+            if (lane == 0) red[warp][nb] = acc;
         }
         __syncthreads();
         if (warp == 0) {   // softmax over the m logits, two per lane
@@ -178,16 +213,32 @@ __global__ void __launch_bounds__(kThreads) attnres_kernel(const AttnResParams p
             if (lane + 32 < m) wgt[lane + 32] = e1 * inv;
         }
         __syncthreads();
-        // pass 2: the weighted sum (the running sum read back from where it was stored)
+        // pass 2: the weighted sum, kBatch stored blocks at a time, then the running sum
         for (int c = tid; c < pieces; c += blockDim.x) {
-            float o[V], x[V];
+            float o[V];
 #pragma unroll
             for (int e = 0; e < V; ++e) o[e] = 0.f;
-            for (int j = 0; j < m; ++j) {
-                if (j < p.nb) Vec<T>::load(blocks + (size_t)j * plane + row + (size_t)c * V, x);
-                else if (partial_out) ld_f32<V>(partial_out + row + (size_t)c * V, x);
+            for (int j0 = 0; j0 < nb; j0 += kBatch) {
+                uint4 raw[kBatch];
+#pragma unroll
+                for (int jj = 0; jj < kBatch; ++jj)
+                    if (j0 + jj < nb) raw[jj] = ld_raw(blocks + (size_t)(j0 + jj) * plane + row + (size_t)c * V);
+#pragma unroll
+                for (int jj = 0; jj < kBatch; ++jj) {
+                    if (j0 + jj < nb) {
+                        float x[V];
+                        Vec<T>::unpack(raw[jj], x);
+                        const float w = wgt[j0 + jj];
+#pragma unroll
+                        for (int e = 0; e < V; ++e) o[e] = fmaf(w, x[e], o[e]);
+                    }
+                }
+            }
+            if (has_p) {
+                float x[V];
+                if (partial_out) ld_f32<V>(partial_out + row + (size_t)c * V, x);
                 else running(c, x);
-                const float w = wgt[j];
+                const float w = wgt[nb];
 #pragma unroll
                 for (int e = 0; e < V; ++e) o[e] = fmaf(w, x[e], o[e]);
             }
@@ -208,7 +259,7 @@ cudaError_t launch_attnres(const void* blocks, int32_t nb, const float* partial,
     int threads = (d / vec + 31) / 32 * 32;
     if (threads > kThreads) threads = kThreads;
     const int sms = sm_count();
-    const int64_t grid64 = T < (int64_t)sms * 8 ? T : (int64_t)sms * 8;
+    const int64_t grid64 = T < (int64_t)sms * kCtasPerSm ? T : (int64_t)sms * kCtasPerSm;
     const int grid = grid64 > 0 ? (int)grid64 : 1;
     if (dtype == KDA_BF16)
         attnres_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(p);
