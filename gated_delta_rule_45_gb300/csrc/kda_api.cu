@@ -258,25 +258,39 @@ kda_status kda_decode_step_gates(const void* q, const void* k, const void* v, co
                             stream);
 }
 
-size_t kda_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
-                                   int32_t d_k, int32_t d_v, int32_t chunk) {
+// Bytes kda_backward_gates needs: the backward layout, plus for the gate
+// layouts other than per-channel fp32 the gate expanded per channel and the
+// gradient with respect to it (fp32 [T][H][d_v] each).
+static size_t backward_bytes(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                             int32_t d_v, int32_t chunk, kda_gate_format gate) {
     if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k != 128 || d_v < 64 || d_v % 64 != 0 ||
         chunk != 64)
         return 0;
-    return kda::backward_layout(num_seqs, total_tokens, H, d_v).end;
+    if (gate != KDA_GATE_CHANNEL_F32 && gate != KDA_GATE_HEAD_F32 &&
+        gate != KDA_GATE_CHANNEL_LOG_BF16)
+        return 0;
+    size_t bytes = kda::backward_layout(num_seqs, total_tokens, H, d_v).end;
+    if (gate != KDA_GATE_CHANNEL_F32)
+        bytes += 2 * (((size_t)total_tokens * H * d_v * sizeof(float) + 255) & ~(size_t)255);
+    return bytes;
 }
 
-kda_status kda_backward(const void* q, const void* k, const void* v, const float* alpha,
-                        const float* beta, const float* S0, const int32_t* cu_seqlens,
-                        int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
-                        int32_t d_v, kda_dtype dtype, int32_t chunk, const void* d_o,
-                        const float* dS_T, float* dq, float* dk, float* dv, float* dalpha,
-                        float* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
-                        kda_stream_t stream_) {
+// Validation and launches behind kda_backward / kda_backward_gates.
+static kda_status backward_impl(const void* q, const void* k, const void* v, const void* alpha,
+                                kda_gate_format gate, const float* beta, const float* S0,
+                                const int32_t* cu_seqlens, int32_t num_seqs,
+                                int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                kda_dtype dtype, int32_t chunk, const void* d_o,
+                                const float* dS_T, float* dq, float* dk, float* dv,
+                                float* dalpha, float* dbeta, float* dS0, void* workspace,
+                                size_t workspace_bytes, kda_stream_t stream_) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1)
         return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (gate != KDA_GATE_CHANNEL_F32 && gate != KDA_GATE_HEAD_F32 &&
+        gate != KDA_GATE_CHANNEL_LOG_BF16)
+        return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 || d_k != 128 || d_v % 64 != 0 || d_v > 1024 || chunk != 64)
         return KDA_ERR_UNSUPPORTED;
     if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
@@ -286,7 +300,8 @@ kda_status kda_backward(const void* q, const void* k, const void* v, const float
                              !dalpha || !dbeta))
         return KDA_ERR_INVALID_ARG;
     const kda::BackwardLayout L = kda::backward_layout(num_seqs, total_tokens, H, d_v);
-    if (workspace_bytes < L.end) return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < backward_bytes(num_seqs, total_tokens, H, d_k, d_v, chunk, gate))
+        return KDA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, alpha, beta, S0, cu_seqlens, d_o, dS_T, dq, dk, dv,
                           dalpha, dbeta, dS0, workspace};
     for (const void* p : ptrs)
@@ -294,11 +309,14 @@ kda_status kda_backward(const void* q, const void* k, const void* v, const float
     // no output may overlap an input or another output
     const size_t tq = (size_t)total_tokens * H * d_k, tv = (size_t)total_tokens * H * d_v;
     const size_t ts = (size_t)total_tokens * H, ns = (size_t)num_seqs * H * d_v * d_k;
+    const size_t n_gate = gate == KDA_GATE_HEAD_F32 ? 4 * ts
+                          : gate == KDA_GATE_CHANNEL_LOG_BF16 ? 2 * tv : 4 * tv;
+    const size_t n_dgate = gate == KDA_GATE_HEAD_F32 ? 4 * ts : 4 * tv;
     const void* ins[] = {q, k, v, alpha, beta, S0, d_o, dS_T, workspace};
-    const size_t in_n[] = {2 * tq, 2 * tq, 2 * tv, 4 * tv, 4 * ts, 4 * ns, 2 * tv, 4 * ns,
+    const size_t in_n[] = {2 * tq, 2 * tq, 2 * tv, n_gate, 4 * ts, 4 * ns, 2 * tv, 4 * ns,
                            workspace_bytes};
     const void* outs[] = {dq, dk, dv, dalpha, dbeta, dS0};
-    const size_t out_n[] = {4 * tq, 4 * tq, 4 * tv, 4 * tv, 4 * ts, 4 * ns};
+    const size_t out_n[] = {4 * tq, 4 * tq, 4 * tv, n_dgate, 4 * ts, 4 * ns};
     for (int o = 0; o < 6; ++o) {
         for (int i = 0; i < 9; ++i)
             if (overlaps(outs[o], out_n[o], ins[i], in_n[i])) return KDA_ERR_INVALID_ARG;
@@ -316,11 +334,62 @@ kda_status kda_backward(const void* q, const void* k, const void* v, const float
     if (kda::launch_planner(pa, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (num_seqs == 0) return KDA_OK;
     kda::BackwardArgs a;
-    a.q = q; a.k = k; a.v = v; a.dO = d_o; a.alpha = alpha; a.beta = beta; a.S0 = S0;
+    a.q = q; a.k = k; a.v = v; a.dO = d_o; a.beta = beta; a.S0 = S0;
     a.dS_T = dS_T; a.cu_seqlens = cu_seqlens; a.num_seqs = num_seqs;
     a.total_tokens = total_tokens; a.H = H; a.d_v = d_v;
-    a.dq = dq; a.dk = dk; a.dv = dv; a.dalpha = dalpha; a.dbeta = dbeta; a.dS0 = dS0;
-    return kda::launch_backward(a, L, ws, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dbeta = dbeta; a.dS0 = dS0;
+    if (gate == KDA_GATE_CHANNEL_F32) {
+        a.alpha = static_cast<const float*>(alpha);
+        a.dalpha = dalpha;
+        return kda::launch_backward(a, L, ws, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
+    // the gate per channel and its gradient, in the workspace after the layout
+    const size_t plane = ((size_t)total_tokens * H * d_v * sizeof(float) + 255) & ~(size_t)255;
+    float* ax = reinterpret_cast<float*>(ws + L.end);
+    float* dax = reinterpret_cast<float*>(ws + L.end + plane);
+    a.alpha = ax;
+    a.dalpha = dax;
+    if (kda::launch_gate_expand(alpha, gate, a, ax, pa.status, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (kda::launch_backward(a, L, ws, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    return kda::launch_gate_grad(gate, a, ax, dax, dalpha, pa.status, stream) == cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
+size_t kda_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                   int32_t d_k, int32_t d_v, int32_t chunk) {
+    return backward_bytes(num_seqs, total_tokens, H, d_k, d_v, chunk, KDA_GATE_CHANNEL_F32);
+}
+
+size_t kda_backward_gates_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                         int32_t d_k, int32_t d_v, int32_t chunk,
+                                         kda_gate_format gate_format) {
+    return backward_bytes(num_seqs, total_tokens, H, d_k, d_v, chunk, gate_format);
+}
+
+kda_status kda_backward(const void* q, const void* k, const void* v, const float* alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens,
+                        int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                        int32_t d_v, kda_dtype dtype, int32_t chunk, const void* d_o,
+                        const float* dS_T, float* dq, float* dk, float* dv, float* dalpha,
+                        float* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
+                        kda_stream_t stream) {
+    return backward_impl(q, k, v, alpha, KDA_GATE_CHANNEL_F32, beta, S0, cu_seqlens, num_seqs,
+                         total_tokens, H, d_k, d_v, dtype, chunk, d_o, dS_T, dq, dk, dv, dalpha,
+                         dbeta, dS0, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_backward_gates(const void* q, const void* k, const void* v, const void* alpha,
+                              kda_gate_format gate_format, const float* beta, const float* S0,
+                              const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                              int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                              int32_t chunk, const void* d_o, const float* dS_T, float* dq,
+                              float* dk, float* dv, float* dgate, float* dbeta, float* dS0,
+                              void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    return backward_impl(q, k, v, alpha, gate_format, beta, S0, cu_seqlens, num_seqs,
+                         total_tokens, H, d_k, d_v, dtype, chunk, d_o, dS_T, dq, dk, dv, dgate,
+                         dbeta, dS0, workspace, workspace_bytes, stream);
 }
 
 kda_status attnres_layer(const void* blocks, int32_t num_blocks, const float* partial,

@@ -809,6 +809,49 @@ __global__ void kda_backward_reduce(const BwdParams p, float* __restrict__ dq,
     }
 }
 
+// The gate of one (token, head) per value channel: the head's scalar gate, or
+// exp of the bf16 log gate.  Tokens past cu_seqlens[N] are left alone.
+__global__ void gate_expand_kernel(const void* gate_in, int gate, const int32_t* __restrict__ cu,
+                                   int N, int H, int d_v, float* __restrict__ ax,
+                                   const int32_t* __restrict__ status) {
+    if (*status != 0) return;
+    const int64_t n = (int64_t)cu[N] * H * d_v;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        if (gate == KDA_GATE_HEAD_F32)
+            ax[e] = static_cast<const float*>(gate_in)[e / d_v];
+        else
+            ax[e] = __expf(__bfloat162float(static_cast<const __nv_bfloat16*>(gate_in)[e]));
+    }
+}
+
+// The gradient with respect to the gate in its own layout (chain rule through
+// the expansion): the sum over the head's channels for a scalar gate (one warp
+// per token and head, fixed reduction order), alpha * dL/dalpha for log alpha.
+__global__ void gate_grad_kernel(int gate, const int32_t* __restrict__ cu, int N, int H, int d_v,
+                                 const float* __restrict__ ax, const float* __restrict__ dax,
+                                 float* __restrict__ dgate, const int32_t* __restrict__ status) {
+    if (*status != 0) return;
+    const int64_t th_n = (int64_t)cu[N] * H;
+    if (gate == KDA_GATE_HEAD_F32) {
+        const int lane = threadIdx.x & 31;
+        const int64_t w0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+        const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+        for (int64_t th = w0; th < th_n; th += nw) {
+            float s = 0.f;
+            for (int i = lane; i < d_v; i += 32) s += dax[th * d_v + i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) dgate[th] = s;
+        }
+    } else {
+        const int64_t n = th_n * d_v;
+        for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+             e += (int64_t)gridDim.x * blockDim.x)
+            dgate[e] = ax[e] * dax[e];
+    }
+}
+
 }  // namespace
 
 BackwardLayout backward_layout(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_v) {
@@ -859,6 +902,27 @@ cudaError_t launch_backward(const BackwardArgs& a, const BackwardLayout& L, char
     if (a.total_tokens == 0) return cudaSuccess;
     const int rblocks = 4 * sm_count();
     kda_backward_reduce<<<rblocks > 0 ? rblocks : 1, 256, 0, stream>>>(p, a.dq, a.dk, a.dbeta);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
+
+namespace kda {
+
+cudaError_t launch_gate_expand(const void* gate_in, kda_gate_format gate, const BackwardArgs& a,
+                               float* ax, const int32_t* status, cudaStream_t stream) {
+    const int blocks = 4 * (sm_count() > 0 ? sm_count() : 1);
+    gate_expand_kernel<<<blocks, 256, 0, stream>>>(gate_in, (int)gate, a.cu_seqlens, a.num_seqs,
+                                                   a.H, a.d_v, ax, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate_grad(kda_gate_format gate, const BackwardArgs& a, const float* ax,
+                             const float* dax, float* dgate, const int32_t* status,
+                             cudaStream_t stream) {
+    const int blocks = 4 * (sm_count() > 0 ? sm_count() : 1);
+    gate_grad_kernel<<<blocks, 256, 0, stream>>>((int)gate, a.cu_seqlens, a.num_seqs, a.H, a.d_v,
+                                                 ax, dax, dgate, status);
     return cudaGetLastError();
 }
 

@@ -114,6 +114,14 @@ bool prefill_tc_supports(const PrefillArgs& a);
 // workspace base, planner already enqueued).
 cudaError_t launch_backward(const BackwardArgs& a, const BackwardLayout& L, char* ws,
                             cudaStream_t stream);
+// Gate layouts of the backward pass: the gate expanded per channel (ax) before
+// the chain kernel, and the gradient (dax, per channel) reduced to the gate's
+// layout after it (a: the sizes and cu_seqlens; status: the planner's word).
+cudaError_t launch_gate_expand(const void* gate_in, kda_gate_format gate, const BackwardArgs& a,
+                               float* ax, const int32_t* status, cudaStream_t stream);
+cudaError_t launch_gate_grad(kda_gate_format gate, const BackwardArgs& a, const float* ax,
+                             const float* dax, float* dgate, const int32_t* status,
+                             cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // Blocked Attention Residuals, one layer (attnres.cu; arguments as attnres_layer).
 cudaError_t launch_attnres(const void* blocks, int32_t nb, const float* partial,

@@ -83,6 +83,12 @@ def load(path: str | None = None):
     lib.kda_backward.restype = ctypes.c_int
     lib.kda_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                  ctypes.c_int, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_backward_gates_workspace_size.restype = sz
+    lib.kda_backward_gates_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, ctypes.c_int]
+    lib.kda_backward_gates.restype = ctypes.c_int
+    lib.kda_backward_gates.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, vp, i32, i64, i32,
+                                       i32, i32, ctypes.c_int, i32, vp, vp, vp, vp, vp, vp, vp,
+                                       vp, vp, sz, vp]
     lib.attnres_layer.restype = ctypes.c_int
     lib.attnres_layer.argtypes = [vp, i32, vp, vp, vp, vp, vp, ctypes.c_float, i64, i32,
                                   ctypes.c_int, vp, vp]
@@ -353,6 +359,48 @@ def backward(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, chunk: int 
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     backward_into(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T, grads, ws, chunk=chunk,
                   stream=stream)
+    if check_device_status:
+        device_status(ws, stream=stream)
+    return grads
+
+
+def backward_gates(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, gate: str = "channel",
+                   chunk: int = 64, stream=None, check_device_status: bool = False):
+    """kda_backward_gates: ``backward`` with the forget gate in layout `gate`
+    ("channel", "head" [T, H] fp32, "log_bf16" log alpha [T, H, d_v] bf16).
+    Returns the gradients; "dgate" is the gradient with respect to the gate in
+    its own layout ([T, H] for "head", d/d log alpha for "log_bf16")."""
+    code, adt, arank = _GATES[gate]
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if alpha.dtype != adt or alpha.dim() != arank:
+        raise TypeError(f"gate layout {gate!r} wants a rank-{arank} {adt} tensor")
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T)
+    if cu_seqlens.dtype != torch.int32 or beta.dtype != torch.float32:
+        raise TypeError("cu_seqlens must be int32 and beta float32")
+    if dO.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v and dO must share one dtype")
+    dev = q.device
+    gshape = (T, H) if gate == "head" else (T, H, d_v)
+    grads = {"dq": torch.zeros((T, H, d_k), dtype=torch.float32, device=dev),
+             "dk": torch.zeros((T, H, d_k), dtype=torch.float32, device=dev),
+             "dv": torch.zeros((T, H, d_v), dtype=torch.float32, device=dev),
+             "dgate": torch.zeros(gshape, dtype=torch.float32, device=dev),
+             "dbeta": torch.zeros((T, H), dtype=torch.float32, device=dev),
+             "dS0": torch.zeros((N, H, d_v, d_k), dtype=torch.float32, device=dev)}
+    lib = load()
+    nbytes = int(lib.kda_backward_gates_workspace_size(N, T, H, d_k, d_v, chunk, code))
+    if nbytes == 0:
+        raise KdaError(ERR_UNSUPPORTED, "kda_backward_gates")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = lib.kda_backward_gates(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), code, _ptr(beta),
+                                _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v, _dtype_code(q),
+                                chunk, _ptr(dO), _ptr(dS_T), _ptr(grads["dq"]), _ptr(grads["dk"]),
+                                _ptr(grads["dv"]), _ptr(grads["dgate"]), _ptr(grads["dbeta"]),
+                                _ptr(grads["dS0"]), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_backward_gates")
     if check_device_status:
         device_status(ws, stream=stream)
     return grads

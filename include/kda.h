@@ -296,6 +296,30 @@ kda_status kda_backward(const void* q, const void* k, const void* v, const float
                         float* dbeta, float* dS0, void* workspace, size_t workspace_bytes,
                         kda_stream_t stream);
 
+/* Workspace for kda_backward_gates: kda_backward_workspace_size plus, for the
+ * two non-channel layouts, 2 x total_tokens x H x d_v x 4 bytes (the gate per
+ * channel and its gradient).  0 for an unsupported shape or layout. */
+size_t kda_backward_gates_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                         int32_t d_k, int32_t d_v, int32_t chunk,
+                                         kda_gate_format gate_format);
+
+/*
+ * kda_backward with the forget gate in another layout (kda_gate_format), as
+ * kda_prefill_gates takes it.  `dgate` is the gradient with respect to the
+ * gate in its own layout, fp32: [T][H] for KDA_GATE_HEAD_F32 (the sum of the
+ * per-channel gradients: one gate drives every channel of the head),
+ * [T][H][d_v] with respect to log alpha for KDA_GATE_CHANNEL_LOG_BF16
+ * (alpha times the per-channel gradient).  Everything else as kda_backward;
+ * KDA_GATE_CHANNEL_F32 is exactly kda_backward.
+ */
+kda_status kda_backward_gates(const void* q, const void* k, const void* v, const void* alpha,
+                              kda_gate_format gate_format, const float* beta, const float* S0,
+                              const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                              int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                              int32_t chunk, const void* d_o, const float* dS_T, float* dq,
+                              float* dk, float* dv, float* dgate, float* dbeta, float* dS0,
+                              void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
 /* Static description of a status code.  Never NULL. */
 const char* kda_status_string(kda_status s);
 

@@ -177,6 +177,43 @@ def pin_naive_linear_attention_gradients(lib) -> float:
     return err
 
 
+def pin_gate_layout_chain_rules(lib) -> float:
+    """One gate per head drives every value channel, so its gradient is the sum
+    of the per-channel gradients; for log alpha it is alpha times the
+    per-channel gradient.  Both checked by central differences of the dense-form
+    loss with the gate expanded (the reductions the gate-layout tests apply to
+    the oracle's per-channel gradient)."""
+    rng = np.random.default_rng(25)
+    lengths, H, d_k, d_v = [4, 3], 2, 4, 3
+    q, k, v, alpha, beta, S0, cu, dO, dS_T = _problem(rng, lengths, H, d_k, d_v)
+    T = q.shape[0]
+    head = alpha[:, :, :1].astype(np.float64)                     # [T, H, 1]
+    logs = np.log(alpha.astype(np.float64))                         # [T, H, d_v]
+    a_head = np.ascontiguousarray(np.broadcast_to(head, (T, H, d_v)), dtype=np.float32)
+    g_head = oracle.backward(q, k, v, a_head, beta, S0, cu, dO, dS_T, lib=lib)["dalpha"].sum(axis=2)
+    g_log = oracle.backward(q, k, v, alpha, beta, S0, cu, dO, dS_T, lib=lib)["dalpha"] * np.exp(logs)
+    qf, kf, vf, bf, s0 = _as_f64(q, k, v, beta, S0)
+    h = 1e-6
+    fd_head = np.zeros((T, H))
+    for t in range(T):
+        for hh in range(H):
+            pm = []
+            for sgn in (1, -1):
+                a = np.broadcast_to(head, (T, H, d_v)).copy()
+                a[t, hh, :] += sgn * h
+                pm.append(_dense_loss(qf, kf, vf, a, bf, s0, cu, dO, dS_T))
+            fd_head[t, hh] = (pm[0] - pm[1]) / (2 * h)
+    fd_log = np.zeros((T, H, d_v))
+    for idx in np.ndindex(T, H, d_v):
+        pm = []
+        for sgn in (1, -1):
+            lg = logs.copy()
+            lg[idx] += sgn * h
+            pm.append(_dense_loss(qf, kf, vf, np.exp(lg), bf, s0, cu, dO, dS_T))
+        fd_log[idx] = (pm[0] - pm[1]) / (2 * h)
+    return max(_rel(g_head, fd_head), _rel(g_log, fd_log))
+
+
 # name -> (function, tolerance).  Finite differences with h = 1e-6 in fp64 are
 # good to about 1e-9 relative here; the closed forms to a few hundred roundings.
 PINS = {
@@ -184,6 +221,7 @@ PINS = {
     "fd_directional": (pin_finite_differences_directional, 1e-7),
     "pure_decay_gradients": (pin_pure_decay_gradients, 1e-12),
     "naive_linear_attention_gradients": (pin_naive_linear_attention_gradients, 1e-12),
+    "gate_layout_chain_rules": (pin_gate_layout_chain_rules, 1e-7),
 }
 
 

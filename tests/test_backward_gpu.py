@@ -165,3 +165,38 @@ def test_backward_prefill_workload_sampled():
     """The 8 x 4096-token, 32-head prefill workload at full size; the oracle
     checks three sampled (sequence, head) pairs over all 4096 tokens."""
     _run(synth.PREFILL, pairs=[(0, 0), (3, 17), (7, 31)])
+
+
+@pytest.mark.parametrize("gate", ["head", "log_bf16"])
+def test_backward_gate_layouts(gate):
+    """kda_backward_gates: the gate expanded per channel for the oracle, whose
+    per-channel gradient is reduced to the gate's layout (sum over the head's
+    channels; alpha times it for log alpha)."""
+    spec = synth.PrefillSpec(num_seqs=3, len_lo=40, len_hi=260, H=2, d_k=128, d_v=128,
+                             s0_std=0.1, seed=21)
+    d = synth.prefill_inputs(spec)
+    dO, dS_T = synth.backward_cotangents(d)
+    T, H, d_v = d["v"].shape
+    if gate == "head":
+        g_in = d["alpha"][:, :, 0].contiguous()
+        a_full = g_in[:, :, None].expand(T, H, d_v).contiguous()
+    else:
+        g_in = torch.log(d["alpha"]).to(torch.bfloat16)
+        a_full = torch.exp(g_in.double()).float()
+    d_exp = dict(d, alpha=a_full)
+    dev = parity.to_device(d)
+    g = kda.backward_gates(dev["q"], dev["k"], dev["v"], g_in.cuda(), dev["beta"], dev["S0"],
+                           dev["cu_seqlens"], dO.cuda(), dS_T.cuda(), gate=gate,
+                           check_device_status=True)
+    torch.cuda.synchronize()
+    pairs = [(n, hh) for n in range(spec.num_seqs) for hh in range(H)]
+    ref = _oracle(d_exp, dO, dS_T, pairs)
+    for key in ref:
+        da = ref[key]["dalpha"]
+        n, hh = key
+        a0, a1 = int(d["cu_seqlens"][n]), int(d["cu_seqlens"][n + 1])
+        ref[key]["dalpha"] = da.sum(axis=1) if gate == "head" else \
+            da * a_full[a0:a1, hh].double().numpy()
+    g["dalpha"] = g.pop("dgate")
+    worst = _compare(d, g, ref)
+    assert all(e <= TOL for e in worst.values()), worst
