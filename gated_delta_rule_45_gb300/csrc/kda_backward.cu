@@ -82,6 +82,7 @@ struct BwdParams {
     int64_t T;
     float* ckpt;              // [slots][H][d_v][DK], slot = t0 / C + n + chunk
     uint4* tbuf;              // [slots][H][nrb] the chunk's T pair (PAIR bytes)
+    int32_t tc_ckpt;          // ckpt already written by the tensor-core forward
     float *dq_part, *dk_part; // [nrb][T][H][DK]
     float* db_part;           // [nrb][T][H]
     float *dv, *dalpha;       // [T][H][d_v]
@@ -195,9 +196,9 @@ __device__ __forceinline__ void cp16(char* dst, const void* src, bool ok) {
 }
 
 // Asynchronous copies of one chunk's inputs into shared memory: K and this
-// block's 64 channels of V and alpha (alpha into G), plus Q, dO and the
-// chunk's T (from `tglob`) in the backward sweep.  Rows at or past nvalid are
-// zero-filled.
+// block's 64 channels of V and alpha (alpha into G), plus Q and dO in the
+// backward sweep and the chunk's stored T when `tglob` is given.  Rows at or
+// past nvalid are zero-filled.
 __device__ void prefetch_chunk(const BwdParams& p, char* sm, int64_t tok0, int nvalid, int h,
                                int row0, bool backward, const uint4* tglob) {
     const int tid = threadIdx.x;
@@ -225,7 +226,7 @@ __device__ void prefetch_chunk(const BwdParams& p, char* sm, int64_t tok0, int n
         const int64_t off = ok ? (tok0 + row) * vstride + (int64_t)h * p.d_v + row0 + c : 0;
         cp16(sm + OFF_G + 4 * gidx(row, c), p.alpha + off, ok);
     }
-    if (backward) {
+    if (tglob) {
 #pragma unroll
         for (int e = tid; e < PAIR / 16; e += NTH) cp16(sm + pair_hi(P_T) + 16 * e, tglob + e, true);
     }
@@ -249,12 +250,12 @@ struct Frag {
     __device__ int col128(int nt) const { return n128 + 8 * nt + 2 * t; }
 };
 
-// Per-chunk inputs shared by both sweeps: K (and Q in the backward sweep), beta,
-// Gamma, gamma_C and T = (I + diag(beta) strict_lower(K K^T))^-1 as a hi/lo pair.
-// The forward sweep builds T and keeps a copy at `tglob`; the backward sweep
-// loads it from there.
+// Per-chunk inputs shared by both sweeps, after prefetch_chunk: beta, Gamma,
+// gamma_C and T = (I + diag(beta) strict_lower(K K^T))^-1 as a hi/lo pair,
+// built here when `build_t` (a copy kept at `tstore` when given), else already
+// prefetched from the forward sweep's copy.
 __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nvalid, int h,
-                            int row0, bool backward, uint4* tglob, const Frag& f) {
+                            int row0, bool build_t, uint4* tstore, const Frag& f) {
     float* G = reinterpret_cast<float*>(sm + OFF_G);
     float* Lf = reinterpret_cast<float*>(sm + pair_hi(P_A));
     float* Tf = reinterpret_cast<float*>(sm + pair_hi(P_T));
@@ -286,7 +287,7 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
         for (int j = 0; j < 16; ++j) G[gidx(16 * part + j, i)] = before * a[j];
         if (part == 3) gC[i] = s;
     }
-    if (backward) {
+    if (!build_t) {
         __syncthreads();
         return;
     }
@@ -334,9 +335,11 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
         }
     }
     __syncthreads();
-    const uint4* tsm = reinterpret_cast<const uint4*>(sm + pair_hi(P_T));
+    if (tstore) {
+        const uint4* tsm = reinterpret_cast<const uint4*>(sm + pair_hi(P_T));
 #pragma unroll
-    for (int e = tid; e < PAIR / 16; e += NTH) tglob[e] = tsm[e];
+        for (int e = tid; e < PAIR / 16; e += NTH) tstore[e] = tsm[e];
+    }
 }
 
 __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p) {
@@ -379,8 +382,9 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
     const Op opA = pop(P_A), opT = pop(P_T), opX = pop(P_X), opU = pop(P_U), opP = pop(P_P),
              opW = pop(P_W);
 
-    // ---- forward sweep: chunk-start states into the workspace ----
-    {
+    // ---- forward sweep: chunk-start states into the workspace (unless the
+    // tensor-core forward has written them) ----
+    if (!p.tc_ckpt) {
         float Sm[8][4];   // this block's rows of S, fp32, in accumulator layout
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -405,7 +409,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
                     *reinterpret_cast<float2*>(ck + f.row(e) * DK + f.col128(nt)) =
                         make_float2(Sm[nt][e], Sm[nt][e + 1]);
             prefetch_chunk(p, sm, tok0, nvalid, h, row0, false, nullptr);
-            chunk_setup(p, sm, tok0, nvalid, h, row0, false, tbuf_at(c), f);
+            chunk_setup(p, sm, tok0, nvalid, h, row0, true, tbuf_at(c), f);
             {   // X = diag(beta) (V / Gamma - K S^T)
                 float cY[4][4];
                 zero(cY);
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
     for (int c = nc - 1; c >= 0; --c) {
         const int64_t tok0 = t0 + (int64_t)c * C;
         const int nvalid = min(C, len - c * C);
-        prefetch_chunk(p, sm, tok0, nvalid, h, row0, true, tbuf_at(c));
+        prefetch_chunk(p, sm, tok0, nvalid, h, row0, true, p.tc_ckpt ? nullptr : tbuf_at(c));
         {   // the chunk-start state as hi/lo tiles
             const float* ck = ckpt_at(c);
 #pragma unroll
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
                 st_pair(sm, OFF_SH, OFF_SL, 256, r, col + 2, x.z, x.w);
             }
         }
-        chunk_setup(p, sm, tok0, nvalid, h, row0, true, tbuf_at(c), f);
+        chunk_setup(p, sm, tok0, nvalid, h, row0, p.tc_ckpt != 0, nullptr, f);
         {   // M = tril_incl(Q K^T) into pair A
             float cM[4][4];
             zero(cM);
@@ -865,8 +869,14 @@ BackwardLayout backward_layout(int32_t num_seqs, int64_t total_tokens, int32_t H
     const size_t N = num_seqs > 0 ? (size_t)num_seqs : 0, T = total_tokens > 0 ? (size_t)total_tokens : 0;
     const size_t nrb = (size_t)(d_v > 0 ? d_v : 0) / R;
     const size_t slots = (T + C - 1) / C + N;
+    L.tc = d_v > 0 && d_v % 128 == 0 && d_v <= 1024;
     L.ckpt = take(slots * H * (size_t)d_v * DK * sizeof(float));
-    L.tbuf = take(slots * H * nrb * (size_t)PAIR);
+    if (L.tc) {
+        L.o_tc = take(T * H * (size_t)d_v * 2);
+        L.st_tc = take(N * H * (size_t)d_v * DK * sizeof(float));
+    } else {
+        L.tbuf = take(slots * H * nrb * (size_t)PAIR);
+    }
     L.dq_part = take(nrb * T * H * DK * sizeof(float));
     L.dk_part = take(nrb * T * H * DK * sizeof(float));
     L.db_part = take(nrb * T * H * sizeof(float));
@@ -889,11 +899,27 @@ cudaError_t launch_backward(const BackwardArgs& a, const BackwardLayout& L, char
     p.T = a.total_tokens;
     p.ckpt = reinterpret_cast<float*>(ws + L.ckpt);
     p.tbuf = reinterpret_cast<uint4*>(ws + L.tbuf);
+    p.tc_ckpt = 0;
+    cudaError_t err;
+    if (L.tc) {   // the tensor-core forward writes the chunk-start states
+        PrefillArgs f = {};
+        f.q = a.q; f.k = a.k; f.v = a.v; f.alpha = a.alpha; f.beta = a.beta; f.S0 = a.S0;
+        f.cu_seqlens = a.cu_seqlens; f.num_seqs = a.num_seqs; f.total_tokens = a.total_tokens;
+        f.H = a.H; f.d_k = DK; f.d_v = a.d_v; f.dtype = KDA_BF16; f.chunk = C;
+        f.o = ws + L.o_tc;
+        f.S_T = reinterpret_cast<float*>(ws + L.st_tc);
+        f.status = reinterpret_cast<int32_t*>(ws + WorkspaceLayout::kStatus);
+        f.counter = reinterpret_cast<int32_t*>(ws + WorkspaceLayout::kCounter);
+        f.order = reinterpret_cast<int32_t*>(ws + WorkspaceLayout::kOrder);
+        f.gate = KDA_GATE_CHANNEL_F32;
+        if ((err = launch_prefill_tc_ckpt(f, p.ckpt, stream)) != cudaSuccess) return err;
+        p.tc_ckpt = 1;
+    }
     p.dq_part = reinterpret_cast<float*>(ws + L.dq_part);
     p.dk_part = reinterpret_cast<float*>(ws + L.dk_part);
     p.db_part = reinterpret_cast<float*>(ws + L.db_part);
     p.dv = a.dv; p.dalpha = a.dalpha; p.dS0 = a.dS0;
-    cudaError_t err = cudaFuncSetAttribute(kda_backward_kernel,
+    err = cudaFuncSetAttribute(kda_backward_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
     const int blocks = a.num_seqs * a.H * p.nrb;

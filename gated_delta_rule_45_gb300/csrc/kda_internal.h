@@ -82,8 +82,13 @@ struct DecodeArgs {
 //   dq_part  fp32 [d_v / 64][T][H][d_k]       dq of each 64-row block
 //   dk_part  fp32 [d_v / 64][T][H][d_k]
 //   db_part  fp32 [d_v / 64][T][H]
+//   o_tc     bf16 [T][H][d_v], st_tc fp32 [N][H][d_v][d_k]: scratch outputs of
+//            the tensor-core forward that writes ckpt (d_v a multiple of 128);
+//            other widths run their own forward sweep and keep T in tbuf
 struct BackwardLayout {
-    size_t ckpt = 0, tbuf = 0, dq_part = 0, dk_part = 0, db_part = 0, end = 0;
+    bool tc = false;
+    size_t ckpt = 0, tbuf = 0, o_tc = 0, st_tc = 0, dq_part = 0, dk_part = 0, db_part = 0,
+           end = 0;
 };
 BackwardLayout backward_layout(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_v);
 
@@ -101,6 +106,9 @@ struct BackwardArgs {
 cudaError_t launch_planner(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+// The tensor-core prefill that also writes every chunk's start state (fp32
+// [slots][H][d_v][d_k], slot t0 / 64 + n + chunk) for the backward pass.
+cudaError_t launch_prefill_tc_ckpt(const PrefillArgs& a, float* ckpt, cudaStream_t stream);
 // The split form: segment planner, three chunk-kernel launches and the scan of
 // the segment maps in between (ws: the workspace base).
 cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, char* ws,

@@ -132,6 +132,9 @@ struct TcParams {
     float* g_out;
     float* P_out;
     const float* alpha_s;   // GATE_SCALAR: alpha [T][H]
+    // GATE_F32_CKPT: fp32 [slots][H][d_v][DK]; chunk c of sequence n starting
+    // at token t0 in slot t0 / C + n + c
+    float* ckpt;
 };
 
 struct ItemInfo {
@@ -143,7 +146,9 @@ struct ItemInfo {
 // [T][H][d_v]; one fp32 gate per (token, head) [T][H] (Gated DeltaNet's
 // scalar gate, broadcast over the value channels); per value channel log alpha
 // in bf16 [T][H][d_v] (half the bytes of the largest prefill input).
-enum { GATE_F32 = 0, GATE_SCALAR = 1, GATE_LOG_BF16 = 2 };
+// GATE_F32_CKPT: the fp32 gate, and every chunk's start state is written to
+// TcParams::ckpt for the backward pass.
+enum { GATE_F32 = 0, GATE_SCALAR = 1, GATE_LOG_BF16 = 2, GATE_F32_CKPT = 3 };
 
 // SPLIT: the kernel serves the split launches (virtual sequences, transition
 // items); the plain instantiation compiles none of that.
@@ -755,6 +760,10 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 p.g_out[((size_t)it.n * p.H + it.h) * p.d_v + ch] = 1.f;
             continue;
         }
+        // GATE_F32_CKPT: this thread's 64 key channels of chunk c's start state
+        auto ckpt_row = [&](int c) {
+            return p.ckpt + (((size_t)(it.t0 / C + it.n + c) * p.H + it.h) * p.d_v + ch) * DK + 64 * h;
+        };
 #pragma unroll 1
         for (int q = 0; q < 2; ++q) {
             float x[32];
@@ -762,6 +771,12 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             for (int j = 0; j < 32; j += 4) {
                 const float4 v4 = init4(32 * q + j);
                 x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
+            }
+            if (GATE == GATE_F32_CKPT) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(ckpt_row(0) + 32 * q + j) =
+                        make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
             }
             stage_state_piece(lane_addr, h, q, x);
         }
@@ -945,6 +960,12 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                                 make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
                     }
                 } else {
+                    if (GATE == GATE_F32_CKPT) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(ckpt_row(c + 1) + 32 * q + j) =
+                                make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    }
                     stage_state_piece(lane_addr, h, q, x);
                 }
             }
@@ -1131,6 +1152,7 @@ bool init_params(const PrefillArgs& a, TcParams& p) {
     p.num_items_p = 0;
     p.g_out = nullptr;
     p.P_out = nullptr;
+    p.ckpt = nullptr;
     return true;
 }
 
@@ -1173,6 +1195,19 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
         case GATE_LOG_BF16: return launch_g<false, GATE_LOG_BF16>(p, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_prefill_tc_ckpt(const PrefillArgs& a, float* ckpt, cudaStream_t stream) {
+    if (!prefill_tc_supports(a) || a.gate != GATE_F32 || !ckpt) return cudaErrorInvalidValue;
+    if (a.total_tokens == 0) return launch_prefill_simt(a, stream);   // no chunk to record
+    TcParams p;
+    if (!init_params(a, p)) return cudaErrorInvalidValue;
+    if (p.num_items == 0) return cudaSuccess;
+    p.ckpt = ckpt;
+    const int sms = sm_count();
+    const int grid = p.num_items < sms ? p.num_items : sms;
+    p.a_ctas = grid;
+    return launch_g<false, GATE_F32_CKPT>(p, grid, stream);
 }
 
 cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, char* ws,
