@@ -67,6 +67,8 @@ def load(path: str | None = None):
     lib.kda_oracle_prefill.restype = ctypes.c_int
     lib.kda_oracle_prefill.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, i32, i64,
                                        i32, i32, i32, vp, vp, i32]
+    lib.kda_oracle_prefill_additive.restype = ctypes.c_int
+    lib.kda_oracle_prefill_additive.argtypes = lib.kda_oracle_prefill.argtypes
     lib.kda_oracle_backward.restype = ctypes.c_int
     lib.kda_oracle_backward.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, i32, i64,
                                         i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32]
@@ -89,14 +91,18 @@ def _as_qkv(x: np.ndarray):
     raise TypeError("q, k, v must be bf16 bit patterns (uint16) or float32, got %s" % x.dtype)
 
 
-def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, nthreads: int = 0, lib=None):
+def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, nthreads: int = 0, lib=None,
+            additive: bool = False):
     """Run the recurrence over a packed batch.
 
     q, k: [T_total, H, d_k]; v: [T_total, H, d_v] (uint16 bf16 bits or float32,
     all three the same).  alpha: [T_total, H, d_v] float32; beta: [T_total, H]
     float32; S0: [N, H, d_v, d_k] float64 or None (zeros); cu_seqlens: [N+1]
     int32.  Returns (o [T_total, H, d_v] float64, S_T [N, H, d_v, d_k] float64).
-    Tokens past cu_seqlens[-1] get o = 0.
+    Tokens past cu_seqlens[-1] get o = 0.  additive=True runs the additive
+    update of linear attention instead of the delta rule (no predict step:
+    S_t = diag(alpha_t) S_{t-1} + beta_t v_t k_t^T), the page's naive linear
+    attention when alpha = beta = 1.
     """
     lib = lib or load()
     q, kind = _as_qkv(q)
@@ -119,9 +125,9 @@ def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, nthreads: int = 0, lib=None
             raise ValueError("S0 must be [N, H, d_v, d_k]")
     o = np.zeros((T, H, d_v), dtype=np.float64)
     S_T = np.zeros((N, H, d_v, d_k), dtype=np.float64)
-    rc = lib.kda_oracle_prefill(_ptr(q), _ptr(k), _ptr(v), kind, _ptr(alpha), _ptr(beta),
-                                _ptr(S0), _ptr(cu), N, T, H, d_k, d_v, _ptr(o), _ptr(S_T),
-                                int(nthreads))
+    fn = lib.kda_oracle_prefill_additive if additive else lib.kda_oracle_prefill
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), kind, _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(cu), N,
+            T, H, d_k, d_v, _ptr(o), _ptr(S_T), int(nthreads))
     if rc != 0:
         raise ValueError("kda_oracle_prefill failed with code %d" % rc)
     return o, S_T
@@ -179,7 +185,7 @@ def backward(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, nthreads: i
     return out
 
 
-def decode_step(q, k, v, alpha, beta, S):
+def decode_step(q, k, v, alpha, beta, S, additive: bool = False):
     """One recurrent step for B independent sequences.
 
     q, k: [B, H, d_k]; v, alpha: [B, H, d_v]; beta: [B, H]; S: [B, H, d_v, d_k]
@@ -188,7 +194,7 @@ def decode_step(q, k, v, alpha, beta, S):
     """
     B = q.shape[0]
     cu = np.arange(B + 1, dtype=np.int32)
-    return prefill(q, k, v, alpha, beta, np.asarray(S, dtype=np.float64), cu)
+    return prefill(q, k, v, alpha, beta, np.asarray(S, dtype=np.float64), cu, additive=additive)
 
 
 def max_threads(lib=None) -> int:

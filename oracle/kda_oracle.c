@@ -64,7 +64,7 @@ static double oracle_load(const void* base, int kind, int64_t idx)
 static void oracle_run_pair(const void* q, const void* k, const void* v, int kind,
                             const float* alpha, const float* beta, const double* S0,
                             int64_t t_begin, int64_t t_end, int32_t n, int32_t h,
-                            int32_t H, int32_t d_k, int32_t d_v,
+                            int32_t H, int32_t d_k, int32_t d_v, int additive,
                             double* o, double* S_T,
                             double* S, double* kt, double* qt, double* vpred)
 {
@@ -86,8 +86,9 @@ static void oracle_run_pair(const void* q, const void* k, const void* v, int kin
             double* row = S + (int64_t)r * d_k;
             for (int32_t c = 0; c < d_k; ++c) row[c] = a * row[c];
         }
-        /* predict: v~ = S~ k_t */
-        for (int32_t r = 0; r < d_v; ++r) {
+        /* predict: v~ = S~ k_t (none in the additive update of linear attention) */
+        for (int32_t r = 0; r < d_v && additive; ++r) vpred[r] = 0.0;
+        for (int32_t r = 0; r < d_v && !additive; ++r) {
             const double* row = S + (int64_t)r * d_k;
             double acc = 0.0;
             for (int32_t c = 0; c < d_k; ++c) acc += row[c] * kt[c];
@@ -117,11 +118,11 @@ static void oracle_run_pair(const void* q, const void* k, const void* v, int kin
  * run in parallel over `nthreads` OpenMP threads (<= 0: library default);
  * the arithmetic of each pair is sequential and does not depend on it.
  */
-int kda_oracle_prefill(const void* q, const void* k, const void* v, int kind,
-                       const float* alpha, const float* beta, const double* S0,
-                       const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
-                       int32_t H, int32_t d_k, int32_t d_v,
-                       double* o, double* S_T, int32_t nthreads)
+static int oracle_prefill_rule(const void* q, const void* k, const void* v, int kind,
+                               const float* alpha, const float* beta, const double* S0,
+                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                               int32_t H, int32_t d_k, int32_t d_v, int additive,
+                               double* o, double* S_T, int32_t nthreads)
 {
     if (num_seqs < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || (kind != 0 && kind != 1)) return 1;
     if (!cu_seqlens || (num_seqs > 0 && (!q || !k || !v || !alpha || !beta || !o))) return 1;
@@ -151,11 +152,40 @@ int kda_oracle_prefill(const void* q, const void* k, const void* v, int kind,
             if (!have_scratch) continue;
             const int32_t n = (int32_t)(p / H), h = (int32_t)(p % H);
             oracle_run_pair(q, k, v, kind, alpha, beta, S0, cu_seqlens[n], cu_seqlens[n + 1],
-                            n, h, H, d_k, d_v, o, S_T, S, kt, qt, vpred);
+                            n, h, H, d_k, d_v, additive, o, S_T, S, kt, qt, vpred);
         }
         free(S); free(kt); free(qt); free(vpred);
     }
     return failed ? 3 : 0;
+}
+
+/* The KDA recurrence over a packed batch (the delta rule). */
+int kda_oracle_prefill(const void* q, const void* k, const void* v, int kind,
+                       const float* alpha, const float* beta, const double* S0,
+                       const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                       int32_t H, int32_t d_k, int32_t d_v,
+                       double* o, double* S_T, int32_t nthreads)
+{
+    return oracle_prefill_rule(q, k, v, kind, alpha, beta, S0, cu_seqlens, num_seqs,
+                               total_tokens, H, d_k, d_v, 0, o, S_T, nthreads);
+}
+
+/*
+ * The same recurrence with the additive update of linear attention instead of
+ * the delta rule: predict is dropped (v~ = 0), so S_t = diag(alpha_t) S_{t-1}
+ * + beta_t v_t k_t^T and o_t = S_t q_t.  With alpha = beta = 1 it is the
+ * page's naive linear attention, S_t = S_{t-1} + v_t k_t^T ("Kimi (AI)",
+ * section "Kimi Delta Attention (KDA)", the line before the three-line
+ * update).  Same arguments and return codes as kda_oracle_prefill.
+ */
+int kda_oracle_prefill_additive(const void* q, const void* k, const void* v, int kind,
+                                const float* alpha, const float* beta, const double* S0,
+                                const int32_t* cu_seqlens, int32_t num_seqs,
+                                int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                double* o, double* S_T, int32_t nthreads)
+{
+    return oracle_prefill_rule(q, k, v, kind, alpha, beta, S0, cu_seqlens, num_seqs,
+                               total_tokens, H, d_k, d_v, 1, o, S_T, nthreads);
 }
 
 /* Number of OpenMP threads a call with nthreads <= 0 would use. */

@@ -230,6 +230,55 @@ def pin_varlen_independence(lib) -> float:
     return err
 
 
+def pin_additive_is_naive_linear_attention(lib) -> float:
+    """The additive update with alpha = beta = 1 and S0 = 0 is the page's naive
+    linear attention, o_t = (sum_{i<=t} v_i k_i^T) q_t, for any keys (here
+    random, not orthogonal: the delta rule would differ)."""
+    rng = np.random.default_rng(8)
+    T, H, d_k, d_v = 14, 2, 6, 5
+    q = _f32(rng.standard_normal((T, H, d_k)))
+    k = _f32(rng.standard_normal((T, H, d_k)))
+    v = _f32(rng.standard_normal((T, H, d_v)))
+    alpha = np.ones((T, H, d_v), np.float32)
+    beta = np.ones((T, H), np.float32)
+    o, S_T = oracle.prefill(q, k, v, alpha, beta, None, np.array([0, T], np.int32), lib=lib,
+                            additive=True)
+    err = 0.0
+    for h in range(H):
+        M = np.zeros((d_v, d_k))
+        for t in range(T):
+            M = M + np.outer(v[t, h].astype(np.float64), k[t, h].astype(np.float64))
+            err = max(err, _rel(o[t, h], M @ q[t, h].astype(np.float64)))
+        err = max(err, _rel(S_T[0, h], M))
+    return err
+
+
+def pin_additive_gated_closed_form(lib) -> float:
+    """The gated additive update unrolled: S_t = diag(G_t) S0 +
+    sum_{i<=t} diag(G_t / G_i) beta_i v_i k_i^T with G_t = prod_{j<=t} alpha_j."""
+    rng = np.random.default_rng(9)
+    T, H, d_k, d_v = 11, 2, 4, 6
+    q = _f32(rng.standard_normal((T, H, d_k)))
+    k = _f32(rng.standard_normal((T, H, d_k)))
+    v = _f32(rng.standard_normal((T, H, d_v)))
+    alpha = _f32(rng.uniform(0.4, 1.0, (T, H, d_v)))
+    beta = _f32(rng.uniform(0.0, 1.0, (T, H)))
+    S0 = rng.standard_normal((1, H, d_v, d_k))
+    o, S_T = oracle.prefill(q, k, v, alpha, beta, S0, np.array([0, T], np.int32), lib=lib,
+                            additive=True)
+    err = 0.0
+    for h in range(H):
+        G = np.cumprod(alpha[:, h].astype(np.float64), axis=0)
+        for t in range(T):
+            St = G[t][:, None] * S0[0, h]
+            for i in range(t + 1):
+                St = St + (G[t] / G[i])[:, None] * float(beta[i, h]) * np.outer(
+                    v[i, h].astype(np.float64), k[i, h].astype(np.float64))
+            err = max(err, _rel(o[t, h], St @ q[t, h].astype(np.float64)))
+        err = max(err, _rel(S_T[0, h], St))
+    return err
+
+
 # name -> (function, tolerance).  Tolerances are a few hundred fp64 roundings.
 PINS = {
     "naive_linear_attention": (pin_naive_linear_attention, 1e-12),
@@ -240,6 +289,8 @@ PINS = {
     "row_permutation": (pin_row_permutation, 1e-13),
     "split_resume": (pin_split_resume, 1e-13),
     "varlen_independence": (pin_varlen_independence, 1e-13),
+    "additive_is_naive_linear_attention": (pin_additive_is_naive_linear_attention, 1e-12),
+    "additive_gated_closed_form": (pin_additive_gated_closed_form, 1e-12),
 }
 
 

@@ -39,6 +39,9 @@ MUTANTS = {
     # off-by-one: beta read from the previous token
     "beta_index": ("const double b = (double)beta[th];",
                    "const double b = (double)beta[th > H ? th - H : th];"),
+    # the additive update keeps the prediction term
+    "additive_predicts": ("for (int32_t r = 0; r < d_v && !additive; ++r) {",
+                          "for (int32_t r = 0; r < d_v; ++r) {"),
 }
 
 
