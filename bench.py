@@ -312,6 +312,14 @@ def run_ours(args):
 
     ev_pf = []
 
+    def decode_all():
+        for i in range(n_dec):
+            x = dec[i]
+            kda.decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S, o_dec[i],
+                            stream=stream)
+
+    graph = None   # the 32 decode steps as one CUDA graph, once warmed up
+
     def step(record=False):
         with torch.cuda.stream(stream):
             if record:
@@ -323,10 +331,10 @@ def run_ours(args):
                              g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
             if record:
                 e1.record(stream)
-            for i in range(n_dec):
-                x = dec[i]
-                kda.decode_step(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S, o_dec[i],
-                                stream=stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                decode_all()
             if record:
                 e2.record(stream)
                 ev_pf.append((e0, e1, e2))
@@ -335,6 +343,20 @@ def run_ours(args):
         step()
     kda.device_status(wsp, stream=stream)
     torch.cuda.synchronize()
+    try:   # decode steps are ~44 us each: replaying them as a graph saves their launches
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            decode_all()
+        torch.cuda.synchronize()
+        graph = gr
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+    except Exception as exc:   # capture is an optimisation; launches stay correct without it
+        print(f"decode graph capture failed ({exc}); launching the steps directly",
+              file=sys.stderr)
+        graph = None
+        torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
     barrier()
@@ -396,6 +418,7 @@ def run_ours(args):
                          "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"},
             "clocks": clock_info,
             "gpu_launches": ours_launches * args.steps,
+            "decode_cuda_graph": graph is not None,
             "e2e": e2e,
         }
         if not args.no_cpu_baseline:

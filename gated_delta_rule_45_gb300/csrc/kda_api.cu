@@ -47,7 +47,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
                         int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                         int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
                         void* workspace, size_t workspace_bytes, kda_prefill_kernel kernel,
-                        kda_stream_t stream_, kda_gate_format gate) {
+                        kda_stream_t stream_, kda_gate_format gate, bool additive) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1)
         return KDA_ERR_INVALID_ARG;
@@ -62,6 +62,9 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     if (d_k % 16 != 0 || d_k > 128 || d_v % 16 != 0 || d_v > 1024) return KDA_ERR_UNSUPPORTED;
     if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
     if (gate != KDA_GATE_CHANNEL_F32 && kernel == KDA_KERNEL_CHUNK_TC_SPLIT)
+        return KDA_ERR_UNSUPPORTED;
+    // the additive update runs on the portable kernel only
+    if (additive && (kernel == KDA_KERNEL_CHUNK_TC || kernel == KDA_KERNEL_CHUNK_TC_SPLIT))
         return KDA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * H > (int64_t)INT32_MAX / 64) return KDA_ERR_UNSUPPORTED;
     if (!cu_seqlens || !workspace || (num_seqs > 0 && !S_T)) return KDA_ERR_INVALID_ARG;
@@ -91,13 +94,14 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S0 = S0;
     a.cu_seqlens = cu_seqlens; a.num_seqs = num_seqs; a.total_tokens = total_tokens;
     a.gate = gate;
+    a.additive = additive ? 1 : 0;
     a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.chunk = chunk; a.o = o; a.S_T = S_T;
     char* ws = static_cast<char*>(workspace);
     a.status = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kStatus);
     a.counter = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kCounter);
     a.order = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kOrder);
 
-    const bool tc_ok = kda::prefill_tc_supports(a);
+    const bool tc_ok = kda::prefill_tc_supports(a) && !additive;
     const bool want_tc = kernel == KDA_KERNEL_CHUNK_TC || kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
     if (want_tc && !tc_ok) return KDA_ERR_UNSUPPORTED;
     const bool use_tc = want_tc || (kernel == KDA_KERNEL_AUTO && tc_ok);
@@ -206,7 +210,7 @@ kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream)
 static kda_status decode_impl(const void* q, const void* k, const void* v, const void* alpha,
                               kda_gate_format gate, const float* beta, float* S, int32_t B,
                               int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype, void* o,
-                              kda_stream_t stream) {
+                              kda_stream_t stream, bool additive = false) {
     if (B < 0 || H < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
     if (gate != KDA_GATE_CHANNEL_F32 && gate != KDA_GATE_HEAD_F32 &&
         gate != KDA_GATE_CHANNEL_LOG_BF16)
@@ -238,6 +242,7 @@ static kda_status decode_impl(const void* q, const void* k, const void* v, const
     kda::DecodeArgs a;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.S = S;
     a.B = B; a.H = H; a.d_k = d_k; a.d_v = d_v; a.dtype = dtype; a.o = o; a.gate = gate;
+    a.additive = additive ? 1 : 0;
     return kda::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KDA_OK
                : KDA_ERR_CUDA;
@@ -355,6 +360,25 @@ static kda_status backward_impl(const void* q, const void* k, const void* v, con
     return kda::launch_gate_grad(gate, a, ax, dax, dalpha, pa.status, stream) == cudaSuccess
                ? KDA_OK
                : KDA_ERR_CUDA;
+}
+
+kda_status kda_prefill_additive(const void* q, const void* k, const void* v, const float* alpha,
+                                const float* beta, const float* S0, const int32_t* cu_seqlens,
+                                int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                                int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
+                                void* workspace, size_t workspace_bytes,
+                                kda_prefill_kernel kernel, kda_stream_t stream) {
+    return kda::prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
+                             d_k, d_v, dtype, chunk, o, S_T, workspace, workspace_bytes, kernel,
+                             stream, KDA_GATE_CHANNEL_F32, true);
+}
+
+kda_status kda_decode_step_additive(const void* q, const void* k, const void* v,
+                                    const float* alpha, const float* beta, float* S, int32_t B,
+                                    int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                                    void* o, kda_stream_t stream) {
+    return decode_impl(q, k, v, alpha, KDA_GATE_CHANNEL_F32, beta, S, B, H, d_k, d_v, dtype, o,
+                       stream, true);
 }
 
 size_t kda_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t H,

@@ -51,7 +51,8 @@ template <int DK, typename T, int GATE>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const void* __restrict__ alpha, const float* __restrict__ beta,
-                  float* __restrict__ S, int32_t H, int32_t d_v, T* __restrict__ o) {
+                  float* __restrict__ S, int32_t H, int32_t d_v, T* __restrict__ o,
+                  int32_t additive) {
     using Sh = DecodeShape<DK>;
     const int bh = blockIdx.x;                  // b * H + h
     const int lane = threadIdx.x & 31;
@@ -104,7 +105,8 @@ kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         if (r < d_v) {
             const size_t vi = (size_t)bh * d_v + r;
             const float al = gate_of<GATE>(alpha, bh, vi);
-            const float err = bt * (Elem<T>::load(v + vi) - al * pa);
+            // the additive update of linear attention has no prediction term
+            const float err = bt * (Elem<T>::load(v + vi) - (additive ? 0.f : al * pa));
             float4* dst = reinterpret_cast<float4*>(S + vi * DK);
 #pragma unroll
             for (int j = 0; j < Sh::VEC; ++j) {
@@ -126,7 +128,7 @@ cudaError_t launch_decode_g(const DecodeArgs& a, cudaStream_t stream) {
     dim3 grid(a.B * a.H, (a.d_v + Sh::ROWS_PER_CTA - 1) / Sh::ROWS_PER_CTA);
     kda_decode_kernel<DK, T, GATE><<<grid, kDecodeWarps * 32, 0, stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
-        a.alpha, a.beta, a.S, a.H, a.d_v, static_cast<T*>(a.o));
+        a.alpha, a.beta, a.S, a.H, a.d_v, static_cast<T*>(a.o), a.additive);
     return cudaGetLastError();
 }
 

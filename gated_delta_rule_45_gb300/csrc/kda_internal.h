@@ -60,6 +60,7 @@ struct PrefillArgs {
     int32_t* counter;   // device
     int32_t* order;     // device, [num_seqs]
     int32_t gate = 0;   // kda_gate_format
+    int32_t additive = 0;   // additive update of linear attention instead of the delta rule
 };
 
 struct DecodeArgs {
@@ -73,6 +74,7 @@ struct DecodeArgs {
     kda_dtype dtype;
     void* o;
     int32_t gate = 0;    // kda_gate_format
+    int32_t additive = 0;   // additive update of linear attention instead of the delta rule
 };
 
 // Backward pass (kda_backward.cu).  Buffers appended to the base workspace:
@@ -145,7 +147,8 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
                         int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                         int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
                         void* workspace, size_t workspace_bytes, kda_prefill_kernel kernel,
-                        kda_stream_t stream, kda_gate_format gate = KDA_GATE_CHANNEL_F32);
+                        kda_stream_t stream, kda_gate_format gate = KDA_GATE_CHANNEL_F32,
+                        bool additive = false);
 
 // ---- small device helpers ------------------------------------------------
 

@@ -16,6 +16,10 @@
 // Rows past the end of a sequence are padded with k = q = v = 0, alpha = 1,
 // beta = 0; they leave S unchanged and their o is not stored.
 //
+// The additive update of linear attention (no prediction: S_t = D_t S_{t-1} +
+// beta_t v_t k_t^T) is the same chunk form with the K S^T term dropped from X
+// and T = I.
+//
 // One CTA per (sequence, head, block of 64 value channels); CTAs are issued
 // in the planner's longest-first order.  This kernel covers every supported
 // shape (d_k <= 128, chunk 16/32/64, bf16 or fp32 storage) and is the path for
@@ -185,21 +189,23 @@ kda_prefill_simt_kernel(PrefillArgs a) {
 
         // T = (I + L)^{-1}, unit lower triangular; one thread per column,
         // forward substitution T[i][c] = delta_ic - sum_{j<i} L[i][j] T[j][c]
+        // (the additive update has no prediction: T = I)
         if (tid < C) {
             const int c = tid;
             for (int i = 0; i < C; ++i) {
                 float x = (i == c) ? 1.f : 0.f;
-                if (i > c) {
+                if (i > c && !a.additive) {
                     for (int j = c; j < i; ++j) x = fmaf(-s.Ls[i * s.CP + j], s.Ts[j * s.CP + c], x);
                 }
                 s.Ts[i * s.CP + c] = x;
             }
         }
-        // X = diag(beta) (V / Gamma - K S^T), written over V
+        // X = diag(beta) (V / Gamma - K S^T), written over V (no K S^T term in the
+        // additive update)
         {
             float acc[4][4];
             zero(acc);
-            mm_acc(acc, s.Ks, s.KP, 1, s.Ss, s.KP, 1, C, kDVB, d_k, 0, ty, tx);
+            if (!a.additive) mm_acc(acc, s.Ks, s.KP, 1, s.Ss, s.KP, 1, C, kDVB, d_k, 0, ty, tx);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll

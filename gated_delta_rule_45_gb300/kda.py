@@ -83,6 +83,10 @@ def load(path: str | None = None):
     lib.kda_backward.restype = ctypes.c_int
     lib.kda_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                  ctypes.c_int, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_prefill_additive.restype = ctypes.c_int
+    lib.kda_prefill_additive.argtypes = prefill_args + [ctypes.c_int, vp]
+    lib.kda_decode_step_additive.restype = ctypes.c_int
+    lib.kda_decode_step_additive.argtypes = lib.kda_decode_step.argtypes
     lib.kda_backward_gates_workspace_size.restype = sz
     lib.kda_backward_gates_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, ctypes.c_int]
     lib.kda_backward_gates.restype = ctypes.c_int
@@ -297,6 +301,43 @@ def decode_step_gates(q, k, v, alpha, beta, S, o=None, *, gate: str = "channel",
                                       _ptr(S), B, H, d_k, d_v, dt, _ptr(o), _stream_ptr(stream))
     if st != OK:
         raise KdaError(st, "kda_decode_step_gates")
+    return o
+
+
+def prefill_additive(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64,
+                     kernel: str = "auto", stream=None, check_device_status: bool = False):
+    """kda_prefill_additive: the additive update of linear attention (no predict
+    step; naive linear attention when alpha = beta = 1).  Returns (o, S_T)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens)
+    o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
+    S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=q.device)
+    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk), dtype=torch.uint8, device=q.device)
+    st = load().kda_prefill_additive(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                     _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v,
+                                     _dtype_code(q), chunk, _ptr(o), _ptr(S_T), _ptr(ws),
+                                     ws.numel(), _KERNELS[kernel], _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_prefill_additive")
+    if check_device_status:
+        device_status(ws, stream=stream)
+    return o, S_T
+
+
+def decode_step_additive(q, k, v, alpha, beta, S, o=None, *, stream=None):
+    """kda_decode_step_additive: one step of the additive update, S in place; returns o."""
+    B, H, d_k = q.shape
+    d_v = v.shape[2]
+    if o is None:
+        o = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
+    _check_cuda(q, k, v, alpha, beta, S, o)
+    st = load().kda_decode_step_additive(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                         _ptr(S), B, H, d_k, d_v, _dtype_code(q), _ptr(o),
+                                         _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_decode_step_additive")
     return o
 
 

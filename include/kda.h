@@ -320,6 +320,31 @@ kda_status kda_backward_gates(const void* q, const void* k, const void* v, const
                               float* dk, float* dv, float* dgate, float* dbeta, float* dS0,
                               void* workspace, size_t workspace_bytes, kda_stream_t stream);
 
+/*
+ * The additive update of linear attention instead of the delta rule: the
+ * predict step is dropped, so S_t = diag(alpha_t) S_{t-1} + beta_t v_t k_t^T
+ * and o_t = S_t q_t.  With alpha = beta = 1 this is the page's naive linear
+ * attention, S_t = S_{t-1} + v_t k_t^T, o_t = (sum_{i<=t} v_i k_i^T) q_t
+ * ("Kimi (AI)", section "Kimi Delta Attention (KDA)", the line before the
+ * three-line update).  Arguments, layouts and rules as kda_prefill_ex with the
+ * per-channel fp32 gate; the chunk form is the delta rule's with the K S^T
+ * term and the triangular solve dropped.  Runs on the portable kernel:
+ * KDA_KERNEL_CHUNK_TC and KDA_KERNEL_CHUNK_TC_SPLIT return KDA_ERR_UNSUPPORTED.
+ */
+kda_status kda_prefill_additive(const void* q, const void* k, const void* v, const float* alpha,
+                                const float* beta, const float* S0, const int32_t* cu_seqlens,
+                                int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                                int32_t d_v, kda_dtype dtype, int32_t chunk, void* o, float* S_T,
+                                void* workspace, size_t workspace_bytes,
+                                kda_prefill_kernel kernel, kda_stream_t stream);
+
+/* One decode step of the additive update (kda_prefill_additive's recurrence):
+ * arguments and shapes as kda_decode_step. */
+kda_status kda_decode_step_additive(const void* q, const void* k, const void* v,
+                                    const float* alpha, const float* beta, float* S, int32_t B,
+                                    int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                                    void* o, kda_stream_t stream);
+
 /* Static description of a status code.  Never NULL. */
 const char* kda_status_string(kda_status s);
 

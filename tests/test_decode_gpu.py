@@ -97,3 +97,18 @@ def test_decode_gate_layouts(gate, d_k, d_v):
                       for b in range(spec.B) for h in range(spec.H)), parity.rel(o_g, o_ref))
     worst_s = max(parity.rel(S_g[b, h], S_ref[b, h]) for b in range(spec.B) for h in range(spec.H))
     assert worst_o <= parity.TOL_BF16 and worst_s <= parity.TOL_BF16, (worst_o, worst_s)
+
+
+def test_decode_additive_update():
+    """kda_decode_step_additive against the oracle's additive recurrence."""
+    spec = synth.DecodeSpec(B=8, H=4, d_k=128, d_v=96, seed=5)
+    d = synth.decode_inputs(spec)
+    S = d["S"].cuda()
+    o = kda.decode_step_additive(*(d[k].cuda() for k in ("q", "k", "v", "alpha", "beta")), S)
+    torch.cuda.synchronize()
+    bits = synth.bf16_bits
+    o_ref, S_ref = oracle.decode_step(bits(d["q"]), bits(d["k"]), bits(d["v"]),
+                                      d["alpha"].numpy(), d["beta"].numpy(),
+                                      d["S"].double().numpy(), additive=True)
+    assert parity.rel(o.float().cpu().numpy(), parity.round_to(o_ref[:, :, :], torch.bfloat16)) <= 2e-3
+    assert parity.rel(S.cpu().numpy(), S_ref) <= 2e-5

@@ -266,3 +266,37 @@ def test_gate_layouts_on_the_portable_kernel(gate):
     ref = parity.oracle_pairs(d, [(n, h) for n in range(spec.num_seqs) for h in range(spec.H)])
     wo, ws = parity.compare_pairs(d, o, S_T, ref)
     assert wo <= 1e-4 and ws <= 1e-4, (gate, wo, ws)
+
+
+@pytest.mark.parametrize("spec", [
+    synth.PrefillSpec(num_seqs=4, len_lo=1, len_hi=300, H=2, d_k=128, d_v=128, s0_std=0.1,
+                      seed=31),
+    synth.PrefillSpec(num_seqs=2, len_lo=50, len_hi=200, H=3, d_k=64, d_v=48, dtype="fp32",
+                      chunk=32, s0_std=0.1, seed=32),
+])
+def test_additive_update_matches_oracle(spec):
+    """kda_prefill_additive (the update of linear attention without the
+    prediction term) against the oracle's additive recurrence."""
+    d = synth.prefill_inputs(spec)
+    dev = parity.to_device(d)
+    o, S_T = kda.prefill_additive(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"],
+                                  dev["S0"], dev["cu_seqlens"], chunk=spec.chunk,
+                                  check_device_status=True)
+    torch.cuda.synchronize()
+    f = (lambda x: synth.bf16_bits(x)) if spec.dtype == "bf16" else (lambda x: x.numpy())
+    o_ref, S_ref = oracle.prefill(f(d["q"]), f(d["k"]), f(d["v"]), d["alpha"].numpy(),
+                                  d["beta"].numpy(),
+                                  None if d["S0"] is None else d["S0"].double().numpy(),
+                                  d["cu_seqlens"].numpy(), additive=True)
+    cu = d["cu_seqlens"].numpy()
+    tol = parity.TOL_BF16 if spec.dtype == "bf16" else parity.TOL_FP32
+    for n in range(spec.num_seqs):
+        a, b = int(cu[n]), int(cu[n + 1])
+        for h in range(spec.H):
+            if b > a:
+                assert parity.rel_gate(o[a:b, h].float().cpu().numpy(), o_ref[a:b, h],
+                                       o.dtype) <= tol
+            assert parity.rel(S_T[n, h].cpu().numpy(), S_ref[n, h]) <= tol
+    with pytest.raises(kda.KdaError):   # the tensor-core kernel has no additive mode
+        kda.prefill_additive(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"],
+                             dev["S0"], dev["cu_seqlens"], chunk=spec.chunk, kernel="tc")
