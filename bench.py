@@ -647,8 +647,9 @@ def run_component(args):
                 f"chunk={spec.chunk}; dO bf16, dS_T fp32; all six gradients fp32")
     else:
         gate = {"prefill_head_gate": "head", "prefill_log_gate": "log_bf16"}.get(args.workload)
+        additive = args.workload == "prefill_additive"
         name = "varlen" if args.workload == "varlen_prefill" else \
-            "prefill" if gate else args.workload
+            "prefill" if (gate or additive) else args.workload
         spec = synth.WORKLOADS[name]
         d = synth.prefill_inputs(spec)
         g = {key: (d[key].to(dev) if d[key] is not None else None)
@@ -660,7 +661,12 @@ def run_component(args):
                           dtype=torch.uint8, device=dev)
 
         alpha_bytes = None
-        if gate is None:
+        if additive:   # the additive update of linear attention on the same inputs
+            def launch():
+                kda.prefill_additive_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                                          g["cu_seqlens"], o, S, wsp, chunk=spec.chunk,
+                                          stream=stream)
+        elif gate is None:
             def launch():
                 kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
                                  g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
@@ -682,7 +688,8 @@ def run_component(args):
         units, unit = T, "tokens/s"
         desc = (f"{args.workload}: N={spec.num_seqs}, T={T}, H={spec.H}, d_k={spec.d_k}, "
                 f"d_v={spec.d_v}, chunk={spec.chunk}"
-                + (f", gate layout {gate}" if gate else ""))
+                + (f", gate layout {gate}" if gate else "")
+                + (", additive update (no prediction)" if additive else ""))
         lens = [int(x) for x in d["lengths"]]
         mma_flops = (MMA_FLOPS_PER_BLOCK_CHUNK * spec.H * (spec.d_v // 128)
                      * sum((n + spec.chunk - 1) // spec.chunk for n in lens))
@@ -750,7 +757,8 @@ def main(argv=None):
     p.add_argument("--workload",
                    choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
                             "l2_resident", "prefill_head_gate", "prefill_log_gate",
-                            "backward", "backward_small", "attnres", "attnres_small"],
+                            "backward", "backward_small", "attnres", "attnres_small",
+                            "prefill_additive"],
                    default="varlen",
                    help="varlen (default): the full step; others time one kernel alone "
                         "(varlen_prefill: the varlen batch's prefill without the decode steps; "
@@ -760,7 +768,8 @@ def main(argv=None):
                         "backward: kda_backward on the prefill workload; backward_small: "
                         "the same with 512 tokens per sequence, for profiling; attnres: "
                         "Blocked Attention Residuals over a 64-layer network; attnres_small: "
-                        "the same with 4096 tokens, for profiling)")
+                        "the same with 4096 tokens, for profiling; prefill_additive: the "
+                        "prefill workload under the additive update of linear attention)")
     args = p.parse_args(argv)
     # at least 3 untimed warm-up steps; the JSON line reports the number used
     args.warmup = max(3, args.warmup)

@@ -63,9 +63,8 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     if (total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
     if (gate != KDA_GATE_CHANNEL_F32 && kernel == KDA_KERNEL_CHUNK_TC_SPLIT)
         return KDA_ERR_UNSUPPORTED;
-    // the additive update runs on the portable kernel only
-    if (additive && (kernel == KDA_KERNEL_CHUNK_TC || kernel == KDA_KERNEL_CHUNK_TC_SPLIT))
-        return KDA_ERR_UNSUPPORTED;
+    // the additive update has no sequence-axis split
+    if (additive && kernel == KDA_KERNEL_CHUNK_TC_SPLIT) return KDA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * H > (int64_t)INT32_MAX / 64) return KDA_ERR_UNSUPPORTED;
     if (!cu_seqlens || !workspace || (num_seqs > 0 && !S_T)) return KDA_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !alpha || !beta || !o)) return KDA_ERR_INVALID_ARG;
@@ -101,13 +100,14 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     a.counter = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kCounter);
     a.order = reinterpret_cast<int32_t*>(ws + kda::WorkspaceLayout::kOrder);
 
-    const bool tc_ok = kda::prefill_tc_supports(a) && !additive;
+    const bool tc_ok = kda::prefill_tc_supports(a);
     const bool want_tc = kernel == KDA_KERNEL_CHUNK_TC || kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
     if (want_tc && !tc_ok) return KDA_ERR_UNSUPPORTED;
     const bool use_tc = want_tc || (kernel == KDA_KERNEL_AUTO && tc_ok);
     // sequence-axis split: few chains, long sequences, room in the workspace
     kda::SplitLayout split;
-    if (use_tc && kernel != KDA_KERNEL_CHUNK_TC && num_seqs > 0 && gate == KDA_GATE_CHANNEL_F32) {
+    if (use_tc && kernel != KDA_KERNEL_CHUNK_TC && num_seqs > 0 && gate == KDA_GATE_CHANNEL_F32 &&
+        !additive) {
         const int M = kda::split_segments(num_seqs, H, d_k, d_v, chunk);
         const bool forced = kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
         if (forced && M < 3) return KDA_ERR_UNSUPPORTED;

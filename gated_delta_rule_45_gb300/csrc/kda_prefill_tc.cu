@@ -147,8 +147,11 @@ struct ItemInfo {
 // scalar gate, broadcast over the value channels); per value channel log alpha
 // in bf16 [T][H][d_v] (half the bytes of the largest prefill input).
 // GATE_F32_CKPT: the fp32 gate, and every chunk's start state is written to
-// TcParams::ckpt for the backward pass.
-enum { GATE_F32 = 0, GATE_SCALAR = 1, GATE_LOG_BF16 = 2, GATE_F32_CKPT = 3 };
+// TcParams::ckpt for the backward pass.  GATE_F32_ADD: the fp32 gate with the
+// additive update of linear attention (no prediction): beta is taken as zero
+// in L, so T = I, and X = beta V / Gamma without the S K^T term; the MMA
+// schedule is unchanged.
+enum { GATE_F32 = 0, GATE_SCALAR = 1, GATE_LOG_BF16 = 2, GATE_F32_CKPT = 3, GATE_F32_ADD = 4 };
 
 // SPLIT: the kernel serves the split launches (virtual sequences, transition
 // items); the plain instantiation compiles none of that.
@@ -549,7 +552,7 @@ __device__ __forceinline__ void warp_store16(float* Y, int ldy, const float (&ac
 // the KQK accumulator, then T = (I + L)^{-1} by blocks of 16: the four
 // diagonal blocks D_b by forward substitution, the rest by recursive doubling
 // of the block-triangular inverse, and finally T and P as bf16 hi/lo tiles.
-template <bool SPLIT>
+template <bool SPLIT, int GATE>
 __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int warp, int lane) {
     Group grp{t, 1, 128, 0, cx.slots};
     const int quarter = warp & 3;
@@ -570,7 +573,7 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
         uint8_t* t_hi = cx.smem + SM_T + s * TP_BUF;
         uint8_t* p_hi = cx.smem + SM_P + s * TP_BUF;
         const bool krow = kr < 64;           // warp-uniform
-        const float bt = krow ? bst[kr] : 0.f;
+        const float bt = krow && GATE != GATE_F32_ADD ? bst[kr] : 0.f;
         const int tq = kr - 64;
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -889,7 +892,8 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                     uint32_t hi[8], lo[8];
 #pragma unroll
                     for (int j2 = 0; j2 < 4; ++j2) {
-                        const float4 bq = b4[4 * q2 + j2];
+                        const float4 bq = GATE == GATE_F32_ADD ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                               : b4[4 * q2 + j2];
                         const int jj = 16 * q2 + 4 * j2;
                         const float2 x01 = __ffma2_rn(
                             make_float2(-bq.x, -bq.y),
@@ -1073,7 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     } else if (warp == 1) {
         run_mma<SPLIT>(p, cx);
     } else if (warp >= 2 && warp < 6) {
-        run_token_group<SPLIT>(p, cx, tid - 64, warp, lane);
+        run_token_group<SPLIT, GATE>(p, cx, tid - 64, warp, lane);
     } else {
         run_row_group<SPLIT, GATE>(p, cx, tid - 192, warp, lane);
     }
@@ -1189,6 +1193,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
     const int sms = sm_count();
     const int grid = p.num_items < sms ? p.num_items : sms;
     p.a_ctas = grid;
+    if (a.additive) {
+        if (a.gate != GATE_F32) return cudaErrorInvalidValue;
+        return launch_g<false, GATE_F32_ADD>(p, grid, stream);
+    }
     switch (a.gate) {
         case GATE_F32: return launch_g<false, GATE_F32>(p, grid, stream);
         case GATE_SCALAR: return launch_g<false, GATE_SCALAR>(p, grid, stream);

@@ -304,6 +304,21 @@ def decode_step_gates(q, k, v, alpha, beta, S, o=None, *, gate: str = "channel",
     return o
 
 
+def prefill_additive_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace, *,
+                          chunk: int = 64, kernel: str = "auto", stream=None) -> None:
+    """Enqueue kda_prefill_additive into preallocated outputs (as prefill_into)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    N = cu_seqlens.numel() - 1
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace)
+    st = load().kda_prefill_additive(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                     _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v,
+                                     _dtype_code(q), chunk, _ptr(o), _ptr(S_T), _ptr(workspace),
+                                     workspace.numel(), _KERNELS[kernel], _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_prefill_additive")
+
+
 def prefill_additive(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64,
                      kernel: str = "auto", stream=None, check_device_status: bool = False):
     """kda_prefill_additive: the additive update of linear attention (no predict
@@ -311,16 +326,11 @@ def prefill_additive(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64,
     T, H, d_k = q.shape
     d_v = v.shape[2]
     N = cu_seqlens.numel() - 1
-    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens)
     o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
     S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=q.device)
     ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk), dtype=torch.uint8, device=q.device)
-    st = load().kda_prefill_additive(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
-                                     _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v,
-                                     _dtype_code(q), chunk, _ptr(o), _ptr(S_T), _ptr(ws),
-                                     ws.numel(), _KERNELS[kernel], _stream_ptr(stream))
-    if st != OK:
-        raise KdaError(st, "kda_prefill_additive")
+    prefill_additive_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, ws, chunk=chunk,
+                          kernel=kernel, stream=stream)
     if check_device_status:
         device_status(ws, stream=stream)
     return o, S_T

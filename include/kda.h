@@ -328,8 +328,8 @@ kda_status kda_backward_gates(const void* q, const void* k, const void* v, const
  * ("Kimi (AI)", section "Kimi Delta Attention (KDA)", the line before the
  * three-line update).  Arguments, layouts and rules as kda_prefill_ex with the
  * per-channel fp32 gate; the chunk form is the delta rule's with the K S^T
- * term and the triangular solve dropped.  Runs on the portable kernel:
- * KDA_KERNEL_CHUNK_TC and KDA_KERNEL_CHUNK_TC_SPLIT return KDA_ERR_UNSUPPORTED.
+ * term dropped and T = I.  Both chunk kernels take it (the tensor-core one for
+ * the shapes it covers); KDA_KERNEL_CHUNK_TC_SPLIT returns KDA_ERR_UNSUPPORTED.
  */
 kda_status kda_prefill_additive(const void* q, const void* k, const void* v, const float* alpha,
                                 const float* beta, const float* S0, const int32_t* cu_seqlens,

@@ -279,10 +279,6 @@ def test_additive_update_matches_oracle(spec):
     prediction term) against the oracle's additive recurrence."""
     d = synth.prefill_inputs(spec)
     dev = parity.to_device(d)
-    o, S_T = kda.prefill_additive(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"],
-                                  dev["S0"], dev["cu_seqlens"], chunk=spec.chunk,
-                                  check_device_status=True)
-    torch.cuda.synchronize()
     f = (lambda x: synth.bf16_bits(x)) if spec.dtype == "bf16" else (lambda x: x.numpy())
     o_ref, S_ref = oracle.prefill(f(d["q"]), f(d["k"]), f(d["v"]), d["alpha"].numpy(),
                                   d["beta"].numpy(),
@@ -290,13 +286,21 @@ def test_additive_update_matches_oracle(spec):
                                   d["cu_seqlens"].numpy(), additive=True)
     cu = d["cu_seqlens"].numpy()
     tol = parity.TOL_BF16 if spec.dtype == "bf16" else parity.TOL_FP32
-    for n in range(spec.num_seqs):
-        a, b = int(cu[n]), int(cu[n + 1])
-        for h in range(spec.H):
-            if b > a:
-                assert parity.rel_gate(o[a:b, h].float().cpu().numpy(), o_ref[a:b, h],
-                                       o.dtype) <= tol
-            assert parity.rel(S_T[n, h].cpu().numpy(), S_ref[n, h]) <= tol
-    with pytest.raises(kda.KdaError):   # the tensor-core kernel has no additive mode
+    dt = torch.bfloat16 if spec.dtype == "bf16" else torch.float32
+    kernels = ["simt"] + (["tc"] if kda.supported("tc", spec.H, spec.d_k, spec.d_v, dt,
+                                                  spec.chunk) else [])
+    for kernel in kernels:
+        o, S_T = kda.prefill_additive(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"],
+                                      dev["S0"], dev["cu_seqlens"], chunk=spec.chunk,
+                                      kernel=kernel, check_device_status=True)
+        torch.cuda.synchronize()
+        for n in range(spec.num_seqs):
+            a, b = int(cu[n]), int(cu[n + 1])
+            for h in range(spec.H):
+                if b > a:
+                    assert parity.rel_gate(o[a:b, h].float().cpu().numpy(), o_ref[a:b, h],
+                                           o.dtype) <= tol, kernel
+                assert parity.rel(S_T[n, h].cpu().numpy(), S_ref[n, h]) <= tol, kernel
+    with pytest.raises(kda.KdaError):   # no sequence-axis split for the additive update
         kda.prefill_additive(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"],
-                             dev["S0"], dev["cu_seqlens"], chunk=spec.chunk, kernel="tc")
+                             dev["S0"], dev["cu_seqlens"], chunk=spec.chunk, kernel="tc_split")
