@@ -129,7 +129,7 @@ __device__ __forceinline__ void mma_tile(float (&c)[NT][4], const Op& A, const O
                                          int n0) {
     const int l = threadIdx.x & 31;
     const int r8 = l & 7, j1 = (l >> 3) & 1, j2 = l >> 4;
-#pragma unroll 1
+#pragma unroll 2
     for (int ks = 0; ks < KS; ++ks) {
         const int k = 16 * ks;
         uint32_t ah[4], al[4], bh[NT / 2][4], bl[NT / 2][4];
