@@ -23,9 +23,11 @@
 //             D <- dS^ + dP^T Q - dY^T K
 //
 // Value channels (rows of S) only interact through sums that end in dq, dk
-// and dbeta, so one CTA owns one (sequence, head, 64-row block) chain: a
-// forward sweep over its chunks writes the chunk-start states to the
-// workspace, a backward sweep walks the chunks in reverse.  dq, dk and dbeta
+// and dbeta, so one CTA owns one (sequence, head, 64-row block) chain and
+// walks its chunks in reverse.  The chunk-start states it needs come from the
+// tensor-core prefill (launched first, writing them to the workspace) when
+// d_v is a multiple of 128; for other widths the CTA first runs a forward
+// sweep of its own, keeping the states and each chunk's T.  dq, dk and dbeta
 // are written per row block and summed by a second kernel in a fixed order,
 // so results are deterministic.
 //
