@@ -251,6 +251,83 @@ def time_oracle_sample(d, steps, pairs_wanted: int, budget_s: float, seed: int =
     return th / dt / spec.H, cores, desc, dt
 
 
+def time_oracle_backward_sample(d, dO, dS_T, budget_s: float, seed: int = 0):
+    """Time the oracle's reverse mode on sampled (sequence, head) pairs of a
+    prefill workload, one pair per host thread, each over its whole sequence.
+    Returns (tokens/s, cores, description); tokens/s = token-heads/s / H."""
+    import oracle
+    spec = d["spec"]
+    cu = d["cu_seqlens"].numpy()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    rng = np.random.default_rng(seed)
+    # about 40 d_k d_v fp64 flops per token-head (forward re-run + reverse), ~1.5 Gflop/s a core
+    per_pair_s = 40.0 * spec.d_k * spec.d_v * float(np.mean(np.diff(cu))) / 1.5e9
+    n_pairs = int(max(1, min(cores * max(1, round(budget_s / max(per_pair_s, 1e-3))),
+                             spec.num_seqs * spec.H)))
+    chosen = [divmod(int(i), spec.H) for i in rng.permutation(spec.num_seqs * spec.H)[:n_pairs]]
+    parts = {key: [] for key in ("q", "k", "v", "alpha", "beta")}
+    dos, lens = [], []
+    for n, h in chosen:
+        a, b = int(cu[n]), int(cu[n + 1])
+        for key in parts:
+            parts[key].append(d[key][a:b, h:h + 1])
+        dos.append(dO[a:b, h:h + 1])
+        lens.append(b - a)
+    cat = lambda key: torch.cat(parts[key])
+    pcu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    st = (len(chosen), 1, spec.d_v, spec.d_k)
+    S0 = np.zeros(st) if d["S0"] is None else np.stack(
+        [d["S0"][n, h].double().numpy() for n, h in chosen])[:, None]
+    dst = np.stack([dS_T[n, h].double().numpy() for n, h in chosen])[:, None]
+    t0 = time.perf_counter()
+    oracle.backward(synth.bf16_bits(cat("q")), synth.bf16_bits(cat("k")), synth.bf16_bits(cat("v")),
+                    cat("alpha").numpy(), cat("beta").numpy(), S0, pcu,
+                    torch.cat(dos).double().numpy(), dst, nthreads=cores)
+    dt = time.perf_counter() - t0
+    th = int(pcu[-1])
+    desc = (f"{len(chosen)} (sequence, head) pairs of the workload, reverse mode over each "
+            f"whole sequence: {th} token-heads, fp64, {dt:.1f} s on {cores} threads; "
+            f"tokens/s = token-heads/s / H")
+    return th / dt / spec.H, cores, desc
+
+
+def time_oracle_attnres_sample(x, calls, budget_s: float):
+    """Time the Attention Residuals oracle (numpy fp64) on the first tokens of
+    the network, every layer in turn with the stored block sums and the running
+    sum carried as a model does.  Returns (tokens/s, cores, description)."""
+    from oracle import attnres as ar
+    spec = x["spec"]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    scale = 1.0 / np.sqrt(spec.d)
+    n_tok = 64
+    max_tok = 1024   # keeps the fp64 copy of the layer outputs near 1 GB
+    while True:
+        h0 = x["h0"][:n_tok].cpu().double().numpy()
+        outs = x["outs"][:, :n_tok].cpu().double().numpy()
+        qs = x["queries"].cpu().double().numpy()
+        t0 = time.perf_counter()
+        blocks, partial, layer = [h0], None, 0
+        h_last = None
+        for n, size in enumerate(spec.block_sizes, start=1):
+            for i in range(size):
+                if i == 0 and n > 1:
+                    _, P = ar.layer_step(np.stack(blocks), partial, h_last, qs[layer], scale)
+                    blocks.append(P)
+                    partial = None
+                else:
+                    _, partial = ar.layer_step(np.stack(blocks), partial, h_last, qs[layer],
+                                               scale)
+                h_last = outs[layer]
+                layer += 1
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * budget_s or n_tok >= min(spec.T, max_tok):
+            break
+        n_tok = min(spec.T, max_tok, n_tok * max(2, int(budget_s / max(dt, 1e-3))))
+    desc = (f"the first {n_tok} tokens through all {layer} layers, numpy fp64 "
+            f"({dt:.1f} s; numpy's threads, up to {cores} cores)")
+    return n_tok / dt, cores, desc
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if ws > 1:
@@ -735,14 +812,24 @@ def run_component(args):
                     "mma_flops_per_launch": mma_flops, "peak_source": tsrc,
                     "hbm_equivalent_gbs": achieved}
         l2 = "L2-resident on purpose (~110 MB of inputs and states, relaunched back to back)"
-    print(json.dumps({
+    line = {
         "metric": METRIC, "value": units / (ms / 1e3), "unit": unit, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 in/out; fp32 state", "data": "synthetic (seeded)",
         "config": {"workload": desc, "l2": l2},
         "roofline": roofline,
-        "clocks": clock_info, "component_only": True}), flush=True)
+        "clocks": clock_info, "component_only": True}
+    if not args.no_cpu_baseline and args.workload in ("backward", "attnres"):
+        # the oracle beside the GPU figure, on a bounded sample of the same workload
+        if args.workload == "backward":
+            v, cores, cdesc = time_oracle_backward_sample(d, dO.cpu(), dS_T.cpu(),
+                                                          args.ref_budget)
+        else:
+            v, cores, cdesc = time_oracle_attnres_sample(x, calls, args.ref_budget)
+        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+                                "sample": cdesc}
+    print(json.dumps(line), flush=True)
 
 
 def main(argv=None):
