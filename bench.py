@@ -40,7 +40,7 @@ UNIT = "tokens/s"
 # kernel (the prefill kernel on this workload's full-size batch, 1-pass ncu
 # capture; see profiles/kda_prefill_tc_prefill_workload.md).  Must be set back
 # to None whenever that kernel changes until it is captured again.
-NCU_TRAFFIC_BYTES_PER_LAUNCH = 10.32e9
+NCU_TRAFFIC_BYTES_PER_LAUNCH = 10.31e9
 
 
 # ---------------------------------------------------------------- distributed
