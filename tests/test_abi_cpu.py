@@ -268,3 +268,57 @@ def test_attnres_rejects_on_host(lib, kw, expect):
 def test_attnres_empty_is_a_no_op(lib):
     # T == 0 returns before any CUDA call
     assert _attnres(lib, T=0) == 0
+
+
+def test_prefill_additive_rejects_on_host(lib):
+    def call(**kw):
+        args = dict(q=_fake(0x10000), k=_fake(0x20000), v=_fake(0x30000), alpha=_fake(0x40000),
+                    beta=_fake(0x50000), S0=None, cu=_fake(0x60000), N=2, T=64, H=2, d_k=128,
+                    d_v=128, dtype=0, chunk=64, o=_fake(0x70000), S_T=_fake(0x80000),
+                    ws=_fake(0x90000), ws_bytes=4096, kernel=0)
+        args.update(kw)
+        return lib.kda_prefill_additive(args["q"], args["k"], args["v"], args["alpha"],
+                                        args["beta"], args["S0"], args["cu"], args["N"],
+                                        args["T"], args["H"], args["d_k"], args["d_v"],
+                                        args["dtype"], args["chunk"], args["o"], args["S_T"],
+                                        args["ws"], args["ws_bytes"], args["kernel"], None)
+    assert call(kernel=3) == 2          # no sequence-axis split for the additive update
+    assert call(kernel=9) == 1
+    assert call(chunk=48) == 2
+    assert call(o=None) == 1
+    assert call(o=_fake(0x70008)) == 1  # misaligned
+
+
+def test_decode_additive_rejects_on_host(lib):
+    def call(**kw):
+        args = dict(d_k=128, o=_fake(0x900000), S=_fake(0x100000))
+        args.update(kw)
+        return lib.kda_decode_step_additive(_fake(0x10000), _fake(0x20000), _fake(0x30000),
+                                            _fake(0x40000), _fake(0x50000), args["S"], 2, 2,
+                                            args["d_k"], 128, 0, args["o"], None)
+    assert call(d_k=96) == 2
+    assert call(o=None) == 1
+    assert call(o=_fake(0x40000)) == 1  # o overlaps alpha
+
+
+def test_backward_gates_host_checks(lib):
+    f = lib.kda_backward_gates_workspace_size
+    base = lib.kda_backward_workspace_size(2, 64, 2, 128, 128, 64)
+    assert f(2, 64, 2, 128, 128, 64, 0) == base
+    # the other layouts add the gate per channel and its gradient, fp32 each
+    for gate in (1, 2):
+        assert f(2, 64, 2, 128, 128, 64, gate) >= base + 2 * 64 * 2 * 128 * 4
+    assert f(2, 64, 2, 128, 128, 64, 7) == 0
+    M = 0x1000000
+
+    def call(gate, ws_bytes=None, dgate=_fake(11 * M)):
+        if ws_bytes is None:
+            ws_bytes = f(2, 64, 2, 128, 128, 64, gate if gate in (0, 1, 2) else 0)
+        return lib.kda_backward_gates(_fake(1 * M), _fake(2 * M), _fake(3 * M), _fake(4 * M),
+                                      gate, _fake(5 * M), None, _fake(6 * M), 2, 64, 2, 128,
+                                      128, 0, 64, _fake(7 * M), None, _fake(8 * M),
+                                      _fake(9 * M), _fake(10 * M), dgate, _fake(12 * M), None,
+                                      _fake(13 * M), ws_bytes, None)
+    assert call(7) == 1                                  # unknown layout
+    assert call(1, ws_bytes=base) == 1                   # too small for the expanded gate
+    assert call(2, dgate=_fake(4 * M + 1024)) == 1       # d/d log alpha overlaps the gate
