@@ -1240,12 +1240,18 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, 
     p1.n_base_p = N;
     p1.num_items_p = (M - 2) * N * a.H;
     p1.P_out = reinterpret_cast<float*>(ws + L.pbuf);
-    // one CTA per plain chain when they fit, the rest to transitions
-    int a_ctas = p1.num_items < sms ? p1.num_items : sms;
-    int p_ctas = sms - a_ctas;
-    if (p_ctas > p1.num_items_p) p_ctas = p1.num_items_p;
-    if (p_ctas < 1) {   // more chains than SMs: split the grid evenly
-        a_ctas = sms / 2;
+    // one CTA per item when they all fit; otherwise the SMs are divided in
+    // proportion to the two kinds of items, so that both take the same number
+    // of waves
+    int a_ctas, p_ctas;
+    const int64_t all = (int64_t)p1.num_items + p1.num_items_p;
+    if (all <= sms) {
+        a_ctas = p1.num_items;
+        p_ctas = p1.num_items_p;
+    } else {
+        a_ctas = (int)(((int64_t)sms * p1.num_items + all / 2) / all);
+        if (a_ctas < 1) a_ctas = 1;
+        if (a_ctas > sms - 1) a_ctas = sms - 1;
         p_ctas = sms - a_ctas;
     }
     p1.a_ctas = a_ctas;

@@ -20,11 +20,22 @@ int split_segments(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int32_
     if (num_seqs <= 0 || H <= 0 || d_k != 128 || d_v % 128 != 0 || chunk != 64) return 1;
     const int64_t chains = (int64_t)num_seqs * H * (d_v / 128);
     const int64_t sms = sm_count();
-    // the first pass holds (M-1) chains per (sequence, head, block) and (M-2)
-    // transition chains per (sequence, head); all of them must fit one wave
+    if (sms <= 0 || 2 * chains + (int64_t)num_seqs * H > sms) return 1;
+    // a pass takes (waves of its items) x (chunks per segment) chunk times: the
+    // first pass has (M-1) items per chain plus (M-2) transition items per
+    // (sequence, head), the second (M-1) per chain; pick the M in [3, 8] with
+    // the fewest waves per segment of the sequence (ties: the smaller M)
     int M = 1;
-    for (int m = 3; m <= 8; ++m)
-        if ((m - 1) * chains + (int64_t)(m - 2) * num_seqs * H <= sms) M = m;
+    double best = 0.0;
+    for (int m = 3; m <= 8; ++m) {
+        const int64_t p1 = (m - 1) * chains + (int64_t)(m - 2) * num_seqs * H;
+        const int64_t p2 = (m - 1) * chains;
+        const double cost = (double)((p1 + sms - 1) / sms + (p2 + sms - 1) / sms) / m;
+        if (M == 1 || cost < best - 1e-9) {
+            M = m;
+            best = cost;
+        }
+    }
     return M;
 }
 
