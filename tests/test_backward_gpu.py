@@ -103,6 +103,10 @@ CASES = [
     # fast decay: products of alpha over a chunk down to ~1e-12
     synth.PrefillSpec(num_seqs=2, len_lo=150, len_hi=200, H=2, d_k=128, d_v=128, alpha_mu=1.0,
                       s0_std=0.1, seed=15),
+    # d_v = 192: three row blocks, and the kernel's own forward sweep (no
+    # tensor-core checkpoints for a width that is not a multiple of 128)
+    synth.PrefillSpec(num_seqs=3, len_lo=30, len_hi=220, H=2, d_k=128, d_v=192, s0_std=0.1,
+                      seed=22),
 ]
 
 
