@@ -1,5 +1,4 @@
 """kda_decode_step against the oracle (GPU)."""
-import numpy as np
 import pytest
 import torch
 

@@ -1,7 +1,6 @@
 """The Attention Residuals oracle against its pins, and planted mistakes
 against the pins (CPU only)."""
 import importlib.util
-import os
 
 import numpy as np
 import pytest
