@@ -24,8 +24,11 @@ from __future__ import annotations
 import numpy as np
 
 
-def run_sequence(q, k, v, alpha, beta, S0, C):
-    """One (sequence, head): q, k [L, d_k]; v, alpha [L, d_v]; beta [L]; S0 [d_v, d_k]."""
+def run_sequence(q, k, v, alpha, beta, S0, C, additive=False):
+    """One (sequence, head): q, k [L, d_k]; v, alpha [L, d_v]; beta [L]; S0 [d_v, d_k].
+
+    additive=True: the additive update of linear attention (no prediction), whose
+    chunk form is this one with T = I and no K S^T term in X."""
     q, k, v, alpha, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, alpha, beta))
     L, d_k = k.shape
     d_v = v.shape[1]
@@ -39,9 +42,13 @@ def run_sequence(q, k, v, alpha, beta, S0, C):
         Ac = np.ones((C, d_v)); Ac[:n] = alpha[c0:c0 + n]
         bc = np.zeros(C); bc[:n] = beta[c0:c0 + n]
         G = np.cumprod(Ac, axis=0)
-        A = np.eye(C) + bc[:, None] * np.tril(Kc @ Kc.T, -1)
-        T = np.linalg.inv(A)
-        X = bc[:, None] * (Vc / G - Kc @ S.T)
+        if additive:
+            T = np.eye(C)
+            X = bc[:, None] * (Vc / G)
+        else:
+            A = np.eye(C) + bc[:, None] * np.tril(Kc @ Kc.T, -1)
+            T = np.linalg.inv(A)
+            X = bc[:, None] * (Vc / G - Kc @ S.T)
         U = T @ X
         O = G * (Qc @ S.T + np.tril(Qc @ Kc.T) @ U)
         S = G[-1][:, None] * (S + U.T @ Kc)
@@ -49,7 +56,7 @@ def run_sequence(q, k, v, alpha, beta, S0, C):
     return o, S
 
 
-def run_packed(q, k, v, alpha, beta, S0, cu_seqlens, C):
+def run_packed(q, k, v, alpha, beta, S0, cu_seqlens, C, additive=False):
     """Packed batch: q, k [T, H, d_k]; v, alpha [T, H, d_v]; beta [T, H]; S0 [N, H, d_v, d_k] or None."""
     T, H, d_k = q.shape
     d_v = v.shape[2]
@@ -61,7 +68,7 @@ def run_packed(q, k, v, alpha, beta, S0, cu_seqlens, C):
         for h in range(H):
             s0 = None if S0 is None else S0[n, h]
             o[a:b, h], S_T[n, h] = run_sequence(q[a:b, h], k[a:b, h], v[a:b, h],
-                                                alpha[a:b, h], beta[a:b, h], s0, C)
+                                                alpha[a:b, h], beta[a:b, h], s0, C, additive)
     return o, S_T
 
 

@@ -95,3 +95,17 @@ def test_chunk_backward_matches_reverse_mode(oracle_lib, C):
     got = chunk_form.backward_packed(_widen(q), _widen(k), _widen(v), a, b, S0, cu, dO, dS_T, C)
     for name in ref:
         assert _rel(got[name], ref[name]) < 1e-10, name
+
+
+@pytest.mark.parametrize("C", [16, 64])
+def test_chunk_form_of_the_additive_update(oracle_lib, C):
+    """The additive update's chunk form (T = I, no K S^T term in X), which both
+    chunk kernels implement, against the oracle's additive recurrence."""
+    spec = synth.PrefillSpec(num_seqs=4, len_lo=1, len_hi=150, H=2, d_k=32, d_v=48,
+                             alpha_mu=2.0, s0_std=0.3, seed=8)
+    q, k, v, a, b, S0, cu = _np_inputs(synth.prefill_inputs(spec))
+    o_ref, S_ref = oracle.prefill(q, k, v, a, b, S0, cu, lib=oracle_lib, additive=True)
+    o, S = chunk_form.run_packed(_widen(q), _widen(k), _widen(v), a, b, S0, cu, C,
+                                 additive=True)
+    assert _rel(o, o_ref) < 1e-11
+    assert _rel(S, S_ref) < 1e-11
