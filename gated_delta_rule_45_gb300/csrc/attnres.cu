@@ -82,6 +82,12 @@ __device__ __forceinline__ void st_f32(float* p, const float (&x)[V]) {
         *reinterpret_cast<float4*>(p + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
 }
 
+// A contiguous row brought into L2 by the bulk-copy unit (no registers, no
+// completion to wait for).  The address and the size are multiples of 16 bytes.
+__device__ __forceinline__ void l2_prefetch_row(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 struct AttnResParams {
     const void* blocks;
     const float* partial;
@@ -119,6 +125,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attnres_kernel(const Att
 
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
         const size_t row = (size_t)t * p.d;
+        {   // the next token's source rows: one bulk L2 prefetch per source, so that
+            // they stream in from HBM while this token's dependent rounds run
+            const int64_t tn = t + gridDim.x;
+            const size_t nrow = (size_t)tn * p.d;
+            for (int j = tid; tn < p.T && j < nb + 2; j += blockDim.x) {
+                const void* src = nullptr;
+                uint32_t bytes = (uint32_t)(p.d * sizeof(T));
+                if (j < nb) src = blocks + (size_t)j * plane + nrow;
+                else if (j == nb) { src = partial ? partial + nrow : nullptr; bytes = (uint32_t)(p.d * 4); }
+                else src = h_last ? h_last + nrow : nullptr;
+                if (src) l2_prefetch_row(src, bytes);
+            }
+        }
         // the running sum partial + h_last (partial may be the output buffer itself)
         auto running = [&](int c, float (&x)[V]) {
             float y[V];
@@ -244,7 +263,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attnres_kernel(const Att
             }
             Vec<T>::store(hout + row + (size_t)c * V, o);
         }
-        __syncthreads();   // red and wgt are reused by the next token
+        // No barrier here: the next token writes red only after passing this
+        // token's second barrier (warp 0 has read red by then), and rewrites wgt
+        // only after its own first barrier (every thread has read wgt by then).
     }
 }
 
