@@ -58,6 +58,7 @@ def _layer_case(T, d, nb, with_partial, with_last, dtype, seed, inplace=False, b
     dict(T=99, d=1024, nb=3, with_partial=True, with_last=True),      # later layers
     dict(T=64, d=4096, nb=2, with_partial=True, with_last=True),      # several pieces per thread
     dict(T=40, d=64, nb=63, with_partial=True, with_last=False),      # 64 sources, narrow rows
+    dict(T=48, d=8192, nb=2, with_partial=True, with_last=True),      # wide rows, four pieces per thread
 ])
 def test_attnres_layer_matches_oracle(case, dtype):
     _layer_case(**case, dtype=dtype, seed=hash(tuple(case.values())) % 1000)
