@@ -102,6 +102,7 @@ struct AttnResParams {
 };
 
 constexpr int kBatch = 4;   // stored blocks whose pieces are in flight together
+static_assert(kBatch == 4, "the warp reduce-scatter of pass 1 is written for four sources");
 constexpr int kCtasPerSm = 4;   // resident CTAs: 64 registers a thread
 
 template <typename T>
@@ -183,13 +184,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attnres_kernel(const Att
                     }
                 }
             }
+            // reduce-scatter of the four sums over the warp: after the exchanges
+            // across 16 and 8 lanes each lane carries one source's partial sum,
+            // and lane 8 v ends with source v's total
+            const bool hi16 = lane & 16, hi8 = lane & 8;
+            const float b0 = (hi16 ? acc[2] : acc[0]) +
+                             __shfl_xor_sync(0xffffffffu, hi16 ? acc[0] : acc[2], 16);
+            const float b1 = (hi16 ? acc[3] : acc[1]) +
+                             __shfl_xor_sync(0xffffffffu, hi16 ? acc[1] : acc[3], 16);
+            float a = (hi8 ? b1 : b0) + __shfl_xor_sync(0xffffffffu, hi8 ? b0 : b1, 8);
 #pragma unroll
-            for (int jj = 0; jj < kBatch; ++jj) {
-                float a = acc[jj];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                if (lane == 0 && j0 + jj < nb) red[warp][j0 + jj] = a;
-            }
+            for (int o = 4; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if ((lane & 7) == 0 && j0 + (lane >> 3) < nb) red[warp][j0 + (lane >> 3)] = a;
         }
         if (has_p) {   // the running sum, stored on the way
             float acc = 0.f;
