@@ -28,7 +28,7 @@ def _worker(rank, world, port, out):
 def test_two_rank_max_time_and_sum_of_units():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()   # no fork of this multi-threaded process
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, port, out), nprocs=world, join=True,
                        start_method="spawn")
