@@ -200,16 +200,19 @@ BWD_MMA_FMA_PER_BLOCK_CHUNK = 3_407_872 + 21_495_808
 
 
 # ---------------------------------------------------------------- CPU oracle
-def time_oracle_sample(d, steps, pairs_wanted: int, budget_s: float, seed: int = 0):
+def time_oracle_sample(d, steps, pairs_wanted: int, budget_s: float, seed: int = 0,
+                       threads: int | None = None):
     """Time the oracle on sampled (sequence, head) pairs of the workload (prefill
-    over the whole sequence, then the 32 decode tokens).  Returns (tokens/s,
-    cores, description).  A token is counted per head, divided by H to give
+    over the whole sequence, then the 32 decode tokens), on ``threads`` threads
+    (default: every host core this process may use).  Returns (tokens/s, cores,
+    description, seconds).  A token is counted per head, divided by H to give
     tokens (all heads) per second, the unit of the GPU figure."""
     import oracle
     spec = d["spec"]
     rng = np.random.default_rng(seed)
     cu = d["cu_seqlens"].numpy()
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = threads or (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                        else os.cpu_count())
     order = rng.permutation(spec.num_seqs * spec.H)
     chosen = []
     token_heads = 0
@@ -247,7 +250,8 @@ def time_oracle_sample(d, steps, pairs_wanted: int, budget_s: float, seed: int =
     th = int(pcu[-1])
     desc = (f"{len(chosen)} (sequence, head) pairs of the varlen workload, each over its "
             f"whole prefill plus its 32 decode tokens: {th} token-heads, fp64, "
-            f"{dt:.1f} s on {cores} threads; tokens/s = token-heads/s / H")
+            f"{dt:.1f} s on {cores} thread{'s' if cores != 1 else ''}; "
+            f"tokens/s = token-heads/s / H")
     return th / dt / spec.H, cores, desc, dt
 
 
@@ -501,8 +505,13 @@ def run_ours(args):
         if not args.no_cpu_baseline:
             v, cores, desc, _ = time_oracle_sample(d, steps, pairs_wanted=64,
                                                    budget_s=args.ref_budget)
+            # the same oracle on one thread, over a quarter of the budget
+            v1, _, desc1, _ = time_oracle_sample(d, steps, pairs_wanted=64,
+                                                 budget_s=args.ref_budget / 4, seed=1, threads=1)
             line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                    "sample": desc}
+                                    "sample": desc,
+                                    "single_core": {"value": v1, "unit": UNIT, "cores": 1,
+                                                    "sample": desc1}}
         print(json.dumps(line), flush=True)
 
 
