@@ -119,6 +119,82 @@ def pin_incremental_matches_formula(ar) -> float:
     return err
 
 
+def _constant_layer_inputs(h0, c, qs, sizes, scale):
+    """Closed form of every layer's input in a blocked network whose layers all
+    output the same array c (whatever their input).  A finished block of n
+    layers then sums to n c, and a block's partial sum after i layers is i c,
+    so layer (block, i) attends over h0 and multiples m_j c of c:
+
+        h = (w_0 h0 + (sum_j w_j m_j) c),   w = softmax(scale q.h0, scale m_j q.c)
+
+    with multipliers m_j = the finished blocks' sizes, then i when i >= 1.
+    Returns the inputs and, per layer, the multiplier of the running sum the
+    layer forms (i at i >= 1; at a block's first layer, the size of the block
+    just finished; None for the first block's first layer)."""
+    ins, run_mult = [], []
+    finished, layer, prev = [], 0, None
+    for n_size in sizes:
+        for i in range(n_size):
+            q = qs[layer]
+            mults = list(finished) + ([i] if i >= 1 else [])
+            a0 = scale * (h0 @ q)                        # [T]
+            ac = scale * (c @ q)                         # [T]
+            logits = np.stack([a0] + [m * ac for m in mults], axis=1)
+            logits = logits - logits.max(axis=1, keepdims=True)
+            w = np.exp(logits)
+            w = w / w.sum(axis=1, keepdims=True)
+            cm = sum(w[:, 1 + j] * m for j, m in enumerate(mults)) if mults else 0.0
+            ins.append(w[:, :1] * h0 + np.asarray(cm)[..., None] * c)
+            run_mult.append(i if i >= 1 else prev)
+            layer += 1
+        finished.append(n_size)
+        prev = n_size
+    return ins, run_mult
+
+
+def _constant_case():
+    rng = np.random.default_rng(48)
+    T, d = 8, 10
+    sizes = [3, 1, 4, 2]
+    h0 = rng.standard_normal((T, d))
+    c = rng.standard_normal((T, d))
+    qs = rng.standard_normal((sum(sizes), d))
+    return h0, c, qs, sizes, 0.4
+
+
+def pin_constant_layers_blocked(ar) -> float:
+    """The blocked network's inputs against the closed form for layers that
+    all output the same array (block sums are integer multiples of it)."""
+    h0, c, qs, sizes, scale = _constant_case()
+    expect, _ = _constant_layer_inputs(h0, c, qs, sizes, scale)
+    got, _ = ar.blocked_network(h0, lambda i, h: c, qs, sizes, scale)
+    return max(_rel(a, b) for a, b in zip(got, expect))
+
+
+def pin_constant_layers_step(ar) -> float:
+    """layer_step driven as a model drives it (stored block sums, the running
+    sum carried between layers) on the same network: each input and each
+    running sum it returns against the closed form."""
+    h0, c, qs, sizes, scale = _constant_case()
+    expect, mult = _constant_layer_inputs(h0, c, qs, sizes, scale)
+    blocks, partial, h_last = [h0], None, None
+    err, layer = 0.0, 0
+    for n_size in sizes:
+        for i in range(n_size):
+            h, P = ar.layer_step(np.stack(blocks), partial, h_last, qs[layer], scale)
+            err = max(err, _rel(h, expect[layer]))
+            if mult[layer] is None:
+                err = max(err, 0.0 if P is None else 1.0)
+            else:
+                err = max(err, _rel(P, mult[layer] * c))
+            if i == 0 and P is not None:      # P is the previous block's sum
+                blocks.append(P)
+                P = None
+            layer += 1
+            partial, h_last = P, c
+    return err
+
+
 PINS = {
     "library_attention": (pin_library_attention, 1e-12),
     "zero_query_is_mean": (pin_zero_query_is_mean, 1e-14),
@@ -127,6 +203,8 @@ PINS = {
     "source_order": (pin_source_order, 1e-14),
     "unit_blocks_are_plain": (pin_unit_blocks_are_plain, 1e-13),
     "incremental_matches_formula": (pin_incremental_matches_formula, 1e-13),
+    "constant_layers_blocked": (pin_constant_layers_blocked, 1e-13),
+    "constant_layers_step": (pin_constant_layers_step, 1e-13),
 }
 
 

@@ -50,7 +50,8 @@ def test_mutant_is_caught(tmp_path, name):
     assert src.count(old) == 1, f"mutation anchor for {name} not unique"
     path = tmp_path / "attnres_mutant.py"
     path.write_text(src.replace(old, new))
-    assert pins.failing_pins(_load(str(path))), f"mutant {name} passed every pin"
+    failing = pins.failing_pins(_load(str(path)))
+    assert len(failing) >= 2, f"mutant {name} tripped only {failing}"
 
 
 def test_unmutated_copy_passes(tmp_path):

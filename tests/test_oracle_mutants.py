@@ -86,7 +86,8 @@ def test_mutant_is_caught(tmp_path, name):
     old, new = MUTANTS[name]
     lib = _build_mutant(tmp_path, old, new, name)
     failing = oracle_pins.failing_pins(lib)
-    assert failing, f"mutant {name} passed every pin"
+    # two independent pins per mistake, so that no single pin carries one alone
+    assert len(failing) >= 2, f"mutant {name} tripped only {failing}"
 
 
 @pytest.mark.parametrize("name", sorted(BACKWARD_MUTANTS))
@@ -94,7 +95,7 @@ def test_backward_mutant_is_caught(tmp_path, name):
     old, new = BACKWARD_MUTANTS[name]
     lib = _build_mutant(tmp_path, old, new, name)
     failing = oracle_backward_pins.failing_pins(lib)
-    assert failing, f"backward mutant {name} passed every pin"
+    assert len(failing) >= 2, f"backward mutant {name} tripped only {failing}"
 
 
 def test_backward_tape_segment_does_not_change_results(tmp_path):
