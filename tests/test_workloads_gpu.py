@@ -108,3 +108,22 @@ def test_l2_resident_contraction_case():
     ref = parity.oracle_pairs(d, [(n, 0) for n in range(spec.num_seqs)])
     wo, ws = parity.compare_pairs(d, o, S_T, ref)
     assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
+
+
+@pytest.mark.gpu
+def test_cuda_path_matches_the_fixture():
+    """The stored small case (two sequences of 3 and 6 tokens, d = 16, fp32,
+    chunk 16) against its outputs, written by the oracle alone."""
+    from test_golden import load_fixture
+
+    _, x, y = load_fixture()
+    dev = lambda a, dt=torch.float32: torch.from_numpy(a).to(dt).cuda()
+    o, S_T = kda.prefill(dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["alpha"]),
+                         dev(x["beta"]), dev(x["S0"]), dev(x["cu_seqlens"], torch.int32),
+                         chunk=16, check_device_status=True)
+    torch.cuda.synchronize()
+    o, S_T = o.double().cpu().numpy(), S_T.double().cpu().numpy()
+    cu = x["cu_seqlens"]
+    for n in range(len(cu) - 1):
+        assert parity.rel(o[cu[n]:cu[n + 1]], y["o"][cu[n]:cu[n + 1]]) <= parity.TOL_FP32
+        assert parity.rel(S_T[n], y["S_T"][n]) <= parity.TOL_FP32
