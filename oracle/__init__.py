@@ -185,7 +185,7 @@ def backward(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, nthreads: i
     return out
 
 
-def decode_step(q, k, v, alpha, beta, S, additive: bool = False):
+def decode_step(q, k, v, alpha, beta, S, additive: bool = False, *, lib=None):
     """One recurrent step for B independent sequences.
 
     q, k: [B, H, d_k]; v, alpha: [B, H, d_v]; beta: [B, H]; S: [B, H, d_v, d_k]
@@ -194,7 +194,8 @@ def decode_step(q, k, v, alpha, beta, S, additive: bool = False):
     """
     B = q.shape[0]
     cu = np.arange(B + 1, dtype=np.int32)
-    return prefill(q, k, v, alpha, beta, np.asarray(S, dtype=np.float64), cu, additive=additive)
+    return prefill(q, k, v, alpha, beta, np.asarray(S, dtype=np.float64), cu, lib=lib,
+                   additive=additive)
 
 
 def max_threads(lib=None) -> int:

@@ -280,6 +280,34 @@ def pin_additive_gated_closed_form(lib) -> float:
 
 
 # name -> (function, tolerance).  Tolerances are a few hundred fp64 roundings.
+def pin_decode_continuation(lib) -> float:
+    """A decode step is the recurrence over sequences of length one: a packed
+    prefill of each sequence's first tokens, then n batched decode steps (one
+    token of every sequence per step), equals the prefill of all the tokens,
+    sequence by sequence; under both update rules."""
+    rng = np.random.default_rng(10)
+    lens, n, H, d_k, d_v = [5, 8, 3], 4, 2, 6, 5
+    B = len(lens)
+    q, k, v, alpha, beta, S0, cu_full = _random_problem(rng, [L + n for L in lens], H, d_k, d_v)
+    head = np.concatenate([np.arange(cu_full[b], cu_full[b] + lens[b]) for b in range(B)])
+    cu = np.zeros(B + 1, np.int32)
+    cu[1:] = np.cumsum(lens)
+    err = 0.0
+    for additive in (False, True):
+        o_full, S_full = oracle.prefill(q, k, v, alpha, beta, S0, cu_full, lib=lib,
+                                        additive=additive)
+        o_p, S = oracle.prefill(q[head], k[head], v[head], alpha[head], beta[head], S0, cu,
+                                lib=lib, additive=additive)
+        err = max(err, _rel(o_p, o_full[head]))
+        for j in range(n):
+            tok = np.array([cu_full[b] + lens[b] + j for b in range(B)])
+            o_d, S = oracle.decode_step(q[tok], k[tok], v[tok], alpha[tok], beta[tok], S,
+                                        additive, lib=lib)
+            err = max(err, _rel(o_d, o_full[tok]))
+        err = max(err, _rel(S, S_full))
+    return err
+
+
 PINS = {
     "naive_linear_attention": (pin_naive_linear_attention, 1e-12),
     "pure_decay": (pin_pure_decay, 1e-12),
@@ -289,6 +317,7 @@ PINS = {
     "row_permutation": (pin_row_permutation, 1e-13),
     "split_resume": (pin_split_resume, 1e-13),
     "varlen_independence": (pin_varlen_independence, 1e-13),
+    "decode_continuation": (pin_decode_continuation, 1e-13),
     "additive_is_naive_linear_attention": (pin_additive_is_naive_linear_attention, 1e-12),
     "additive_gated_closed_form": (pin_additive_gated_closed_form, 1e-12),
 }
