@@ -124,7 +124,29 @@ def _dtype_code(t: torch.Tensor) -> int:
         return BF16
     if t.dtype == torch.float32:
         return FP32
-    raise TypeError(f"q, k, v must be bfloat16 or float32, got {t.dtype}")
+    raise TypeError(f"the storage dtype must be bfloat16 or float32, got {t.dtype}")
+
+
+# Types are checked before placement, for every entry point: the C ABI reads
+# alpha, beta, states and gradients as fp32 and cu_seqlens as int32, so a
+# tensor of another type would be misread rather than rejected.
+def _check_qkv(q, *others):
+    """q and the tensors stored like it (k, v, o, dO) share one dtype, bf16 or fp32."""
+    _dtype_code(q)
+    for t in others:
+        if t is not None and t.dtype != q.dtype:
+            raise TypeError("q, k, v and the tensors stored like them must share one dtype")
+
+
+def _check_f32(what: str, *ts):
+    for t in ts:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{what} must be float32")
+
+
+def _check_int32(cu_seqlens):
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
 
 
 def _check_cuda(*ts):
@@ -153,19 +175,14 @@ def prefill_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace, *, chu
     cu_seqlens: int32 [N+1] on the device; S_T: [N, H, d_v, d_k] fp32 (may be S0);
     workspace: a uint8 device tensor of at least ``workspace_size(N)`` bytes.
     """
+    _check_int32(cu_seqlens)
+    _check_f32("alpha, beta and the states", alpha, beta, S0, S_T)
+    _check_qkv(q, k, v, o)
     _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace)
     T, H, d_k = q.shape
     d_v = v.shape[2]
     N = cu_seqlens.numel() - 1
-    if cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
-    if alpha.dtype != torch.float32 or beta.dtype != torch.float32:
-        raise TypeError("alpha and beta must be float32")
-    if S_T.dtype != torch.float32 or (S0 is not None and S0.dtype != torch.float32):
-        raise TypeError("states must be float32")
     dt = _dtype_code(q)
-    if k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype:
-        raise TypeError("q, k, v and o must share one dtype")
     st = load().kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
                                _ptr(cu_seqlens), N, T, H, d_k, d_v, dt, chunk, _ptr(o),
                                _ptr(S_T), _ptr(workspace), workspace.numel(), _KERNELS[kernel],
@@ -180,20 +197,17 @@ def prefill_gates_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace, 
     """Enqueue kda_prefill_gates: as prefill_into with the forget gate in layout `gate`:
     "channel" alpha [T, H, d_v] fp32, "head" alpha [T, H] fp32 (one gate per head),
     "log_bf16" log alpha [T, H, d_v] bf16."""
-    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace)
     code, adt, arank = _GATES[gate]
+    if alpha.dtype != adt or alpha.dim() != arank:
+        raise TypeError(f"gate layout {gate!r} wants a rank-{arank} {adt} tensor")
+    _check_int32(cu_seqlens)
+    _check_f32("beta and the states", beta, S0, S_T)
+    _check_qkv(q, k, v, o)
+    _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace)
     T, H, d_k = q.shape
     d_v = v.shape[2]
     N = cu_seqlens.numel() - 1
-    if alpha.dtype != adt or alpha.dim() != arank:
-        raise TypeError(f"gate layout {gate!r} wants a rank-{arank} {adt} tensor")
-    if cu_seqlens.dtype != torch.int32 or beta.dtype != torch.float32:
-        raise TypeError("cu_seqlens must be int32 and beta float32")
-    if S_T.dtype != torch.float32 or (S0 is not None and S0.dtype != torch.float32):
-        raise TypeError("states must be float32")
     dt = _dtype_code(q)
-    if k.dtype != q.dtype or v.dtype != q.dtype or o.dtype != q.dtype:
-        raise TypeError("q, k, v and o must share one dtype")
     st = load().kda_prefill_gates(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), code, _ptr(beta),
                                   _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v, dt, chunk,
                                   _ptr(o), _ptr(S_T), _ptr(workspace), workspace.numel(),
@@ -243,6 +257,9 @@ def prefill_noalloc_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, *, chunk:
     """Enqueue kda_prefill_noalloc: like ``prefill_into`` but the scratch lives in
     the library (for callers that cannot allocate).  Calls must not overlap on
     the GPU; at most NOALLOC_MAX_SEQS sequences."""
+    _check_int32(cu_seqlens)
+    _check_f32("alpha, beta and the states", alpha, beta, S0, S_T)
+    _check_qkv(q, k, v, o)
     _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T)
     T, H, d_k = q.shape
     d_v = v.shape[2]
@@ -271,9 +288,9 @@ def decode_step(q, k, v, alpha, beta, S, o=None, *, stream=None):
     d_v = v.shape[2]
     if o is None:
         o = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
+    _check_f32("S, alpha and beta", S, alpha, beta)
+    _check_qkv(q, k, v, o)
     _check_cuda(q, k, v, alpha, beta, S, o)
-    if S.dtype != torch.float32 or alpha.dtype != torch.float32 or beta.dtype != torch.float32:
-        raise TypeError("S, alpha and beta must be float32")
     dt = _dtype_code(q)
     st = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S),
                                 B, H, d_k, d_v, dt, _ptr(o), _stream_ptr(stream))
@@ -291,11 +308,11 @@ def decode_step_gates(q, k, v, alpha, beta, S, o=None, *, gate: str = "channel",
     d_v = v.shape[2]
     if o is None:
         o = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
-    _check_cuda(q, k, v, alpha, beta, S, o)
     if alpha.dtype != adt or alpha.dim() != arank:
         raise TypeError(f"gate layout {gate!r} wants a rank-{arank} {adt} tensor")
-    if S.dtype != torch.float32 or beta.dtype != torch.float32:
-        raise TypeError("S and beta must be float32")
+    _check_f32("S and beta", S, beta)
+    _check_qkv(q, k, v, o)
+    _check_cuda(q, k, v, alpha, beta, S, o)
     dt = _dtype_code(q)
     st = load().kda_decode_step_gates(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), code, _ptr(beta),
                                       _ptr(S), B, H, d_k, d_v, dt, _ptr(o), _stream_ptr(stream))
@@ -310,6 +327,9 @@ def prefill_additive_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspac
     T, H, d_k = q.shape
     d_v = v.shape[2]
     N = cu_seqlens.numel() - 1
+    _check_int32(cu_seqlens)
+    _check_f32("alpha, beta and the states", alpha, beta, S0, S_T)
+    _check_qkv(q, k, v, o)
     _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace)
     st = load().kda_prefill_additive(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
                                      _ptr(S0), _ptr(cu_seqlens), N, T, H, d_k, d_v,
@@ -342,6 +362,8 @@ def decode_step_additive(q, k, v, alpha, beta, S, o=None, *, stream=None):
     d_v = v.shape[2]
     if o is None:
         o = torch.empty((B, H, d_v), dtype=q.dtype, device=q.device)
+    _check_f32("S, alpha and beta", S, alpha, beta)
+    _check_qkv(q, k, v, o)
     _check_cuda(q, k, v, alpha, beta, S, o)
     st = load().kda_decode_step_additive(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
                                          _ptr(S), B, H, d_k, d_v, _dtype_code(q), _ptr(o),
@@ -368,19 +390,15 @@ def backward_into(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T, grads, workspa
     ``backward_workspace_size`` bytes.
     """
     dS0 = grads.get("dS0")
+    _check_int32(cu_seqlens)
+    _check_qkv(q, k, v, dO)
+    _check_f32("alpha, beta, states and gradients", alpha, beta, S0, dS_T, grads["dq"],
+               grads["dk"], grads["dv"], grads["dalpha"], grads["dbeta"], dS0)
     _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T, grads["dq"], grads["dk"],
                 grads["dv"], grads["dalpha"], grads["dbeta"], dS0, workspace)
     T, H, d_k = q.shape
     d_v = v.shape[2]
     N = cu_seqlens.numel() - 1
-    if cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
-    if dO.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k, v and dO must share one dtype")
-    for t in (alpha, beta, S0, dS_T, grads["dq"], grads["dk"], grads["dv"], grads["dalpha"],
-              grads["dbeta"], dS0):
-        if t is not None and t.dtype != torch.float32:
-            raise TypeError("alpha, beta, states and gradients must be float32")
     st = load().kda_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
                              _ptr(cu_seqlens), N, T, H, d_k, d_v, _dtype_code(q), chunk,
                              _ptr(dO), _ptr(dS_T), _ptr(grads["dq"]), _ptr(grads["dk"]),
@@ -427,11 +445,10 @@ def backward_gates(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T=None, *, gate:
     N = cu_seqlens.numel() - 1
     if alpha.dtype != adt or alpha.dim() != arank:
         raise TypeError(f"gate layout {gate!r} wants a rank-{arank} {adt} tensor")
+    _check_int32(cu_seqlens)
+    _check_f32("beta and the states", beta, S0, dS_T)
+    _check_qkv(q, k, v, dO)
     _check_cuda(q, k, v, alpha, beta, S0, cu_seqlens, dO, dS_T)
-    if cu_seqlens.dtype != torch.int32 or beta.dtype != torch.float32:
-        raise TypeError("cu_seqlens must be int32 and beta float32")
-    if dO.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k, v and dO must share one dtype")
     dev = q.device
     gshape = (T, H) if gate == "head" else (T, H, d_v)
     grads = {"dq": torch.zeros((T, H, d_k), dtype=torch.float32, device=dev),
@@ -469,15 +486,13 @@ def attnres_layer(blocks, q, *, partial=None, h_last=None, partial_out=None, blo
     nb, T, d = blocks.shape
     if h is None:
         h = torch.empty((T, d), dtype=blocks.dtype, device=blocks.device)
-    _check_cuda(blocks, q, partial, h_last, partial_out, block_out, h)
-    if q.dtype != torch.float32:
-        raise TypeError("q must be float32")
-    for t in (partial, partial_out):
-        if t is not None and t.dtype != torch.float32:
-            raise TypeError("the running sum is float32")
+    _dtype_code(blocks)
+    _check_f32("q", q)
+    _check_f32("the running sum", partial, partial_out)
     for t in (h_last, block_out, h):
         if t is not None and t.dtype != blocks.dtype:
             raise TypeError("h_last, block_out and h share the dtype of blocks")
+    _check_cuda(blocks, q, partial, h_last, partial_out, block_out, h)
     if scale is None:
         scale = 1.0 / float(d) ** 0.5
     st = load().attnres_layer(_ptr(blocks) if nb > 0 else None, nb, _ptr(partial), _ptr(h_last),
