@@ -51,6 +51,13 @@ extern "C" {
  *
  * Supported: dtype KDA_BF16 or KDA_FP32, d a multiple of 8, 1 to 64 sources.
  * T == 0 is a valid no-op.
+ *
+ * Returns, before any launch: KDA_ERR_INVALID_ARG for a negative count or
+ * size, an unknown dtype, no source at all, partial_out or block_out without
+ * partial or h_last, a missing q, h or (num_blocks > 0) blocks, a pointer not
+ * 16-byte aligned, or overlapping buffers; KDA_ERR_UNSUPPORTED for d not a
+ * multiple of 8 or more than 64 sources.  KDA_ERR_CUDA if the launch fails.
+ * The kernel has no data-dependent error: any finite inputs give a result.
  */
 kda_status attnres_layer(const void* blocks, int32_t num_blocks, const float* partial,
                          const void* h_last, float* partial_out, void* block_out,
