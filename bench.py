@@ -36,11 +36,36 @@ from gated_delta_rule_45_gb300 import synth  # noqa: E402
 METRIC = "KDA prefill tokens/s & decode state-updates/s at 1 GB300; % of TC/HBM roofline"
 UNIT = "tokens/s"
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
-# kernel (the prefill kernel on this workload's full-size batch, 1-pass ncu
-# capture; see profiles/kda_prefill_tc_prefill_workload.md).  Must be set back
-# to None whenever that kernel changes until it is captured again.
-NCU_TRAFFIC_BYTES_PER_LAUNCH = 10.31e9
+# DRAM traffic of one launch of the dominant kernel (the tensor-core prefill on
+# this workload's full-size batch), from a 1-pass ncu capture of
+# dram__bytes_read.sum + dram__bytes_write.sum.  It is reported only while the
+# kernel's source is the one the capture was taken on (its sha256 below);
+# after any change to the kernel it is null until captured again.
+TRAFFIC_CAPTURE = {
+    "bytes_per_launch": 10.31e9,
+    "date": "2026-12-02",
+    "sources_sha256": None,
+}
+TRAFFIC_SOURCES = ("gated_delta_rule_45_gb300/csrc/kda_prefill_tc.cu",
+                   "gated_delta_rule_45_gb300/csrc/kda_tc.cuh")
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def stored_traffic():
+    """(bytes per launch or None, where the figure comes from)."""
+    cap = TRAFFIC_CAPTURE
+    if cap["sources_sha256"] and cap["sources_sha256"] == kernel_sources_sha256():
+        return cap["bytes_per_launch"], ("ncu capture of this kernel version (" + cap["date"]
+                                         + "), dram__bytes_read.sum + dram__bytes_write.sum")
+    return None, "no ncu capture of the current kernel version"
 
 
 # ---------------------------------------------------------------- distributed
@@ -186,6 +211,13 @@ def bf16_peak():
 MMA_FLOPS_PER_BLOCK_CHUNK = (2 * 2 * 128 * 128 * 128 + 2 * 128 * 64 * 128
                              + 3 * 2 * 128 * 64 * 64 + 2 * 2 * 128 * 128 * 64
                              + 3 * 2 * 128 * 64 * 64)
+
+
+# Algorithmic flops of the chunk form per token-head (d_k = d_v = 128, C = 64),
+# every contraction counted as dense tiles: 4 C d_k + 4 C d_v + 6 d_k d_v; and
+# counting only the causal triangles that carry work: 2 C d_k + 2 C d_v + 6 d_k d_v.
+ALG_FLOPS_PER_TOKEN_HEAD = 4 * 64 * 128 + 4 * 64 * 128 + 6 * 128 * 128
+ALG_FLOPS_PER_TOKEN_HEAD_USEFUL = 2 * 64 * 128 + 2 * 64 * 128 + 6 * 128 * 128
 
 
 # Multiply-adds of the chunkwise backward per (64-value-row block, 64-token
@@ -468,6 +500,11 @@ def run_ours(args):
 
     # end to end: host buffers, copies inside the timed region
     e2e = run_e2e(args, kda, d, steps, spec, dev, stream)
+    # the other workloads' kernels, timed alone after the step (one GPU only)
+    components_more = {}
+    if ws == 1 and not args.no_components:
+        components_more = kernel_components(kda, dev, stream, steps=5, warmup=3)
+    traffic, traffic_src = stored_traffic()
 
     if rank == 0:
         ours_launches = 2 + n_dec  # planner + prefill kernel + one kernel per decode step
@@ -491,9 +528,11 @@ def run_ours(args):
                 "decode_state_updates_per_s": N * H / dec_step_s,
                 "decode_hbm_gbs": decode_bytes / dec_step_s / 1e9,
                 "decode_hbm_frac": decode_bytes / dec_step_s / 1e9 / hbm_peak,
+                "kernels_alone": components_more,
             },
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": NCU_TRAFFIC_BYTES_PER_LAUNCH,
+                         "frac": achieved / hbm_peak, "traffic": traffic,
+                         "traffic_source": traffic_src,
                          "kernel": "kda_prefill (planner + chunk kernel)",
                          "algorithmic_bytes_per_launch": prefill_bytes,
                          "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"},
@@ -626,6 +665,129 @@ def run_e2e(args, kda, d, steps, spec, dev, stream):
                         "third stream, overlapped; decode steps after the last group"}
 
 
+KERNEL_CASES = ("decode", "prefill", "long", "l2_resident")
+
+
+def prefill_case(name, kda, dev, stream, gen_device="cpu"):
+    """One prefill workload's kernel launch on device-resident inputs: dict(launch,
+    nbytes, units, unit, desc, mma_flops, alg_flops).  name: a key of
+    synth.WORKLOADS, varlen_prefill, or a gate / update variant of prefill."""
+    gate = {"prefill_head_gate": "head", "prefill_log_gate": "log_bf16"}.get(name)
+    additive = name == "prefill_additive"
+    wname = "varlen" if name == "varlen_prefill" else "prefill" if (gate or additive) else name
+    spec = synth.WORKLOADS[wname]
+    d = synth.prefill_inputs(spec, device=gen_device)
+    g = {key: (d[key].to(dev) if d[key] is not None else None)
+         for key in ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")}
+    del d["q"], d["k"], d["v"], d["alpha"], d["beta"]
+    T = int(g["cu_seqlens"][-1])
+    o = torch.empty((T, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
+    S = torch.empty((spec.num_seqs, spec.H, spec.d_v, spec.d_k), device=dev)
+    wsp = torch.empty(kda.workspace_size(spec.num_seqs, spec.H, spec.d_k, spec.d_v, spec.chunk),
+                      dtype=torch.uint8, device=dev)
+    alpha_bytes = None
+    if additive:   # the additive update of linear attention on the same inputs
+        def launch():
+            kda.prefill_additive_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                                      g["cu_seqlens"], o, S, wsp, chunk=spec.chunk,
+                                      stream=stream)
+    elif gate is None:
+        def launch():
+            kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
+                             g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
+    else:
+        # the same synthetic gates in the other layout: channel 0's gate for
+        # every channel, or log alpha rounded to bf16
+        if gate == "head":
+            ga = g["alpha"][:, :, 0].contiguous()
+            alpha_bytes = 4
+        else:
+            ga = torch.log(g["alpha"]).to(torch.bfloat16)
+            alpha_bytes = spec.d_v * 2
+
+        def launch():
+            kda.prefill_gates_into(g["q"], g["k"], g["v"], ga, g["beta"], g["S0"],
+                                   g["cu_seqlens"], o, S, wsp, gate=gate, chunk=spec.chunk,
+                                   stream=stream)
+    nbytes, _ = workload_bytes(spec, T, 0, alpha_bytes)
+    desc = (f"{name}: N={spec.num_seqs}, T={T}, H={spec.H}, d_k={spec.d_k}, "
+            f"d_v={spec.d_v}, chunk={spec.chunk}"
+            + (f", gate layout {gate}" if gate else "")
+            + (", additive update (no prediction)" if additive else ""))
+    lens = [int(x) for x in d["lengths"]]
+    chunks = sum((n + spec.chunk - 1) // spec.chunk for n in lens)
+    mma_flops = MMA_FLOPS_PER_BLOCK_CHUNK * spec.H * (spec.d_v // 128) * chunks
+    alg_flops = ALG_FLOPS_PER_TOKEN_HEAD * T * spec.H * spec.d_v // 128
+    return dict(launch=launch, nbytes=nbytes, units=T, unit="tokens/s", desc=desc,
+                mma_flops=mma_flops, alg_flops=alg_flops, token_heads=T * spec.H, d=d,
+                inputs=g)
+
+
+def decode_case(kda, dev, stream, gen_device="cpu"):
+    spec = synth.DECODE
+    d = synth.decode_inputs(spec, device=gen_device)
+    g = {key: d[key].to(dev) for key in ("q", "k", "v", "alpha", "beta", "S")}
+    o = torch.empty((spec.B, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
+
+    def launch():
+        kda.decode_step(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S"], o, stream=stream)
+    esz = 2
+    bh = spec.B * spec.H
+    nbytes = bh * (2 * spec.d_k * esz + 2 * spec.d_v * esz + spec.d_v * 4 + 4
+                   + 2 * spec.d_v * spec.d_k * 4)
+    return dict(launch=launch, nbytes=nbytes, units=bh, unit="state-updates/s",
+                desc="decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)")
+
+
+def time_launches(launch, stream, steps: int, warmup: int):
+    """Mean CUDA-event time (ms) of `launch` on `stream` after `warmup` untimed calls."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            launch()
+    torch.cuda.synchronize()
+    events = []
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+            events.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in events)
+
+
+def kernel_components(kda, dev, stream, steps: int, warmup: int) -> dict:
+    """The other workloads' kernels timed alone (CUDA events), each with its
+    throughput and roofline fraction; inputs drawn on the device (same recipe)."""
+    hbm_peak, _ = peaks()
+    tpeak, _ = bf16_peak()
+    out = {}
+    for name in KERNEL_CASES:
+        c = decode_case(kda, dev, stream, "cuda") if name == "decode" else \
+            prefill_case(name, kda, dev, stream, "cuda")
+        ms = time_launches(c["launch"], stream, steps, warmup)
+        gbs = c["nbytes"] / (ms / 1e3) / 1e9
+        r = {"ms": ms, "value": c["units"] / (ms / 1e3), "unit": c["unit"],
+             "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "workload": c["desc"]}
+        if name != "decode":
+            r["token_heads_per_s"] = c["token_heads"] / (ms / 1e3)
+        if name == "l2_resident":
+            # inputs stay in L2 between launches: the tensor pipe is the roofline;
+            # algorithmic flops (dense tiles of the chunk form) and the flops the
+            # kernel issues (operand splits included) side by side
+            alg = c["alg_flops"] / (ms / 1e3) / 1e12
+            iss = c["mma_flops"] / (ms / 1e3) / 1e12
+            r.update({"tensor_tflops_algorithmic": alg, "tensor_frac_algorithmic": alg / tpeak,
+                      "tensor_tflops_issued": iss, "tensor_frac_issued": iss / tpeak,
+                      "tensor_peak_tflops": tpeak})
+        out[name] = r
+        del c
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_component(args):
     """Time one workload's kernel alone (``--workload prefill|long|decode``): the
     other configurations, reported as kernel-level lines next to the full step."""
@@ -637,20 +799,9 @@ def run_component(args):
     hbm_peak, peak_src = peaks()
     events = []
     if args.workload == "decode":
-        spec = synth.DECODE
-        d = synth.decode_inputs(spec)
-        g = {key: d[key].to(dev) for key in ("q", "k", "v", "alpha", "beta", "S")}
-        o = torch.empty((spec.B, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
-
-        def launch():
-            kda.decode_step(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S"], o,
-                            stream=stream)
-        esz = 2
-        bh = spec.B * spec.H
-        nbytes = bh * (2 * spec.d_k * esz + 2 * spec.d_v * esz + spec.d_v * 4 + 4
-                       + 2 * spec.d_v * spec.d_k * 4)
-        units, unit = bh, "state-updates/s"
-        desc = "decode: B=256, H=32, d_k=d_v=128, bf16, fp32 state in place (1.07 GB)"
+        c = decode_case(kda, dev, stream)
+        launch, nbytes, units, unit, desc = (c["launch"], c["nbytes"], c["units"], c["unit"],
+                                             c["desc"])
     elif args.workload in ("attnres", "attnres_small"):
         # Blocked Attention Residuals over a 64-layer network (8 blocks of 8),
         # 16384 tokens of width 2048, bf16; synthetic layer outputs stand in
@@ -732,53 +883,10 @@ def run_component(args):
         desc = (f"{args.workload}: kda_backward, N={N}, T={T}, H={H}, d_k={d_k}, d_v={d_v}, "
                 f"chunk={spec.chunk}; dO bf16, dS_T fp32; all six gradients fp32")
     else:
-        gate = {"prefill_head_gate": "head", "prefill_log_gate": "log_bf16"}.get(args.workload)
-        additive = args.workload == "prefill_additive"
-        name = "varlen" if args.workload == "varlen_prefill" else \
-            "prefill" if (gate or additive) else args.workload
-        spec = synth.WORKLOADS[name]
-        d = synth.prefill_inputs(spec)
-        g = {key: (d[key].to(dev) if d[key] is not None else None)
-             for key in ("q", "k", "v", "alpha", "beta", "S0", "cu_seqlens")}
-        T = int(d["cu_seqlens"][-1])
-        o = torch.empty((T, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
-        S = torch.empty((spec.num_seqs, spec.H, spec.d_v, spec.d_k), device=dev)
-        wsp = torch.empty(kda.workspace_size(spec.num_seqs, spec.H, spec.d_k, spec.d_v, spec.chunk),
-                          dtype=torch.uint8, device=dev)
-
-        alpha_bytes = None
-        if additive:   # the additive update of linear attention on the same inputs
-            def launch():
-                kda.prefill_additive_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
-                                          g["cu_seqlens"], o, S, wsp, chunk=spec.chunk,
-                                          stream=stream)
-        elif gate is None:
-            def launch():
-                kda.prefill_into(g["q"], g["k"], g["v"], g["alpha"], g["beta"], g["S0"],
-                                 g["cu_seqlens"], o, S, wsp, chunk=spec.chunk, stream=stream)
-        else:
-            # the same synthetic gates in the other layout: channel 0's gate for
-            # every channel, or log alpha rounded to bf16
-            if gate == "head":
-                ga = g["alpha"][:, :, 0].contiguous()
-                alpha_bytes = 4
-            else:
-                ga = torch.log(g["alpha"]).to(torch.bfloat16)
-                alpha_bytes = spec.d_v * 2
-
-            def launch():
-                kda.prefill_gates_into(g["q"], g["k"], g["v"], ga, g["beta"], g["S0"],
-                                       g["cu_seqlens"], o, S, wsp, gate=gate, chunk=spec.chunk,
-                                       stream=stream)
-        nbytes, _ = workload_bytes(spec, T, 0, alpha_bytes)
-        units, unit = T, "tokens/s"
-        desc = (f"{args.workload}: N={spec.num_seqs}, T={T}, H={spec.H}, d_k={spec.d_k}, "
-                f"d_v={spec.d_v}, chunk={spec.chunk}"
-                + (f", gate layout {gate}" if gate else "")
-                + (", additive update (no prediction)" if additive else ""))
-        lens = [int(x) for x in d["lengths"]]
-        mma_flops = (MMA_FLOPS_PER_BLOCK_CHUNK * spec.H * (spec.d_v // 128)
-                     * sum((n + spec.chunk - 1) // spec.chunk for n in lens))
+        c = prefill_case(args.workload, kda, dev, stream)
+        launch, nbytes, units, unit, desc = (c["launch"], c["nbytes"], c["units"], c["unit"],
+                                             c["desc"])
+        mma_flops, alg_flops = c["mma_flops"], c["alg_flops"]
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             launch()
@@ -815,11 +923,14 @@ def run_component(args):
     if args.workload == "l2_resident":
         # inputs stay in L2 between launches: the tensor pipe, not HBM, is the roofline
         tpeak, tsrc = bf16_peak()
-        tflops = mma_flops / (ms / 1e3) / 1e12
+        tflops = alg_flops / (ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
                     "frac": tflops / tpeak, "traffic": None,
-                    "mma_flops_per_launch": mma_flops, "peak_source": tsrc,
-                    "hbm_equivalent_gbs": achieved}
+                    "algorithmic_flops_per_launch": alg_flops,
+                    "issued_mma_flops_per_launch": mma_flops,
+                    "issued_tflops": mma_flops / (ms / 1e3) / 1e12,
+                    "issued_frac": mma_flops / (ms / 1e3) / 1e12 / tpeak,
+                    "peak_source": tsrc, "hbm_equivalent_gbs": achieved}
         l2 = "L2-resident on purpose (~110 MB of inputs and states, relaunched back to back)"
     line = {
         "metric": METRIC, "value": units / (ms / 1e3), "unit": unit, "n_gpus": 1,
@@ -850,6 +961,8 @@ def main(argv=None):
     p.add_argument("--ref-budget", type=float, default=None,
                    help="seconds of CPU work per reference step / cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-components", action="store_true",
+                   help="skip timing the other workloads' kernels alone after the step")
     p.add_argument("--workload",
                    choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
                             "l2_resident", "prefill_head_gate", "prefill_log_gate",

@@ -206,6 +206,19 @@ kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream)
     return st == KDA_ERR_DEVICE_TIMEOUT ? KDA_ERR_DEVICE_TIMEOUT : KDA_ERR_DEVICE_INPUT;
 }
 
+kda_status kda_check_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t timeout_ns,
+                                  kda_stream_t stream) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < kda::WorkspaceLayout::bytes(0))
+        return KDA_ERR_INVALID_ARG;
+    if (timeout_ns < 1000 || timeout_ns > 1000000000ull) return KDA_ERR_INVALID_ARG;
+    int32_t* status =
+        reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kda::WorkspaceLayout::kStatus);
+    return kda::launch_wait_probe(status, timeout_ns, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
 // Validation and launch behind kda_decode_step / kda_decode_step_gates.
 static kda_status decode_impl(const void* q, const void* k, const void* v, const void* alpha,
                               kda_gate_format gate, const float* beta, float* S, int32_t B,

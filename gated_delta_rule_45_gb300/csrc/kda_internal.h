@@ -120,6 +120,9 @@ cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, char* 
 cudaError_t launch_split_combine(const PrefillArgs& a, const SplitLayout& L, char* ws,
                                  cudaStream_t stream);
 bool prefill_tc_supports(const PrefillArgs& a);
+// One CTA that runs the prefill kernel's wait-timeout path with nothing to
+// wait for (status: the workspace's status word, cleared first).
+cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 // The chain kernel and the row-block reduction of the backward pass (ws: the
 // workspace base, planner already enqueued).
 cudaError_t launch_backward(const BackwardArgs& a, const BackwardLayout& L, char* ws,

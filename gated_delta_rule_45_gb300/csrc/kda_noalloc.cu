@@ -5,43 +5,36 @@
 // library holds it (KDA_NOALLOC_MAX_SEQS sequences' worth, about 256 KB) until
 // the process exits.  Host code must not pass the array's name to a kernel:
 // on the host that name is only a stand-in for the symbol.  Its device
-// address is looked up once per device, with that device current, through
-// cudaGetSymbolAddress, on the first call made on that device.
+// address is looked up on every call, with the caller's device and context
+// current, through cudaGetSymbolAddress (which allocates nothing).  A symbol's
+// address belongs to one CUDA context, so no address is cached: a caller that
+// switches between driver contexts, or resets the device, gets the address of
+// the module loaded in the context that is current at the call.  The first
+// call in a context loads the module there; make it before any stream
+// capture.
 //
 // All calls share the one array.  The planner clears the status word and the
 // work counter at the start of every call and rewrites the sequence order, so
 // nothing left by the previous call is read; but two calls whose work
 // overlaps on the GPU (different streams, no ordering between them) race on
-// the array and must not be issued.
+// the array and must not be issued.  The array holds no room for the buffers
+// of the sequence-axis split, so this call never splits the sequence axis.
 #include "kda_internal.h"
-
-#include <mutex>
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr size_t kScratchBytes =
     (kda::WorkspaceLayout::kOrder + sizeof(int32_t) * (size_t)KDA_NOALLOC_MAX_SEQS + 255) &
     ~(size_t)255;
 
 static __device__ __align__(256) unsigned char kda_noalloc_scratch[kScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.
-kda_status scratch_on_current_device(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, kda_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return KDA_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+// Device address of the scratch array in the current context.
+kda_status scratch_in_current_context(void** out) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, kda_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return KDA_ERR_CUDA;
+    *out = p;
     return KDA_OK;
 }
 
@@ -56,8 +49,10 @@ extern "C" kda_status kda_prefill_noalloc(const void* q, const void* k, const vo
                                           kda_stream_t stream) {
     if (num_seqs > KDA_NOALLOC_MAX_SEQS) return KDA_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    const kda_status st = scratch_on_current_device(&scratch);
+    const kda_status st = scratch_in_current_context(&scratch);
     if (st != KDA_OK) return st;
+    // kScratchBytes covers only the schedule, so the sequence-axis split is
+    // never chosen (prefill_impl splits only when the workspace has room)
     return kda::prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
                              d_k, d_v, dtype, chunk, o, S_T, scratch, kScratchBytes,
                              KDA_KERNEL_AUTO, stream);

@@ -51,6 +51,7 @@ constexpr int C = 64;        // tokens per chunk
 constexpr int DK = 128;      // key channels
 constexpr int DVB = 128;     // value channels per work item
 constexpr int kThreads = 448;
+// Limit of every device-side wait of a prefill launch (wall time)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // TMEM columns (512 allocated)
@@ -131,6 +132,7 @@ struct TcParams {
     int32_t n_base, n_base_p, s0_lo, s0_hi, st_lo, st_hi, a_ctas, num_items_p;
     float* g_out;
     float* P_out;
+    uint64_t timeout_ns;    // limit of every device-side wait
     const float* alpha_s;   // GATE_SCALAR: alpha [T][H]
     // GATE_F32_CKPT: fp32 [slots][H][d_v][DK]; chunk c of sequence n starting
     // at token t0 in slot t0 / C + n + c
@@ -231,6 +233,7 @@ struct Ctx {
     volatile int* never;   // always 0: lets drain waits ignore the abort flag
     uint32_t tmem;
     int32_t* status;
+    uint64_t timeout_ns;   // limit of every wait
 };
 
 __device__ __forceinline__ void fail(const Ctx& cx) {
@@ -239,7 +242,7 @@ __device__ __forceinline__ void fail(const Ctx& cx) {
 }
 
 __device__ __forceinline__ bool wait1(const Ctx& cx, int b, uint32_t parity) {
-    if (mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs)) return true;
+    if (mbar_wait(&cx.bars[b], parity, cx.abort, cx.timeout_ns)) return true;
     fail(cx);
     return false;
 }
@@ -247,7 +250,7 @@ __device__ __forceinline__ bool wait1(const Ctx& cx, int b, uint32_t parity) {
 // Every lane of the calling warp waits; the warp goes on only if all lanes
 // saw the phase complete, so its control flow stays uniform.
 __device__ __forceinline__ bool warp_wait(const Ctx& cx, int b, uint32_t parity) {
-    const bool ok = mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs);
+    const bool ok = mbar_wait(&cx.bars[b], parity, cx.abort, cx.timeout_ns);
     if (__all_sync(0xffffffffu, ok)) return true;
     fail(cx);
     return false;
@@ -266,7 +269,7 @@ struct Group {
         __syncwarp();   // bar.sync is warp-aligned: reconverge after the elected wait
         named_bar_sync(bar_id, nthreads);
         if (*s == 0) return false;
-        if (!mbar_wait(&cx.bars[b], parity, cx.abort, kTimeoutNs)) {
+        if (!mbar_wait(&cx.bars[b], parity, cx.abort, cx.timeout_ns)) {
             fail(cx);
             return false;
         }
@@ -359,10 +362,10 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
     // drain: every issued copy must have landed before the CTA may exit
     if (lane == 0) {
         for (int s = 0; s < 2; ++s)
-            if (kq_issued[s]) mbar_wait(&cx.bars[B_KQ_FULL + s], (kq_issued[s] - 1) & 1, cx.never, kTimeoutNs);
-        if (a_issued) mbar_wait(&cx.bars[B_A_FULL], (a_issued - 1) & 1, cx.never, kTimeoutNs);
+            if (kq_issued[s]) mbar_wait(&cx.bars[B_KQ_FULL + s], (kq_issued[s] - 1) & 1, cx.never, cx.timeout_ns);
+        if (a_issued) mbar_wait(&cx.bars[B_A_FULL], (a_issued - 1) & 1, cx.never, cx.timeout_ns);
         for (int s = 0; s < 2; ++s)
-            if (v_issued[s]) mbar_wait(&cx.bars[B_V_FULL + s], (v_issued[s] - 1) & 1, cx.never, kTimeoutNs);
+            if (v_issued[s]) mbar_wait(&cx.bars[B_V_FULL + s], (v_issued[s] - 1) & 1, cx.never, cx.timeout_ns);
     }
     __syncwarp();
 }
@@ -509,7 +512,7 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
     }
     // drain: the MMAs issued last must finish before TMEM is released
     if (last_commit_bar >= 0)
-        mbar_wait(&cx.bars[last_commit_bar], last_commit_parity, cx.never, kTimeoutNs);
+        mbar_wait(&cx.bars[last_commit_bar], last_commit_parity, cx.never, cx.timeout_ns);
     __syncwarp();
 }
 
@@ -1049,6 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     cx.never = reinterpret_cast<volatile int*>(smem + SM_MISC + 8);
     cx.slots = reinterpret_cast<volatile int*>(smem + SM_MISC + 16);
     cx.status = p.status;
+    cx.timeout_ns = p.timeout_ns;
 
     if (tid == 0) {
         *cx.abort = 0;
@@ -1080,6 +1084,53 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
         run_token_group<SPLIT, GATE>(p, cx, tid - 64, warp, lane);
     } else {
         run_row_group<SPLIT, GATE>(p, cx, tid - 192, warp, lane);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(cx.tmem, TM_COLS);
+}
+
+// ------------------------------------------------------------------ wait probe
+// The timeout path of the kernel above, run on purpose: a CTA that allocates
+// its TMEM like the prefill kernel, one warp waiting with a short limit on an
+// mbarrier nothing arrives on (it records KDA_ERR_DEVICE_TIMEOUT and raises
+// the abort flag), a second warp waiting with the prefill's full limit on
+// another such mbarrier (it must end early, through the abort flag), then the
+// same join and TMEM release as the prefill kernel.
+__global__ void __launch_bounds__(64, 1) kda_wait_probe_kernel(int32_t* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int flags[4];
+    __shared__ uint32_t tslot;
+    const int warp = threadIdx.x >> 5;
+    Ctx cx;
+    cx.smem = nullptr;
+    cx.bars = bars;
+    cx.abort = &flags[0];
+    cx.never = &flags[1];
+    cx.slots = &flags[2];
+    cx.status = status;
+    cx.timeout_ns = timeout_ns;
+    if (threadIdx.x == 0) {
+        flags[0] = flags[1] = flags[2] = flags[3] = 0;
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tslot, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cx.tmem = tslot;
+    if (warp == 0) {
+        warp_wait(cx, 0, 0);
+    } else {
+        Ctx full = cx;
+        full.timeout_ns = kTimeoutNs;
+        warp_wait(full, 1, 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -1157,6 +1208,7 @@ bool init_params(const PrefillArgs& a, TcParams& p) {
     p.g_out = nullptr;
     p.P_out = nullptr;
     p.ckpt = nullptr;
+    p.timeout_ns = kTimeoutNs;
     return true;
 }
 
@@ -1176,6 +1228,13 @@ cudaError_t launch(TcParams& p, int grid, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_probe(int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
+    if (err != cudaSuccess) return err;
+    kda_wait_probe_kernel<<<1, 64, 0, stream>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
 
 bool prefill_tc_supports(const PrefillArgs& a) {
     // o is written in 16-byte pieces

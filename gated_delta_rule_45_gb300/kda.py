@@ -70,6 +70,8 @@ def load(path: str | None = None):
                                         ctypes.c_int, i32, vp, vp, vp]
     lib.kda_prefill_supported.restype = ctypes.c_int
     lib.kda_prefill_supported.argtypes = [ctypes.c_int, i32, i32, i32, ctypes.c_int, i32]
+    lib.kda_check_wait_timeout.restype = ctypes.c_int
+    lib.kda_check_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
     lib.kda_prefill_device_status.restype = ctypes.c_int
     lib.kda_prefill_device_status.argtypes = [vp, vp]
     lib.kda_decode_step.restype = ctypes.c_int
@@ -273,6 +275,17 @@ def prefill_noalloc_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, *, chunk:
                                     _stream_ptr(stream))
     if st != OK:
         raise KdaError(st, "kda_prefill_noalloc")
+
+
+def check_wait_timeout(workspace, timeout_ns: int, *, stream=None) -> None:
+    """Enqueue kda_check_wait_timeout: the prefill's device-side timeout path
+    run on purpose; afterwards the workspace's status reads
+    ERR_DEVICE_TIMEOUT."""
+    _check_cuda(workspace)
+    st = load().kda_check_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       int(timeout_ns), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_check_wait_timeout")
 
 
 def device_status(workspace, stream=None) -> None:

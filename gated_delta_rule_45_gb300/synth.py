@@ -80,7 +80,7 @@ WORKLOADS = {"tiny": TINY, "decode": DECODE, "prefill": PREFILL, "long": LONG, "
 
 
 def _normal(gen: torch.Generator, shape, mean: float = 0.0, std: float = 1.0) -> torch.Tensor:
-    x = torch.empty(shape, dtype=torch.float32)
+    x = torch.empty(shape, dtype=torch.float32, device=gen.device)
     x.normal_(mean=mean, std=std, generator=gen)
     return x
 
@@ -104,20 +104,24 @@ def _draw_token_inputs(gen, T, H, d_k, d_v, dtype, alpha_mu, q_norm):
     return q, k, v, alpha, beta
 
 
-def prefill_inputs(spec: PrefillSpec, generator: torch.Generator | None = None) -> dict:
-    """Draw a prefill problem on the CPU.
+def prefill_inputs(spec: PrefillSpec, generator: torch.Generator | None = None,
+                   device: str = "cpu") -> dict:
+    """Draw a prefill problem (on the CPU unless `device` says otherwise).
 
     Returns dict(q, k, v, alpha, beta, S0 (None when s0_std == 0), cu_seqlens
     int32 [N+1], lengths list, spec, generator).  The generator is returned so
-    that follow-up draws (decode steps) continue the same stream.
+    that follow-up draws (decode steps) continue the same stream.  The same
+    recipe on another device draws other numbers from the same distributions
+    (the oracle comparisons use the CPU draws; timing alone may draw on the
+    GPU, which is much faster at full size).
     """
-    gen = generator or torch.Generator(device="cpu").manual_seed(spec.seed)
+    gen = generator or torch.Generator(device=device).manual_seed(spec.seed)
     if spec.len_lo == spec.len_hi:
         lengths = [spec.len_lo] * spec.num_seqs
     else:
         lengths = torch.randint(spec.len_lo, spec.len_hi + 1, (spec.num_seqs,),
-                                generator=gen).tolist()
-    cu = torch.zeros(spec.num_seqs + 1, dtype=torch.int32)
+                                generator=gen, device=gen.device).tolist()
+    cu = torch.zeros(spec.num_seqs + 1, dtype=torch.int32, device=gen.device)
     if spec.num_seqs:
         cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
     T = int(cu[-1])
@@ -176,9 +180,10 @@ def attnres_inputs(spec: AttnResSpec, device="cpu") -> dict:
 
 
 def decode_inputs(spec: DecodeSpec, generator: torch.Generator | None = None,
-                  with_state: bool = True) -> dict:
-    """Draw one decode step on the CPU: q, k [B,H,d_k]; v, alpha [B,H,d_v]; beta [B,H]; S."""
-    gen = generator or torch.Generator(device="cpu").manual_seed(spec.seed)
+                  with_state: bool = True, device: str = "cpu") -> dict:
+    """Draw one decode step (on the CPU unless `device` says otherwise):
+    q, k [B,H,d_k]; v, alpha [B,H,d_v]; beta [B,H]; S."""
+    gen = generator or torch.Generator(device=device).manual_seed(spec.seed)
     q, k, v, alpha, beta = _draw_token_inputs(gen, spec.B, spec.H, spec.d_k, spec.d_v,
                                               spec.dtype, spec.alpha_mu, spec.q_norm)
     S = None

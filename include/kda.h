@@ -191,6 +191,26 @@ kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d
  */
 kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream);
 
+/*
+ * Runs the device-side timeout path of the prefill kernels, so that a user can
+ * see it work on their GPU.  Every wait inside the tensor-core prefill is
+ * bounded: when one runs out, its warp records KDA_ERR_DEVICE_TIMEOUT in the
+ * workspace and raises a flag that stops the CTA's other warps at their next
+ * wait; each warp waits (bounded) for the copies and MMAs it issued, the CTA
+ * frees its tensor memory and exits, and the context stays usable.  This call
+ * enqueues one CTA that allocates tensor memory as the prefill kernel does,
+ * waits with the limit `timeout_ns` on a barrier that nothing arrives on, and
+ * on a second one with the prefill's own limit (2 s) until the flag stops it.
+ * Afterwards kda_prefill_device_status(workspace) returns
+ * KDA_ERR_DEVICE_TIMEOUT.  The pages have no counterpart to this call.
+ *
+ *   workspace   device memory of at least kda_prefill_workspace_size(0, ...)
+ *               bytes, 16-byte aligned; its status word is overwritten
+ *   timeout_ns  1e3 .. 1e9 (otherwise KDA_ERR_INVALID_ARG)
+ */
+kda_status kda_check_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t timeout_ns,
+                                  kda_stream_t stream);
+
 /* Largest num_seqs that kda_prefill_noalloc accepts. */
 #define KDA_NOALLOC_MAX_SEQS 65536
 
@@ -202,12 +222,18 @@ kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream)
  * allocate once it is running, where an allocation can stall the device or
  * break a memory plan fixed in advance.
  *
- * Same arguments and results as kda_prefill, minus the workspace.  The
- * scratch it needs lives in a device array built into the library (about
- * 256 KB on every GPU that loads it, held until the process exits).  The
- * first call on a device looks up that array's address with the device
- * current; make that first call before any stream capture.  The call itself
- * allocates nothing.
+ * Same arguments and results as kda_prefill, minus the workspace, except
+ * that this call never splits the sequence axis (its scratch has no room for
+ * the segment buffers): a batch with few long chains, such as one sequence
+ * of 128K tokens with 32 heads, runs slower here than through kda_prefill
+ * with a full workspace.  The scratch it needs lives in a device array built
+ * into the library (about 256 KB on every GPU that loads it, held until the
+ * process exits).  Every call looks up that array's address in the CUDA
+ * context current at the call (cudaGetSymbolAddress, which allocates
+ * nothing), so switching driver contexts or resetting the device between
+ * calls is safe.  The first call in a context loads the library's device
+ * code there; make that first call before any stream capture.  The call
+ * itself allocates nothing.
  *
  * Every call shares the one array and leaves its contents behind; each call
  * clears what it needs cleared, but calls that overlap on the GPU (issued on
