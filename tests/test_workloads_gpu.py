@@ -26,8 +26,13 @@ def test_prefill_workload_full():
     dev = parity.to_device(d)
     o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], None,
                          dev["cu_seqlens"], chunk=spec.chunk, check_device_status=True)
-    pairs = _sample_pairs(spec.num_seqs, spec.H, 24, 0) + [(0, 0), (spec.num_seqs - 1, spec.H - 1)]
-    ref = parity.oracle_pairs(d, sorted(set(pairs)))
+    # 64 of the 256 (sequence, head) pairs, each over its whole sequence, plus
+    # every head of the first sequence and every sequence of the last head
+    pairs = _sample_pairs(spec.num_seqs, spec.H, 64, 0) \
+        + [(0, h) for h in range(spec.H)] + [(n, spec.H - 1) for n in range(spec.num_seqs)]
+    pairs = sorted(set(pairs))
+    assert len(pairs) >= 64
+    ref = parity.oracle_pairs(d, pairs)
     wo, ws = parity.compare_pairs(d, o, S_T, ref)
     assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
     assert torch.isfinite(o.float()).all() and torch.isfinite(S_T).all()
@@ -40,7 +45,8 @@ def test_long_context_workload_full():
     dev = parity.to_device(d)
     o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
                          dev["cu_seqlens"], chunk=spec.chunk, check_device_status=True)
-    pairs = [(0, 0), (0, 13), (0, 31)]
+    # every one of the 32 chains, each over all 131072 tokens
+    pairs = [(0, h) for h in range(spec.H)]
     ref = parity.oracle_pairs(d, pairs)
     wo, ws = parity.compare_pairs(d, o, S_T, ref)
     assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
@@ -69,8 +75,11 @@ def test_varlen_workload_with_decode_continuation():
     lengths = d["lengths"]
     longest = int(np.argmax(lengths))
     shortest = int(np.argmin(lengths))
-    pairs = sorted(set(_sample_pairs(spec.num_seqs, spec.H, 10, 1)
-                       + [(longest, 0), (shortest, spec.H - 1)]))
+    # 32 sampled pairs plus the longest and the shortest sequence under every head
+    pairs = sorted(set(_sample_pairs(spec.num_seqs, spec.H, 32, 1)
+                       + [(longest, h) for h in range(spec.H)]
+                       + [(shortest, h) for h in range(spec.H)]))
+    assert len(pairs) >= 64
     ref = parity.oracle_pairs(d, pairs)
     wo, ws = parity.compare_pairs(d, o, S_T, ref)
     assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)

@@ -68,8 +68,10 @@ def test_noalloc_recovers_after_a_rejected_call():
     dev = parity.to_device(d)
     o_ref, S_ref = _reference(dev, spec)
     # cu_seqlens that decreases: the planner flags it and no output is written
-    bad = dev["cu_seqlens"].clone()
-    bad[1], bad[2] = bad[2], bad[1]
+    cu = dev["cu_seqlens"].cpu().tolist()
+    cu[1], cu[2] = cu[2], cu[1]
+    bad = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    assert cu[2] < cu[1]
     o = torch.full_like(o_ref, float("nan"))
     S_T = torch.full_like(S_ref, float("nan"))
     assert _noalloc_via_c_abi(lib, dev, o, S_T, spec.chunk, cu=bad) == kda.OK
