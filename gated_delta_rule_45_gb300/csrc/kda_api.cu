@@ -203,7 +203,8 @@ kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream)
         return KDA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
     if (st == 0) return KDA_OK;
-    return st == KDA_ERR_DEVICE_TIMEOUT ? KDA_ERR_DEVICE_TIMEOUT : KDA_ERR_DEVICE_INPUT;
+    if (st == KDA_ERR_DEVICE_TIMEOUT || st == KDA_ERR_DEVICE_RANGE) return (kda_status)st;
+    return KDA_ERR_DEVICE_INPUT;
 }
 
 kda_status kda_check_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t timeout_ns,
@@ -474,6 +475,7 @@ const char* kda_status_string(kda_status s) {
         case KDA_ERR_CUDA: return "CUDA error";
         case KDA_ERR_DEVICE_INPUT: return "invalid device input (cu_seqlens)";
         case KDA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case KDA_ERR_DEVICE_RANGE: return "alpha decays too fast for the chunk form (device input)";
         default: return "unknown status";
     }
 }

@@ -345,7 +345,7 @@ __device__ void chunk_setup(const BwdParams& p, char* sm, int64_t tok0, int nval
 }
 
 __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p) {
-    if (*p.status != 0) return;
+    if (*p.status == KDA_ERR_DEVICE_INPUT) return;
     extern __shared__ __align__(128) char sm[];
     const uint32_t sb = (uint32_t)__cvta_generic_to_shared(sm);
     float* G = reinterpret_cast<float*>(sm + OFF_G);
@@ -791,7 +791,7 @@ __global__ void __launch_bounds__(NTH, 1) kda_backward_kernel(const BwdParams p)
 
 __global__ void kda_backward_reduce(const BwdParams p, float* __restrict__ dq,
                                     float* __restrict__ dk, float* __restrict__ dbeta) {
-    if (*p.status != 0) return;
+    if (*p.status == KDA_ERR_DEVICE_INPUT) return;
     const int64_t used = p.cu[p.N];
     const int64_t n4 = used * p.H * (DK / 4);
     const size_t part = (size_t)p.T * p.H * DK;
@@ -820,7 +820,7 @@ __global__ void kda_backward_reduce(const BwdParams p, float* __restrict__ dq,
 __global__ void gate_expand_kernel(const void* gate_in, int gate, const int32_t* __restrict__ cu,
                                    int N, int H, int d_v, float* __restrict__ ax,
                                    const int32_t* __restrict__ status) {
-    if (*status != 0) return;
+    if (*status == KDA_ERR_DEVICE_INPUT) return;
     const int64_t n = (int64_t)cu[N] * H * d_v;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -837,7 +837,7 @@ __global__ void gate_expand_kernel(const void* gate_in, int gate, const int32_t*
 __global__ void gate_grad_kernel(int gate, const int32_t* __restrict__ cu, int N, int H, int d_v,
                                  const float* __restrict__ ax, const float* __restrict__ dax,
                                  float* __restrict__ dgate, const int32_t* __restrict__ status) {
-    if (*status != 0) return;
+    if (*status == KDA_ERR_DEVICE_INPUT) return;
     const int64_t th_n = (int64_t)cu[N] * H;
     if (gate == KDA_GATE_HEAD_F32) {
         const int lane = threadIdx.x & 31;

@@ -9,8 +9,14 @@
 
 namespace kda {
 
+// Smallest product of alpha over the tokens of one pass of the chunk form,
+// per channel: the form divides by it, so it must stay far from the float
+// range's end.  A chunk below it on some channel is taken again in passes of
+// 16 tokens; a pass of 16 below it is reported as KDA_ERR_DEVICE_RANGE.
+constexpr float kDecayFloor = 1e-30f;
+
 // Layout of the prefill workspace (all offsets in bytes from its start).
-//   [0, 4)    int32 device status (0 = ok, KDA_ERR_DEVICE_INPUT)
+//   [0, 4)    int32 device status (0 = ok, or a KDA_ERR_DEVICE_* code)
 //   [4, 8)    int32 work counter of the persistent tensor-core kernel
 //   [16, ...) int32 order[num_seqs]: sequence indices, longest first
 struct WorkspaceLayout {

@@ -96,7 +96,7 @@ __device__ __forceinline__ void zero(float (&acc)[4][4]) {
 template <typename T, int C>
 __global__ void __launch_bounds__(kThreads)
 kda_prefill_simt_kernel(PrefillArgs a) {
-    if (*a.status != 0) return;               // planner rejected cu_seqlens
+    if (*a.status == KDA_ERR_DEVICE_INPUT) return;   // planner rejected cu_seqlens
     extern __shared__ float smem[];
     const int d_k = a.d_k, d_v = a.d_v, H = a.H;
     SimtSmem s = carve(smem, C, d_k);
@@ -126,8 +126,13 @@ kda_prefill_simt_kernel(PrefillArgs a) {
     }
     __syncthreads();
 
-    for (int64_t c0 = t_begin; c0 < t_end; c0 += C) {
-        const int nvalid = (int)min((int64_t)C, t_end - c0);
+    // A chunk whose product of alpha falls below kDecayFloor on some channel of
+    // this block is taken again as a chunk of 16 tokens (1 / gamma must stay
+    // finite); the loop then advances by the tokens actually processed.
+    int step = C;
+    for (int64_t c0 = t_begin; c0 < t_end; c0 += step) {
+      int nvalid = (int)min((int64_t)C, t_end - c0);
+      for (;;) {
         // load the chunk; padded tokens: k = q = v = 0, alpha = 1, beta = 0
         for (int idx = tid; idx < C * d_k; idx += kThreads) {
             const int t = idx / d_k, c = idx % d_k;
@@ -160,13 +165,26 @@ kda_prefill_simt_kernel(PrefillArgs a) {
         __syncthreads();
 
         // Gamma: running product of alpha over the chunk, per value channel
+        bool fast = false;
         if (tid < kDVB) {
             float g = 1.f;
             for (int t = 0; t < C; ++t) {
                 g *= s.Gs[t * kDVP + tid];
                 s.Gs[t * kDVP + tid] = g;
             }
+            fast = !(g >= kDecayFloor);
         }
+        if (__syncthreads_or(fast)) {
+            if (nvalid > 16) {   // once more, over the first 16 tokens only
+                nvalid = 16;
+                continue;
+            }
+            // even 16 tokens decay too fast for the chunk form: reported
+            if (tid == 0) atomicCAS(a.status, 0, (int32_t)KDA_ERR_DEVICE_RANGE);
+        }
+        step = nvalid;
+        break;
+      }
         // L = diag(beta) strict_lower(K K^T);  P = tril_incl(Q K^T)
         {
             float acc[4][4], accp[4][4];

@@ -66,7 +66,7 @@ namespace {
 __global__ void split_plan_kernel(const int32_t* __restrict__ cu, int N, int M,
                                   int64_t* __restrict__ vt0, int32_t* __restrict__ vlen,
                                   const int32_t* __restrict__ status) {
-    if (*status != 0) return;
+    if (*status == KDA_ERR_DEVICE_INPUT) return;
     for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
         const int64_t t0 = cu[n];
         const int len = cu[n + 1] - cu[n];
@@ -89,7 +89,7 @@ constexpr int kLd = kB + 4;    // padded row stride in shared memory
 __global__ void __launch_bounds__(256) split_combine_kernel(
     int N, int H, int d_v, int M, const float* __restrict__ sfin, const float* __restrict__ pbuf,
     const float* __restrict__ gbuf, float* __restrict__ sst, const int32_t* __restrict__ status) {
-    if (*status != 0) return;
+    if (*status == KDA_ERR_DEVICE_INPUT) return;
     extern __shared__ float sh[];
     float* sS = sh;              // [128][kLd]
     float* sP = sh + kB * kLd;   // [128][kLd]

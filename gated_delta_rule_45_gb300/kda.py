@@ -24,6 +24,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_INPUT, ERR_DEVICE_TIMEOUT = 0, 1, 2, 3, 4, 5
+ERR_DEVICE_RANGE = 6
 BF16, FP32 = 0, 1
 KERNEL_AUTO, KERNEL_CHUNK_SIMT, KERNEL_CHUNK_TC, KERNEL_CHUNK_TC_SPLIT = 0, 1, 2, 3
 _KERNELS = {"auto": KERNEL_AUTO, "simt": KERNEL_CHUNK_SIMT, "tc": KERNEL_CHUNK_TC,

@@ -54,7 +54,9 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2,   /* sizes outside what the kernels implement (see each call) */
     KDA_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
     KDA_ERR_DEVICE_INPUT = 4,  /* device data invalid: cu_seqlens not 0-based, decreasing or past T */
-    KDA_ERR_DEVICE_TIMEOUT = 5 /* a device-side wait hit its time limit; outputs are incomplete */
+    KDA_ERR_DEVICE_TIMEOUT = 5, /* a device-side wait hit its time limit; outputs are incomplete */
+    KDA_ERR_DEVICE_RANGE = 6   /* device data outside the chunk form's range: alpha decays by more
+                                  than a factor 1e30 within 16 tokens of one channel */
 } kda_status;
 
 typedef enum {

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     from gated_delta_rule_45_gb300 import kda
-    for code in range(6):
+    for code in range(7):
         assert isinstance(kda.status_string(code), str)
     assert kda.status_string(0) == "ok"
     assert lib.kda_version() >> 16 == 1

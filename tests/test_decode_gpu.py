@@ -111,3 +111,12 @@ def test_decode_additive_update():
                                       d["S"].double().numpy(), additive=True)
     assert parity.rel(o.float().cpu().numpy(), parity.round_to(o_ref[:, :, :], torch.bfloat16)) <= 2e-3
     assert parity.rel(S.cpu().numpy(), S_ref) <= 2e-5
+
+
+@pytest.mark.parametrize("mu", [1.0, 0.0, -1.0])
+def test_decode_fast_decay(mu):
+    """A decode step multiplies by alpha and divides by nothing: gates far from
+    1 are exact as well (alpha = sigmoid(N(mu, 1)))."""
+    spec = synth.DecodeSpec(B=16, H=4, d_k=128, d_v=128, alpha_mu=mu, seed=71)
+    wo, ws = _run(spec)
+    assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)

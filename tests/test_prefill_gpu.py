@@ -304,3 +304,79 @@ def test_additive_update_matches_oracle(spec):
     with pytest.raises(kda.KdaError):   # no sequence-axis split for the additive update
         kda.prefill_additive(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"],
                              dev["S0"], dev["cu_seqlens"], chunk=spec.chunk, kernel="tc_split")
+
+
+# Fast decay: per-channel gates far from 1 ("Kimi (AI)", section "Kimi Delta
+# Attention (KDA)", the forget gating line: alpha_t in (0, 1) per value
+# channel).  At alpha = sigmoid(N(-1, 1)) the product over a 64-token chunk is
+# about e^-96, beyond what the chunk form can divide by; such chunks run in
+# passes of 16 tokens.
+FAST_MU = [1.0, 0.0, -1.0]
+
+
+@pytest.mark.parametrize("mu", FAST_MU)
+def test_fast_decay_tensor_core_kernel(mu):
+    spec = synth.PrefillSpec(num_seqs=4, len_lo=1, len_hi=400, H=2, d_k=128, d_v=256,
+                             alpha_mu=mu, s0_std=0.1, seed=41)
+    d = synth.prefill_inputs(spec)
+    if not kda.supported("tc", spec.H, spec.d_k, spec.d_v, torch.bfloat16, 64):
+        pytest.skip("tensor-core kernel not available for this shape")
+    o, S_T, _ = _check(spec, "tc")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S_T).all()
+
+
+@pytest.mark.parametrize("mu", FAST_MU)
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_fast_decay_portable_kernel(mu, chunk):
+    spec = synth.PrefillSpec(num_seqs=3, len_lo=1, len_hi=300, H=2, d_k=64, d_v=48,
+                             dtype="fp32", chunk=chunk, alpha_mu=mu, s0_std=0.1, seed=42)
+    _check(spec, "simt")
+
+
+@pytest.mark.parametrize("mu", FAST_MU)
+def test_fast_decay_additive_update(mu):
+    spec = synth.PrefillSpec(num_seqs=3, len_lo=1, len_hi=300, H=2, d_k=128, d_v=128,
+                             alpha_mu=mu, s0_std=0.1, seed=43)
+    d = synth.prefill_inputs(spec)
+    dev = parity.to_device(d)
+    o_ref, S_ref = oracle.prefill(synth.bf16_bits(d["q"]), synth.bf16_bits(d["k"]),
+                                  synth.bf16_bits(d["v"]), d["alpha"].numpy(), d["beta"].numpy(),
+                                  d["S0"].double().numpy(), d["cu_seqlens"].numpy(),
+                                  additive=True)
+    cu = d["cu_seqlens"].numpy()
+    for kernel in ("simt", "tc"):
+        o, S_T = kda.prefill_additive(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"],
+                                      dev["S0"], dev["cu_seqlens"], kernel=kernel,
+                                      check_device_status=True)
+        torch.cuda.synchronize()
+        for n in range(spec.num_seqs):
+            a, b = int(cu[n]), int(cu[n + 1])
+            for h in range(spec.H):
+                if b > a:
+                    assert parity.rel_gate(o[a:b, h].float().cpu().numpy(), o_ref[a:b, h],
+                                           o.dtype) <= parity.TOL_BF16, (kernel, n, h)
+                assert parity.rel(S_T[n, h].cpu().numpy(), S_ref[n, h]) <= parity.TOL_BF16
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+def test_decay_beyond_the_chunk_forms_range_is_reported(kernel):
+    """A channel whose alpha multiplies to 1e-40 over 16 tokens: even one pass
+    of 16 cannot divide by that, and the device reports KDA_ERR_DEVICE_RANGE
+    (an input error, found on the device; nothing faults).  Sequences and heads
+    that stay in range are still right."""
+    spec = synth.PrefillSpec(num_seqs=2, len_lo=64, len_hi=200, H=2, d_k=128, d_v=128,
+                             s0_std=0.1, seed=44)
+    d = synth.prefill_inputs(spec)
+    a = int(d["cu_seqlens"][1])
+    d["alpha"][a:a + 16, 1, 5] = 10.0 ** -2.5     # sequence 1, head 1, channel 5
+    dev = parity.to_device(d)
+    with pytest.raises(kda.KdaError) as e:
+        kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                    dev["cu_seqlens"], kernel=kernel, check_device_status=True)
+    assert e.value.status == kda.ERR_DEVICE_RANGE
+    o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], kernel=kernel)
+    torch.cuda.synchronize()
+    ref = parity.oracle_pairs(d, [(0, 0), (0, 1), (1, 0)])
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
