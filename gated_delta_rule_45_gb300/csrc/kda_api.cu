@@ -121,13 +121,25 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
         }
     }
 
+    // room for the channels the tensor-core kernel may hand back to the portable one
+    const size_t redo_at = kda::WorkspaceLayout::bytes(num_seqs);
+    const size_t redo_n = kda::WorkspaceLayout::redo_bytes(num_seqs, H, d_v);
+    if (use_tc && split.M < 3 && redo_n > 0 && workspace_bytes >= redo_at + redo_n && d_v % 128 == 0)
+        a.redo = reinterpret_cast<uint32_t*>(ws + redo_at);
+
     if (kda::launch_planner(a, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (num_seqs == 0) return KDA_OK;
+    if (a.redo && cudaMemsetAsync(a.redo, 0, redo_n, stream) != cudaSuccess) return KDA_ERR_CUDA;
     cudaError_t err;
-    if (use_tc && split.M >= 3)
+    if (use_tc && split.M >= 3) {
         err = kda::launch_prefill_tc_split(a, split, ws, stream);
-    else
-        err = use_tc ? kda::launch_prefill_tc(a, stream) : kda::launch_prefill_simt(a, stream);
+    } else if (use_tc) {
+        err = kda::launch_prefill_tc(a, stream);
+        if (err == cudaSuccess && a.redo && total_tokens > 0)
+            err = kda::launch_prefill_simt_redo(a, stream);
+    } else {
+        err = kda::launch_prefill_simt(a, stream);
+    }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -140,10 +152,13 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int3
     if (num_seqs < 0) return 0;
     const size_t base = kda::WorkspaceLayout::bytes(num_seqs);
     if (H < 1 || d_k < 1 || d_v < 1) return base;
+    // the channels handed back by the tensor-core kernel, in the place the
+    // split's buffers take when it splits
+    const size_t with_redo = base + kda::WorkspaceLayout::redo_bytes(num_seqs, H, d_v);
     const int M = kda::split_segments(num_seqs, H, d_k, d_v, chunk);
-    if (M < 3) return base;
+    if (M < 3) return with_redo;
     const size_t split = kda::split_layout(num_seqs, H, d_k, d_v, M).end;
-    return split > base ? split : base;
+    return split > with_redo ? split : with_redo;
 }
 
 kda_status kda_prefill(const void* q, const void* k, const void* v, const float* alpha,

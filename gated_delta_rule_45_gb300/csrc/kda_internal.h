@@ -19,12 +19,22 @@ constexpr float kDecayFloor = 1e-30f;
 //   [0, 4)    int32 device status (0 = ok, or a KDA_ERR_DEVICE_* code)
 //   [4, 8)    int32 work counter of the persistent tensor-core kernel
 //   [16, ...) int32 order[num_seqs]: sequence indices, longest first
+//   then, for the tensor-core kernel without the sequence-axis split (whose
+//   buffers take the same place), when the workspace has room: uint32
+//   [num_seqs][H][d_v / 128][4], for each 128-channel block the channels whose
+//   chunks decayed too fast for the one-pass chunk form (one bit each); the
+//   portable kernel redoes those channels
 struct WorkspaceLayout {
     static constexpr size_t kStatus = 0;
     static constexpr size_t kCounter = 4;
     static constexpr size_t kOrder = 16;
     static size_t bytes(int32_t num_seqs) {
         size_t b = kOrder + sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 0);
+        return (b + 255) & ~(size_t)255;
+    }
+    static size_t redo_bytes(int32_t num_seqs, int32_t H, int32_t d_v) {
+        if (num_seqs <= 0 || H <= 0 || d_v < 128) return 0;
+        const size_t b = (size_t)num_seqs * H * (d_v / 128) * 4 * sizeof(uint32_t);
         return (b + 255) & ~(size_t)255;
     }
 };
@@ -67,6 +77,8 @@ struct PrefillArgs {
     int32_t* order;     // device, [num_seqs]
     int32_t gate = 0;   // kda_gate_format
     int32_t additive = 0;   // additive update of linear attention instead of the delta rule
+    // channels the tensor-core kernel hands back (WorkspaceLayout), or null
+    uint32_t* redo = nullptr;
 };
 
 struct DecodeArgs {
@@ -114,6 +126,10 @@ struct BackwardArgs {
 cudaError_t launch_planner(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+// The portable kernel over the channels the tensor-core kernel handed back in
+// a.redo: every (sequence, head, 128-channel block) with a bit set is run again
+// from S0, and only the marked channels' o and S_T are written.
+cudaError_t launch_prefill_simt_redo(const PrefillArgs& a, cudaStream_t stream);
 // The tensor-core prefill that also writes every chunk's start state (fp32
 // [slots][H][d_v][d_k], slot t0 / 64 + n + chunk) for the backward pass.
 cudaError_t launch_prefill_tc_ckpt(const PrefillArgs& a, float* ckpt, cudaStream_t stream);

@@ -2,7 +2,7 @@
 // caller-provided workspace, for callers that cannot allocate device memory.
 //
 // The scratch is a file-scope __device__ array, so every GPU that loads this
-// library holds it (KDA_NOALLOC_MAX_SEQS sequences' worth, about 256 KB) until
+// library holds it (about 512 KB) until
 // the process exits.  Host code must not pass the array's name to a kernel:
 // on the host that name is only a stand-in for the symbol.  Its device
 // address is looked up on every call, with the caller's device and context
@@ -23,9 +23,13 @@
 
 namespace {
 
-constexpr size_t kScratchBytes =
+// the schedule of KDA_NOALLOC_MAX_SEQS sequences, then room for the channels
+// the tensor-core kernel may hand back to the portable one (16 bytes per
+// (sequence, head, 128-channel block): up to 16384 such blocks)
+constexpr size_t kScheduleBytes =
     (kda::WorkspaceLayout::kOrder + sizeof(int32_t) * (size_t)KDA_NOALLOC_MAX_SEQS + 255) &
     ~(size_t)255;
+constexpr size_t kScratchBytes = kScheduleBytes + 16 * 16384;
 
 static __device__ __align__(256) unsigned char kda_noalloc_scratch[kScratchBytes];
 
@@ -51,8 +55,8 @@ extern "C" kda_status kda_prefill_noalloc(const void* q, const void* k, const vo
     void* scratch = nullptr;
     const kda_status st = scratch_in_current_context(&scratch);
     if (st != KDA_OK) return st;
-    // kScratchBytes covers only the schedule, so the sequence-axis split is
-    // never chosen (prefill_impl splits only when the workspace has room)
+    // kScratchBytes has no room for the buffers of the sequence-axis split, so
+    // that is never chosen (prefill_impl splits only when the workspace has room)
     return kda::prefill_impl(q, k, v, alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
                              d_k, d_v, dtype, chunk, o, S_T, scratch, kScratchBytes,
                              KDA_KERNEL_AUTO, stream);

@@ -93,21 +93,18 @@ __device__ __forceinline__ void zero(float (&acc)[4][4]) {
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 }
 
+// One (sequence n, head h, block vb of 64 value channels) from S0 to S_T.
+// rowmask: null (every channel written) or two words marking the channels of
+// the block whose o and S_T are written.
 template <typename T, int C>
-__global__ void __launch_bounds__(kThreads)
-kda_prefill_simt_kernel(PrefillArgs a) {
-    if (*a.status == KDA_ERR_DEVICE_INPUT) return;   // planner rejected cu_seqlens
-    extern __shared__ float smem[];
+__device__ void simt_item(const PrefillArgs& a, float* smem, int n, int h, int vb,
+                          const uint32_t* rowmask = nullptr) {
+    const uint32_t wm0 = rowmask ? rowmask[0] : 0xffffffffu;
+    const uint32_t wm1 = rowmask ? rowmask[1] : 0xffffffffu;
+    auto marked = [&](int r) { return ((r < 32 ? wm0 >> r : wm1 >> (r - 32)) & 1u) != 0u; };
     const int d_k = a.d_k, d_v = a.d_v, H = a.H;
     SimtSmem s = carve(smem, C, d_k);
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-
-    const int nvb = (d_v + kDVB - 1) / kDVB;
-    const int item = blockIdx.x;
-    const int rank = item / (H * nvb);
-    const int h = (item / nvb) % H;
-    const int vb = item % nvb;
-    const int n = a.order[rank];
     const int64_t t_begin = a.cu_seqlens[n], t_end = a.cu_seqlens[n + 1];
     const int r0 = vb * kDVB;
     const int rows = min(kDVB, d_v - r0);
@@ -263,7 +260,7 @@ kda_prefill_simt_kernel(PrefillArgs a) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int t = ty + 16 * i, r = tx + 16 * j;
-                    if (t < nvalid && r < rows) {
+                    if (t < nvalid && r < rows && marked(r)) {
                         const float y = s.Gs[t * kDVP + r] * acc[i][j];
                         Elem<T>::store(o + ((size_t)(c0 + t) * H + h) * d_v + r0 + r, y);
                     }
@@ -292,7 +289,39 @@ kda_prefill_simt_kernel(PrefillArgs a) {
 
     for (int idx = tid; idx < rows * d_k; idx += kThreads) {
         const int r = idx / d_k, c = idx % d_k;
-        a.S_T[state_off + (size_t)r * d_k + c] = s.Ss[r * s.KP + c];
+        if (marked(r)) a.S_T[state_off + (size_t)r * d_k + c] = s.Ss[r * s.KP + c];
+    }
+}
+
+template <typename T, int C>
+__global__ void __launch_bounds__(kThreads)
+kda_prefill_simt_kernel(PrefillArgs a) {
+    if (*a.status == KDA_ERR_DEVICE_INPUT) return;   // planner rejected cu_seqlens
+    extern __shared__ float smem[];
+    const int nvb = (a.d_v + kDVB - 1) / kDVB;
+    const int item = blockIdx.x;
+    const int rank = item / (a.H * nvb);
+    simt_item<T, C>(a, smem, a.order[rank], (item / nvb) % a.H, item % nvb);
+}
+
+// The channels the tensor-core kernel handed back (their decay too fast for
+// its one-pass chunks): a persistent grid walks every (sequence, head,
+// 64-channel block) and runs those with a marked channel again from S0,
+// writing o and S_T of the marked channels only (the others are right, and
+// their S0 may already be overwritten by S_T).
+template <typename T, int C>
+__global__ void __launch_bounds__(kThreads)
+kda_prefill_simt_redo_kernel(PrefillArgs a) {
+    if (*a.status == KDA_ERR_DEVICE_INPUT) return;
+    extern __shared__ float smem[];
+    const int nb64 = a.d_v / 64;
+    const int total = a.num_seqs * a.H * nb64;
+    for (int i = blockIdx.x; i < total; i += gridDim.x) {
+        const uint32_t* m = a.redo + 2 * (size_t)i;   // 64 channels: two mask words
+        if ((m[0] | m[1]) == 0u) continue;             // uniform across the CTA
+        const int n = i / (a.H * nb64), h = (i / nb64) % a.H, vb = i % nb64;
+        simt_item<T, C>(a, smem, n, h, vb, m);
+        __syncthreads();   // the next item reuses the shared memory
     }
 }
 
@@ -321,6 +350,20 @@ cudaError_t launch_simt_c(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_prefill_simt_redo(const PrefillArgs& a, cudaStream_t stream) {
+    if (!a.redo || a.dtype != KDA_BF16 || a.chunk != 64 || a.d_k > kMaxDK || a.d_v % 128 != 0)
+        return cudaErrorInvalidValue;
+    if (a.num_seqs == 0) return cudaSuccess;
+    const size_t smem = simt_smem_floats(64, kMaxDK) * sizeof(float);
+    cudaError_t err = cudaFuncSetAttribute(kda_prefill_simt_redo_kernel<__nv_bfloat16, 64>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    kda_prefill_simt_redo_kernel<__nv_bfloat16, 64><<<sm_count(), kThreads,
+                                                      simt_smem_floats(64, a.d_k) * sizeof(float),
+                                                      stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream) {
     if (a.d_k > kMaxDK) return cudaErrorInvalidValue;

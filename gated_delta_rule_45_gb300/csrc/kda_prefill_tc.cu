@@ -82,11 +82,9 @@ constexpr uint32_t SM_Y = 214528;        // [4 warps][16][YSTR] fp32 scratch of 
 constexpr uint32_t YSTR = 24;
 constexpr uint32_t SM_BAR = 220672;
 constexpr uint32_t SM_MISC = SM_BAR + 256;
-constexpr uint32_t SM_HALF = SM_MISC + 64;   // [2 rounds][2 halves][128] fp32: products of alpha
-constexpr uint32_t SM_VOTE = SM_HALF + 2048;  // [2 rounds][8 row warps] int: too fast a decay
-constexpr uint32_t SM_OST = SM_VOTE + 64;     // [8 row warps][16 tokens][32 channels] bf16
+constexpr uint32_t SM_HALF = SM_MISC + 64;   // [2][128] fp32: per-half products of alpha
+constexpr uint32_t SM_OST = SM_HALF + 1024;   // [8 row warps][16 tokens][32 channels] bf16
 constexpr uint32_t SMEM_BYTES = SM_OST + 8 * 1024 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 
 // mbarrier indices
 enum {
@@ -106,8 +104,7 @@ enum {
     B_S_DONE = 17,     // MMA commit: S += U^T K complete
     B_O_DONE = 18,     // MMA commit: O^T += U^T P^T complete
     B_O_READ = 19,     // row group (8 warps) -> O read out of TMEM (its columns are free)
-    B_ROW = 20,        // row group (8 warps): products of alpha over each half, and votes
-                       // (21-23 unused)
+    B_PAIR = 20,       // [4] the two row warps of a TMEM lane quarter swap half-chunk products
     B_V_FULL = 24,     // [2] producer -> V buffer loaded
     B_V_EMPTY = 26,    // [2] row group (8 warps) -> V buffer read
     B_COUNT = 28
@@ -135,7 +132,9 @@ struct TcParams {
     int32_t n_base, n_base_p, s0_lo, s0_hi, st_lo, st_hi, a_ctas, num_items_p;
     float* g_out;
     float* P_out;
-    uint64_t timeout_ns;    // limit of every device-side wait
+    // channels whose chunks decayed too fast for the one-pass chunk form, one
+    // bit per channel of [N][H][d_v / 128] blocks (null: reported instead)
+    uint32_t* redo;
     const float* alpha_s;   // GATE_SCALAR: alpha [T][H]
     // GATE_F32_CKPT: fp32 [slots][H][d_v][DK]; chunk c of sequence n starting
     // at token t0 in slot t0 / C + n + c
@@ -295,24 +294,10 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
     uint32_t g = 0;
     uint32_t kq_issued[2] = {0, 0}, a_issued = 0, v_issued[2] = {0, 0};
     const float* beta_st = reinterpret_cast<const float*>(cx.smem + SM_BETA);
-    // beta (and the per-head gate) of the next chunk, loaded into registers one
-    // chunk ahead so that their global-load latency never delays a TMA issue
-    float nb[2], na[2];
-    auto prefetch = [&]() {
-        if (!cur.valid) return;
-        const int64_t t0 = cur.info.t0 + (int64_t)cur.c * C;
-        const int nv = min(C, cur.info.len - cur.c * C);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int j = lane + 32 * e;
-            nb[e] = j < nv ? p.beta[(t0 + j) * p.H + cur.info.h] : 0.f;
-            if (GATE == GATE_SCALAR) na[e] = j < nv ? p.alpha_s[(t0 + j) * p.H + cur.info.h] : 1.f;
-        }
-    };
-    prefetch();
     while (cur.valid) {
         const int s = g & 1;
         const int64_t tok0 = cur.info.t0 + (int64_t)cur.c * C;
+        const int nvalid = min(C, cur.info.len - cur.c * C);
         const int h = cur.info.h;
         if (g >= 2) {
             int r = 1;
@@ -320,8 +305,15 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
             __syncwarp();
             if (!__shfl_sync(0xffffffffu, r, 0)) break;
         }
-        // two arrivals complete the stage: the TMA bytes (with the first) and
-        // the warp's beta stores (the second, after them)
+        float* bst = const_cast<float*>(beta_st) + s * C;
+        for (int j = lane; j < C; j += 32)
+            bst[j] = j < nvalid ? p.beta[(tok0 + j) * p.H + h] : 0.f;
+        if (GATE == GATE_SCALAR) {   // one gate per token rides with beta
+            float* ast = reinterpret_cast<float*>(cx.smem + SM_ALPHA) + s * C;
+            for (int j = lane; j < C; j += 32)
+                ast[j] = j < nvalid ? p.alpha_s[(tok0 + j) * p.H + h] : 1.f;
+        }
+        __syncwarp();
         if (lane == 0) {
             uint64_t* bar = &cx.bars[B_KQ_FULL + s];
             uint8_t* st = cx.smem + SM_KQ + s * KQ_STAGE;
@@ -331,21 +323,10 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
             tma_load_3d(st + 8192, &p.tm_q, bar, 0, h, (int32_t)tok0);
             tma_load_3d(st + KQ_KBLOCK + 8192, &p.tm_q, bar, 64, h, (int32_t)tok0);
         }
-        float* bst = const_cast<float*>(beta_st) + s * C;
-        bst[lane] = nb[0];
-        bst[lane + 32] = nb[1];
-        if (GATE == GATE_SCALAR) {   // one gate per token rides with beta
-            float* ast = reinterpret_cast<float*>(cx.smem + SM_ALPHA) + s * C;
-            ast[lane] = na[0];
-            ast[lane + 32] = na[1];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cx.bars[B_KQ_FULL + s]);
         ++kq_issued[s];
         if (pk) {   // transition items: alpha = 1 and v = 0, nothing to load
             ++g;
             cur.next(p);
-            prefetch();
             continue;
         }
         // alpha: one buffer, free once the row group has read it into registers
@@ -379,7 +360,6 @@ __device__ void run_producer(const TcParams& p, const Ctx& cx, int lane) {
         ++v_issued[s];
         ++g;
         cur.next(p);
-        prefetch();
     }
     // drain: every issued copy must have landed before the CTA may exit
     if (lane == 0) {
@@ -438,105 +418,97 @@ __device__ void run_mma(const TcParams& p, const Ctx& cx) {
         last_commit_parity = 0;
         ahead.next(p);
     }
-    uint32_t pc = 0;   // chain rounds (passes) issued so far
-    // the next chunk's [K;Q]K^T is due once per chunk: issued at the first
-    // point where its tiles are in (after S K^T, after S Q^T, after U^T),
-    // else after the chunk's last O MMAs, so that the token group starts its T
-    // and P as early as possible without holding up this chunk's chain
-    auto try_kqk = [&](bool& due, bool force) -> bool {
-        if (!due || !(force || kqk_ready(cx, g + 1))) return true;
-        if (!issue_kqk(p, cx, g + 1)) return false;
-        last_commit_bar = B_KQK_DONE;
-        last_commit_parity = (g + 1) & 1;
-        ahead.next(p);
-        due = false;
-        return true;
-    };
-    const volatile int* npass_slot = reinterpret_cast<const volatile int*>(cx.smem + SM_MISC + 24);
     while (cur.valid && ok) {
         const int s = g & 1;
         const uint32_t kq = kq_addr(cx, s);
-        bool kqk_due = ahead.valid;
-        // One chain round per pass: one pass per chunk, or one per 16 tokens
-        // when the row group finds the chunk's decay too fast for one pass (it
-        // publishes the count before its first X_READY).
-        int npass = 1;
-        for (int pass = 0; pass < npass && ok; ++pass, ++pc) {
-            // S K^T = S_hi K^T + S_lo K^T first (it feeds the next step of the
-            // chain), then S Q^T (needed only for the output)
-            if (!(ok = warp_wait(cx, B_S_READY, pc & 1))) break;
-            tc_fence_after();
+        // S K^T = S_hi K^T + S_lo K^T first (it feeds the next step of the chain),
+        // then S Q^T (needed only for the output)
+        if (!(ok = warp_wait(cx, B_S_READY, g & 1))) break;
+        tc_fence_after();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                if (elect_one()) {
-                    // groups: (S_hi, k-block 0), (S_hi, 1), (S_lo, 0), (S_lo, 1)
-#pragma unroll 1
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t a0 = tm + ((i >> 1) == 0 ? TM_SHI : TM_SLO) + 32 * (i & 1);
-                        const uint64_t b =
-                            smem_desc_sw128(kq + (i & 1) * KQ_KBLOCK + half * 8192, 0, 1024);
-                        mma_ts4(tm + TM_SKQ + 64 * half, a0, 8, b, 2, id_n64, i != 0);
-                    }
-                    if (half == 0) mma_commit(&cx.bars[B_SKQ_DONE]);
-                }
-                __syncwarp();
-                if (half == 0) {
-                    last_commit_bar = B_SKQ_DONE;
-                    last_commit_parity = pc & 1;
-                    if (!(ok = try_kqk(kqk_due, false))) break;
-                    // S Q^T reuses the columns the previous round's O was read from
-                    if (pc >= 1 && !(ok = warp_wait(cx, B_O_READ, (pc - 1) & 1))) break;
-                }
-            }
-            if (!ok) break;
-            if (!(ok = try_kqk(kqk_due, false))) break;
-            // U^T = X^T T^T   (hi*hi + hi*lo + lo*hi)
-            if (!(ok = warp_wait(cx, B_X_READY, pc & 1))) break;
-            if (pass == 0) {
-                npass = *npass_slot;
-                if (!(ok = warp_wait(cx, B_TP_READY + s, (g >> 1) & 1))) break;
-            }
-            const bool last_pass = pass + 1 == npass;
-            tc_fence_after();
+        for (int half = 0; half < 2; ++half) {
             if (elect_one()) {
-                const uint32_t t_hi = smem_u32(cx.smem + SM_T + s * TP_BUF);
+                // groups: (S_hi, k-block 0), (S_hi, 1), (S_lo, 0), (S_lo, 1)
 #pragma unroll 1
-                for (int part = 0; part < 3; ++part)
-                    mma_ts4(tm + TM_SKQ, tm + (part == 2 ? TM_XLO : TM_XHI), 8,
-                            smem_desc_sw128(t_hi + (part == 1 ? TP_LO : 0), 0, 1024), 2, id_n64,
-                            part != 0);
-                mma_commit(&cx.bars[B_U_DONE]);
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t a0 = tm + ((i >> 1) == 0 ? TM_SHI : TM_SLO) + 32 * (i & 1);
+                    const uint64_t b =
+                        smem_desc_sw128(kq + (i & 1) * KQ_KBLOCK + half * 8192, 0, 1024);
+                    mma_ts4(tm + TM_SKQ + 64 * half, a0, 8, b, 2, id_n64, i != 0);
+                }
+                if (half == 0) mma_commit(&cx.bars[B_SKQ_DONE]);
             }
             __syncwarp();
-            last_commit_bar = B_U_DONE;
-            last_commit_parity = pc & 1;
-            if (!(ok = try_kqk(kqk_due, false))) break;
-            // S += U^T K first (the chain), then O^T += U^T P^T
-            if (!(ok = warp_wait(cx, B_U_READY, pc & 1))) break;
-            tc_fence_after();
-            if (elect_one()) {
-                // B = the K tile read MN-major: 16 tokens (2048 bytes) per k-step
-#pragma unroll 1
-                for (int part = 0; part < 2; ++part)
-                    mma_ts4(tm + TM_S, tm + (part == 0 ? TM_XHI : TM_XLO), 8,
-                            smem_desc_sw128(kq, KQ_KBLOCK, 1024), 2048 >> 4, id_n128_bmn, 1);
-                mma_commit(&cx.bars[B_S_DONE]);
-                // the O MMAs do not read K or Q: the stage is free after the last pass
-                if (last_pass) mma_commit(&cx.bars[B_KQ_EMPTY + s]);
-                const uint32_t p_hi = smem_u32(cx.smem + SM_P + s * TP_BUF);
-#pragma unroll 1
-                for (int part = 0; part < 3; ++part)
-                    mma_ts4(tm + TM_SKQ + 64, tm + (part == 2 ? TM_XLO : TM_XHI), 8,
-                            smem_desc_sw128(p_hi + (part == 1 ? TP_LO : 0), 0, 1024), 2, id_n64, 1);
-                mma_commit(&cx.bars[B_O_DONE]);
-                if (last_pass) mma_commit(&cx.bars[B_TP_FREE + s]);
+            if (half == 0) {
+                last_commit_bar = B_SKQ_DONE;
+                last_commit_parity = g & 1;
+                // S Q^T reuses the columns the previous chunk's O was read from
+                if (g >= 1 && !(ok = warp_wait(cx, B_O_READ, (g - 1) & 1))) break;
             }
-            __syncwarp();
-            last_commit_bar = B_O_DONE;
-            last_commit_parity = pc & 1;
-            if (last_pass && !(ok = try_kqk(kqk_due, true))) break;
         }
         if (!ok) break;
+        // next chunk's [K;Q]K^T, so the token group can build its T and P early;
+        // issued here only if its tiles are in, else after the U or the S MMAs,
+        // so that it never holds up this chunk's chain
+        bool kqk_due = ahead.valid;
+        if (kqk_due && kqk_ready(cx, g + 1)) {
+            if (!(ok = issue_kqk(p, cx, g + 1))) break;
+            last_commit_bar = B_KQK_DONE;
+            last_commit_parity = (g + 1) & 1;
+            ahead.next(p);
+            kqk_due = false;
+        }
+        // U^T = X^T T^T   (hi*hi + hi*lo + lo*hi)
+        if (!(ok = warp_wait(cx, B_X_READY, g & 1))) break;
+        if (!(ok = warp_wait(cx, B_TP_READY + s, (g >> 1) & 1))) break;
+        tc_fence_after();
+        if (elect_one()) {
+            const uint32_t t_hi = smem_u32(cx.smem + SM_T + s * TP_BUF);
+#pragma unroll 1
+            for (int part = 0; part < 3; ++part)
+                mma_ts4(tm + TM_SKQ, tm + (part == 2 ? TM_XLO : TM_XHI), 8,
+                        smem_desc_sw128(t_hi + (part == 1 ? TP_LO : 0), 0, 1024), 2, id_n64,
+                        part != 0);
+            mma_commit(&cx.bars[B_U_DONE]);
+        }
+        __syncwarp();
+        last_commit_bar = B_U_DONE;
+        last_commit_parity = g & 1;
+        if (kqk_due && kqk_ready(cx, g + 1)) {
+            if (!(ok = issue_kqk(p, cx, g + 1))) break;
+            last_commit_bar = B_KQK_DONE;
+            last_commit_parity = (g + 1) & 1;
+            ahead.next(p);
+            kqk_due = false;
+        }
+        // S += U^T K first (the chain), then O^T += U^T P^T
+        if (!(ok = warp_wait(cx, B_U_READY, g & 1))) break;
+        tc_fence_after();
+        if (elect_one()) {
+            // B = the K tile read MN-major: 16 tokens (2048 bytes) per k-step
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part)
+                mma_ts4(tm + TM_S, tm + (part == 0 ? TM_XHI : TM_XLO), 8,
+                        smem_desc_sw128(kq, KQ_KBLOCK, 1024), 2048 >> 4, id_n128_bmn, 1);
+            mma_commit(&cx.bars[B_S_DONE]);
+            mma_commit(&cx.bars[B_KQ_EMPTY + s]);   // the O MMAs do not read K or Q
+            const uint32_t p_hi = smem_u32(cx.smem + SM_P + s * TP_BUF);
+#pragma unroll 1
+            for (int part = 0; part < 3; ++part)
+                mma_ts4(tm + TM_SKQ + 64, tm + (part == 2 ? TM_XLO : TM_XHI), 8,
+                        smem_desc_sw128(p_hi + (part == 1 ? TP_LO : 0), 0, 1024), 2, id_n64, 1);
+            mma_commit(&cx.bars[B_O_DONE]);
+            mma_commit(&cx.bars[B_TP_FREE + s]);
+        }
+        __syncwarp();
+        last_commit_bar = B_O_DONE;
+        last_commit_parity = g & 1;
+        if (kqk_due) {
+            if (!(ok = issue_kqk(p, cx, g + 1))) break;
+            last_commit_bar = B_KQK_DONE;
+            last_commit_parity = (g + 1) & 1;
+            ahead.next(p);
+        }
         ++g;
         cur.next(p);
     }
@@ -736,6 +708,28 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
 }
 
 // ------------------------------------------------------------------ row group
+// A chunk whose product of alpha over some channel falls below kDecayFloor is
+// beyond the one-pass chunk form (it divides by the running product): that
+// channel is handed back, in the workspace's bitmap, to the portable kernel,
+// which runs it again from S0 (so its S_T is not written here).  Without a
+// bitmap (the sequence-axis split), it is reported as KDA_ERR_DEVICE_RANGE.
+// No register carries this across the chunk loop: the bit is set after the
+// chunk's state is handed back, and read back (a global load of the bit this
+// same thread set) before the item's final state is written.
+template <bool SPLIT>
+__device__ __noinline__ void report_fast_decay(const TcParams& p, const ItemInfo& it, int r) {
+    if (!SPLIT && p.redo)
+        atomicOr(p.redo + (((size_t)it.n * p.H + it.h) * p.nvb + it.vb) * 4 + (r >> 5), 1u << (r & 31));
+    else
+        atomicCAS(p.status, 0, (int32_t)KDA_ERR_DEVICE_RANGE);
+}
+template <bool SPLIT>
+__device__ __forceinline__ bool handed_back(const TcParams& p, const ItemInfo& it, int r) {
+    if (SPLIT || !p.redo) return false;
+    const volatile uint32_t* w = p.redo + (((size_t)it.n * p.H + it.h) * p.nvb + it.vb) * 4 + (r >> 5);
+    return (*w >> (r & 31)) & 1u;
+}
+
 // Thread (r, h): value channel r of the item's block; h selects tokens
 // 32h..32h+31 for X, U and O, and key channels 64h..64h+63 for S.
 // 32 key channels (piece q of this thread's half): fp32 S and its bf16 hi/lo pairs
@@ -751,65 +745,18 @@ __device__ __forceinline__ void stage_state_piece(uint32_t lane_addr, int h, int
     tmem_st16(lane_addr + TM_SLO + 32 * h + 16 * q, lo);
 }
 
-// The same for 16 key channels (piece q4 of four), with fewer live registers.
-__device__ __forceinline__ void stage_state_piece16(uint32_t lane_addr, int h, int q4,
-                                                    const float (&x)[16]) {
-    uint32_t raw[16], hi[8], lo[8];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) raw[j] = __float_as_uint(x[j]);
-    tmem_st16(lane_addr + TM_S + 64 * h + 16 * q4, raw);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) split2_bf16(x[2 * j], x[2 * j + 1], hi[j], lo[j]);
-    tmem_st8(lane_addr + TM_SHI + 32 * h + 8 * q4, hi);
-    tmem_st8(lane_addr + TM_SLO + 32 * h + 8 * q4, lo);
-}
-
 template <bool SPLIT, int GATE>
 __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp, int lane) {
     const int quarter = warp & 3;
     const int h = rt >> 7;                 // token half / key-channel half
     const int r = 32 * quarter + lane;     // value channel within the block = TMEM lane
     const uint32_t lane_addr = cx.tmem + ((uint32_t)(32 * quarter) << 16);
-    uint32_t g = 0;    // chunks
-    uint32_t pc = 0;   // chain rounds (one per pass of a chunk)
-    uint32_t rc = 0;   // exchanges of the products of alpha
+    uint32_t g = 0;
     bool ok = true;
     const float* al = reinterpret_cast<const float*>(cx.smem + SM_ALPHA);
     const ItemRange<SPLIT> rg(p);
     float* const st_base = rg.pk ? p.P_out : p.S_T;
     const int dvs = rg.pk ? DK : p.d_v;   // rows per head of the state layout
-    // A chunk's output, packed to bf16 (16 pairs of tokens for this thread's
-    // channel), waits here until the next chunk's U is staged.  It leaves
-    // through a transpose in this warp's shared-memory slot: 32 channels x 16
-    // tokens at a time, as 16-byte pieces of token rows.
-    uint32_t opk[16];
-    bool pend = false;                // warp-uniform
-    __nv_bfloat16* pend_base = nullptr;
-    int pend_lo = 0, pend_hi = 0;     // rows of this half to store
-    const int64_t ostride = (int64_t)p.H * p.d_v;
-    uint16_t* const ost = reinterpret_cast<uint16_t*>(cx.smem + SM_OST + (warp - 6) * 1024);
-    auto flush_output = [&]() {
-        if (!pend) return;
-        pend = false;
-        const int prow = lane >> 2, pcol = (lane & 3) * 8;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                ost[(2 * j) * 32 + lane] = (uint16_t)(opk[8 * k + j] & 0xffffu);
-                ost[(2 * j + 1) * 32 + lane] = (uint16_t)(opk[8 * k + j] >> 16);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int row = prow + 8 * e;
-                const uint4 v = *reinterpret_cast<const uint4*>(ost + row * 32 + pcol);
-                if (16 * k + row >= pend_lo && 16 * k + row < pend_hi)
-                    *reinterpret_cast<uint4*>(pend_base + (int64_t)(16 * k + row) * ostride + pcol) = v;
-            }
-            __syncwarp();
-        }
-    };
     for (int item = rg.first; item < rg.count && ok; item += rg.stride) {
         const ItemInfo it = item_info<SPLIT>(p, item, rg.pk);
         const int ch = it.vb * DVB + r;   // value channel
@@ -864,6 +811,7 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             stage_state_piece(lane_addr, h, q, x);
         }
         float gtot = 1.f;   // prod alpha over the item, for g_out
+
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -875,240 +823,247 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             const bool last = c + 1 == it.nc;
             if (!(ok = warp_wait(cx, B_KQ_FULL + (g & 1), (g >> 1) & 1))) break;
             const float* bst = reinterpret_cast<const float*>(cx.smem + SM_BETA) + (g & 1) * C;
-            const float* ast = reinterpret_cast<const float*>(cx.smem + SM_ALPHA) + (g & 1) * C;
-            const uint16_t* la = reinterpret_cast<const uint16_t*>(al);
-            // alpha of token 32 h + j, 1 outside the window [lo, hi).  The tiles
-            // always hold finite values (TMA fills rows past the tensor with zeros;
-            // rows past the sequence belong to the next one), so the loads are
-            // unconditional and tokens outside the window are masked afterwards.
-            auto alpha_at = [&](int j, int lo, int hi) -> float {
-                const int t = 32 * h + j;
-                float a;
-                if (GATE == GATE_SCALAR) a = ast[t];   // one gate per token, with beta
-                else if (GATE == GATE_LOG_BF16) a = __expf(bf2f(la[t * DVB + r]));
-                else a = al[t * DVB + r];
-                return t >= lo && t < hi ? a : 1.f;
-            };
-            // Gamma over the window: the running product over this thread's half
-            // of the tokens, then the halves swap their totals (and each warp its
-            // vote: a half whose product is below the square root of the floor)
-            // through shared memory and one barrier of the 8 row warps.
-            float gam[32], gC = 1.f;
-            bool sub = false;
-            auto gamma_round = [&](int lo, int hi) -> bool {
-                float run = 1.f;
+            // Gamma (padded tokens: alpha = 1): each thread takes the running
+            // product over its half of the tokens, the halves swap their totals
+            // through shared memory; then vg = beta V / Gamma for its tokens.
+            // Transition items have alpha = 1 and v = 0.
+            float gam[32], vg[32], gC = 1.f;
+            if (rg.pk) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    run *= alpha_at(j, lo, hi);
-                    gam[j] = run;
-                }
-                float* ht = reinterpret_cast<float*>(cx.smem + SM_HALF) + (rc & 1) * 2 * DVB;
-                volatile int* votes = reinterpret_cast<volatile int*>(cx.smem + SM_VOTE) + (rc & 1) * 8;
-                ht[h * DVB + r] = run;
-                const bool fast = __any_sync(0xffffffffu, !(run >= 1e-15f));
-                if (lane == 0) votes[warp - 6] = fast ? 1 : 0;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&cx.bars[B_ROW]);
-                if (!warp_wait(cx, B_ROW, rc & 1)) return false;
-                ++rc;
-                const float other = ht[(1 - h) * DVB + r];
-                if (h == 1) {
+                for (int j = 0; j < 32; ++j) vg[j] = 0.f;
+            } else {
+                float* half_tot = reinterpret_cast<float*>(cx.smem + SM_HALF);
+                // The tiles always hold finite values (TMA fills rows past the tensor
+                // with zeros; rows past the sequence belong to the next one), so the
+                // loads are unconditional and padded tokens are masked afterwards.
+                float a[32], inv[32];
+                if (GATE == GATE_SCALAR) {
+                    // one gate per token (padded tokens: 1), from the beta stage
+                    const float* ast = reinterpret_cast<const float*>(cx.smem + SM_ALPHA) + (g & 1) * C;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float2 gg = __fmul2_rn(make_float2(gam[j], gam[j + 1]),
-                                                     make_float2(other, other));
-                        gam[j] = gg.x;
-                        gam[j + 1] = gg.y;
+                    for (int j = 0; j < 32; ++j) a[j] = ast[32 * h + j];
+                } else {
+                    if (!(ok = warp_wait(cx, B_A_FULL, g & 1))) break;
+                    if (GATE == GATE_LOG_BF16) {   // alpha = exp(log alpha)
+                        const uint16_t* la = reinterpret_cast<const uint16_t*>(al);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) a[j] = __expf(bf2f(la[(32 * h + j) * DVB + r]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) a[j] = al[(32 * h + j) * DVB + r];
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.bars[B_A_EMPTY]);   // alpha is in registers
                 }
-                gC = h == 0 ? run * other : gam[31];
-                int any = 0;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) any |= votes[w];
-                sub = any != 0;
-                return true;
-            };
-            // A chunk runs as one pass over its tokens, or, when some channel's
-            // product of alpha over it could fall below kDecayFloor, as one pass
-            // per 16 tokens (the chunk form divides by the running product).
-            int npass = 1;
-            if (!rg.pk) {
-                if (GATE != GATE_SCALAR && !(ok = warp_wait(cx, B_A_FULL, g & 1))) break;
-                if (!(ok = gamma_round(0, nvalid))) break;
-                if (sub) npass = (nvalid + 15) / 16;
-            }
-            if (rt == 0) *reinterpret_cast<volatile int*>(cx.smem + SM_MISC + 24) = npass;
-            bool vwait = !rg.pk;
-            for (int pass = 0; pass < npass; ++pass, ++pc) {
-                const int lo = sub ? 16 * pass : 0;
-                const int hi = sub ? min(16 * pass + 16, nvalid) : nvalid;
-                const bool lastp = pass + 1 == npass;
-                const bool fin = last && lastp;   // the item's final state follows
-                if (!rg.pk) {
-                    if (sub && !(ok = gamma_round(lo, hi))) break;
-                    if (!(gC >= kDecayFloor)) atomicCAS(cx.status, 0, (int32_t)KDA_ERR_DEVICE_RANGE);
-                    if (vwait && !(ok = warp_wait(cx, B_V_FULL + (g & 1), (g >> 1) & 1))) break;
-                    vwait = false;
-                }
-                gtot *= gC;
-
-                // X = beta (V / Gamma - S K^T) over the window (0 outside), split and
-                // staged as the A operand of U^T = X^T T^T.  The tokens are walked
-                // downwards so that 1 / gamma_t comes from one reciprocal and the
-                // later alphas; transition items have v = 0.
-                if (!(ok = warp_wait(cx, B_SKQ_DONE, pc & 1))) break;
-                tc_fence_after();
                 {
-                    const uint16_t* vs =
-                        reinterpret_cast<const uint16_t*>(cx.smem + ((g & 1) ? SM_V1 : SM_V));
-                    float inv = __frcp_rn(gam[31]);
+                    float run = 1.f;
 #pragma unroll
-                    for (int q2 = 1; q2 >= 0; --q2) {
-                        uint32_t sk[16];
-                        tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16 * q2, sk);
-                        tmem_ld_wait();
-                        uint32_t hi2[8], lo2[8];
+                    for (int j = 0; j < 32; ++j) {
+                        a[j] = 32 * h + j < nvalid ? a[j] : 1.f;
+                        run *= a[j];
+                        gam[j] = run;
+                    }
+                    half_tot[h * DVB + r] = run;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.bars[B_PAIR + quarter]);
+                    if (!(ok = warp_wait(cx, B_PAIR + quarter, g & 1))) break;
+                    const float other = half_tot[(1 - h) * DVB + r];
+                    if (h == 1) {
 #pragma unroll
-                        for (int j = 14; j >= 0; j -= 2) {
-                            const int t = 32 * h + 16 * q2 + j;
-                            const bool in1 = t + 1 >= lo && t + 1 < hi, in0 = t >= lo && t < hi;
-                            float v1 = 0.f, v0 = 0.f;
-                            if (!rg.pk) {
-                                v1 = bf2f(vs[(t + 1) * DVB + r]) * inv;
-                                inv *= alpha_at(16 * q2 + j + 1, lo, hi);
-                                v0 = bf2f(vs[t * DVB + r]) * inv;
-                                if (16 * q2 + j > 0) inv *= alpha_at(16 * q2 + j, lo, hi);
-                            }
-                            const float b1 = in1 && GATE != GATE_F32_ADD ? bst[t + 1] : 0.f;
-                            const float b0 = in0 && GATE != GATE_F32_ADD ? bst[t] : 0.f;
-                            // additive update: X = beta V / Gamma (no S K^T term)
-                            const float w1 = in1 ? bst[t + 1] : 0.f, w0 = in0 ? bst[t] : 0.f;
-                            const float2 vg = __fmul2_rn(make_float2(v0, v1), make_float2(w0, w1));
-                            const float2 x = __ffma2_rn(
-                                make_float2(-b0, -b1),
-                                make_float2(__uint_as_float(sk[j]), __uint_as_float(sk[j + 1])), vg);
-                            split2_bf16(x.x, x.y, hi2[j >> 1], lo2[j >> 1]);
+                        for (int j = 0; j < 32; j += 2) {
+                            const float2 gg = __fmul2_rn(make_float2(gam[j], gam[j + 1]),
+                                                         make_float2(other, other));
+                            gam[j] = gg.x;
+                            gam[j + 1] = gg.y;
                         }
-                        tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi2);
-                        tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo2);
                     }
+                    gC = h == 0 ? run * other : gam[31];
+                    // the chunk form divides by the running product: a chunk whose
+                    // product falls below kDecayFloor leaves this channel's result
+                    // to the portable kernel (both threads of a channel agree)
+                    // 1 / gamma_t from one reciprocal and the products of the later alphas
+                    inv[31] = __frcp_rn(gam[31]);
+#pragma unroll
+                    for (int j = 30; j >= 0; --j) inv[j] = inv[j + 1] * a[j + 1];
                 }
-                tmem_st_wait();
-                tc_fence_before();
+                if (!(ok = warp_wait(cx, B_V_FULL + (g & 1), (g >> 1) & 1))) break;
+                const uint16_t* vs =
+                    reinterpret_cast<const uint16_t*>(cx.smem + ((g & 1) ? SM_V1 : SM_V));
+                const float4* b4 = reinterpret_cast<const float4*>(bst + 32 * h);
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 bq = b4[j4];
+                    const int j = 4 * j4, t = 32 * h + j;
+                    float vq[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float q = bf2f(vs[(t + e) * DVB + r]) * inv[j + e];
+                        vq[e] = t + e < nvalid ? q : 0.f;
+                    }
+                    const float2 v01 = __fmul2_rn(make_float2(vq[0], vq[1]), make_float2(bq.x, bq.y));
+                    const float2 v23 = __fmul2_rn(make_float2(vq[2], vq[3]), make_float2(bq.z, bq.w));
+                    vg[j] = v01.x; vg[j + 1] = v01.y; vg[j + 2] = v23.x; vg[j + 3] = v23.y;
+                }
                 __syncwarp();
-                if (lane == 0) {
-                    if (!rg.pk && lastp) {
-                        if (GATE != GATE_SCALAR) mbar_arrive(&cx.bars[B_A_EMPTY]);   // alpha read
-                        mbar_arrive(&cx.bars[B_V_EMPTY + (g & 1)]);                  // V read
-                    }
-                    mbar_arrive(&cx.bars[B_X_READY]);
-                }
+                if (lane == 0) mbar_arrive(&cx.bars[B_V_EMPTY + (g & 1)]);   // V consumed
+            }
+            gtot *= gC;
 
-                // U^T back from TMEM (0 outside the window), split and staged as the
-                // A operand of U^T P^T and U^T K
-                if (!(ok = warp_wait(cx, B_U_DONE, pc & 1))) break;
-                tc_fence_after();
+            // X = vg - beta (S K^T), split and staged as the A operand of U^T = X^T T^T
+            if (!(ok = warp_wait(cx, B_SKQ_DONE, g & 1))) break;
+            tc_fence_after();
+            {
+                uint32_t sk[2][16];
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h, sk[0]);
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16, sk[1]);
+                tmem_ld_wait();
+                const float4* b4 = reinterpret_cast<const float4*>(bst + 32 * h);
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
-                    uint32_t u[16];
-                    tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16 * q2, u);
-                    tmem_ld_wait();
-                    uint32_t hi2[8], lo2[8];
+                    uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const int t = 32 * h + 16 * q2 + j;
-                        const float u0 = t >= lo && t < hi ? __uint_as_float(u[j]) : 0.f;
-                        const float u1 = t + 1 >= lo && t + 1 < hi ? __uint_as_float(u[j + 1]) : 0.f;
-                        split2_bf16(u0, u1, hi2[j >> 1], lo2[j >> 1]);
+                    for (int j2 = 0; j2 < 4; ++j2) {
+                        const float4 bq = GATE == GATE_F32_ADD ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                               : b4[4 * q2 + j2];
+                        const int jj = 16 * q2 + 4 * j2;
+                        const float2 x01 = __ffma2_rn(
+                            make_float2(-bq.x, -bq.y),
+                            make_float2(__uint_as_float(sk[q2][4 * j2]), __uint_as_float(sk[q2][4 * j2 + 1])),
+                            make_float2(vg[jj], vg[jj + 1]));
+                        const float2 x23 = __ffma2_rn(
+                            make_float2(-bq.z, -bq.w),
+                            make_float2(__uint_as_float(sk[q2][4 * j2 + 2]), __uint_as_float(sk[q2][4 * j2 + 3])),
+                            make_float2(vg[jj + 2], vg[jj + 3]));
+                        split2_bf16(x01.x, x01.y, hi[2 * j2], lo[2 * j2]);
+                        split2_bf16(x23.x, x23.y, hi[2 * j2 + 1], lo[2 * j2 + 1]);
                     }
-                    tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi2);
-                    tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo2);
+                    tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
+                    tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
                 }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.bars[B_X_READY]);
+
+            // U^T back from TMEM, split and staged as the A operand of U^T P^T and U^T K
+            if (!(ok = warp_wait(cx, B_U_DONE, g & 1))) break;
+            tc_fence_after();
+            {
+                uint32_t u[2][16];
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h, u[0]);
+                tmem_ld16(lane_addr + TM_SKQ + 32 * h + 16, u[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        split2_bf16(__uint_as_float(u[q2][2 * j]), __uint_as_float(u[q2][2 * j + 1]),
+                                    hi[j], lo[j]);
+                    tmem_st8(lane_addr + TM_XHI + 16 * h + 8 * q2, hi);
+                    tmem_st8(lane_addr + TM_XLO + 16 * h + 8 * q2, lo);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.bars[B_U_READY]);
+
+            // S <- gamma_C (S + U^T K), handed back to the MMA warp
+            if (!(ok = warp_wait(cx, B_S_DONE, g & 1))) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = 0; q < 2; ++q) {
+                uint32_t sv[32];
+                tmem_ld32(lane_addr + TM_S + 64 * h + 32 * q, sv);
+                tmem_ld_wait();
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    const float2 xx = __fmul2_rn(
+                        make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
+                        make_float2(gC, gC));
+                    x[j] = xx.x;
+                    x[j + 1] = xx.y;
+                }
+                if (last) {
+                    if (st_row >= 0 && gC >= kDecayFloor && !handed_back<SPLIT>(p, it, r)) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(st_base + stoff + 32 * q + j) =
+                                make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    }
+                } else {
+                    if (GATE == GATE_F32_CKPT) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(ckpt_row(c + 1) + 32 * q + j) =
+                                make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    }
+                    stage_state_piece(lane_addr, h, q, x);
+                }
+            }
+            if (!last) {
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&cx.bars[B_U_READY]);
-
-                // the previous round's output leaves now, while the S MMAs run
-                flush_output();
-
-                // S <- gamma (S + U^T K), handed back to the MMA warp
-                if (!(ok = warp_wait(cx, B_S_DONE, pc & 1))) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t sv[16];
-                    tmem_ld16(lane_addr + TM_S + 64 * h + 16 * q, sv);
-                    tmem_ld_wait();
-                    float x[16];
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float2 xx = __fmul2_rn(
-                            make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
-                            make_float2(gC, gC));
-                        x[j] = xx.x;
-                        x[j + 1] = xx.y;
-                    }
-                    if (fin) {
-                        if (st_row >= 0) {
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(st_base + stoff + 16 * q + j) =
-                                    make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-                        }
-                    } else {
-                        if (GATE == GATE_F32_CKPT && lastp) {
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(ckpt_row(c + 1) + 16 * q + j) =
-                                    make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
-                        }
-                        stage_state_piece16(lane_addr, h, q, x);
-                    }
-                }
-                if (!fin) {
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
-                }
-                if (SPLIT && fin && p.g_out && !rg.pk && h == 0)
-                    p.g_out[((size_t)it.n * p.H + it.h) * p.d_v + ch] = gtot;
-                // O = Gamma * (Q S^T + P U), read out of TMEM now (its columns take
-                // the next round's S Q^T); it is stored once the next U is staged
-                if (!(ok = warp_wait(cx, B_O_DONE, pc & 1))) break;
-                const int orow_lo = max(lo - 32 * h, 0), orow_hi = min(hi - 32 * h, 32);
-                if (rg.pk || orow_lo >= orow_hi) {   // no output of this half in this round
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
-                    continue;
-                }
-                tc_fence_after();
-                {
-                    uint32_t ov[32];
-                    tmem_ld32(lane_addr + TM_SKQ + 64 + 32 * h, ov);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float2 oo = __fmul2_rn(make_float2(gam[2 * j], gam[2 * j + 1]),
-                                                     make_float2(__uint_as_float(ov[2 * j]),
-                                                                 __uint_as_float(ov[2 * j + 1])));
-                        opk[j] = pack_bf16x2(oo.x, oo.y);
-                    }
-                }
-                tc_fence_before();
+                if (lane == 0) mbar_arrive(&cx.bars[B_S_READY]);
+            }
+            if (!(gC >= kDecayFloor)) report_fast_decay<SPLIT>(p, it, r);
+            if (SPLIT && last && p.g_out && !rg.pk && h == 0)
+                p.g_out[((size_t)it.n * p.H + it.h) * p.d_v + ch] = gtot;
+            // O = Gamma * (Q S^T + P U); leaves after the state has been handed back
+            if (!(ok = warp_wait(cx, B_O_DONE, g & 1))) break;
+            if (rg.pk) {   // transition items have no output
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
-                pend = true;
-                pend_base = p.o + (tok0 + 32 * h) * ostride + (int64_t)it.h * p.d_v +
-                            it.vb * DVB + 32 * quarter;
-                pend_lo = orow_lo;
-                pend_hi = orow_hi;
+                continue;
             }
-            if (!ok) break;
+            tc_fence_after();
+            uint32_t opk[16];
+            {
+                uint32_t ov[32];
+                tmem_ld32(lane_addr + TM_SKQ + 64 + 32 * h, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float2 oo = __fmul2_rn(make_float2(gam[2 * j], gam[2 * j + 1]),
+                                                 make_float2(__uint_as_float(ov[2 * j]),
+                                                             __uint_as_float(ov[2 * j + 1])));
+                    opk[j] = pack_bf16x2(oo.x, oo.y);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
+            // Out through a transpose in this warp's shared-memory slot: its 32
+            // channels x 16 tokens at a time leave as 16-byte pieces of token rows.
+            uint16_t* ost = reinterpret_cast<uint16_t*>(cx.smem + SM_OST + (warp - 6) * 1024);
+            const int64_t ostride = (int64_t)p.H * p.d_v;
+            __nv_bfloat16* obase = p.o + (tok0 + 32 * h) * ostride + (int64_t)it.h * p.d_v +
+                                   it.vb * DVB + 32 * quarter;
+            const int lim = nvalid - 32 * h;   // tokens of this half inside the sequence
+            const int prow = lane >> 2, pcol = (lane & 3) * 8;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    ost[(2 * j) * 32 + lane] = (uint16_t)(opk[8 * k + j] & 0xffffu);
+                    ost[(2 * j + 1) * 32 + lane] = (uint16_t)(opk[8 * k + j] >> 16);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int row = prow + 8 * e;
+                    const uint4 v = *reinterpret_cast<const uint4*>(ost + row * 32 + pcol);
+                    if (16 * k + row < lim)
+                        *reinterpret_cast<uint4*>(obase + (int64_t)(16 * k + row) * ostride + pcol) = v;
+                }
+                __syncwarp();
+            }
         }
     }
-    flush_output();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1126,14 +1081,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_tc_kernel(const __gri
     cx.never = reinterpret_cast<volatile int*>(smem + SM_MISC + 8);
     cx.slots = reinterpret_cast<volatile int*>(smem + SM_MISC + 16);
     cx.status = p.status;
-    cx.timeout_ns = p.timeout_ns;
+    cx.timeout_ns = kTimeoutNs;   // a constant here: it costs the roles no register
 
     if (tid == 0) {
         *cx.abort = 0;
         *cx.never = 0;
         // arrivals per phase: 1 for TMA / MMA commits, one per warp of a group
-        const uint32_t counts[B_COUNT] = {2, 2, 1, 1, 1, 8, 1, 4, 4, 4, 1, 1, 8, 1,
-                                          8, 1, 8, 1, 1, 8, 8, 1, 1, 1, 1, 1, 8, 8};
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 8, 1, 4, 4, 4, 1, 1, 8, 1,
+                                          8, 1, 8, 1, 1, 8, 2, 2, 2, 2, 1, 1, 8, 8};
         for (int b = 0; b < B_COUNT; ++b) mbar_init(&cx.bars[b], counts[b]);
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_q);
@@ -1282,7 +1237,7 @@ bool init_params(const PrefillArgs& a, TcParams& p) {
     p.g_out = nullptr;
     p.P_out = nullptr;
     p.ckpt = nullptr;
-    p.timeout_ns = kTimeoutNs;
+    p.redo = a.redo;
     return true;
 }
 
@@ -1345,6 +1300,7 @@ cudaError_t launch_prefill_tc_ckpt(const PrefillArgs& a, float* ckpt, cudaStream
     if (!init_params(a, p)) return cudaErrorInvalidValue;
     if (p.num_items == 0) return cudaSuccess;
     p.ckpt = ckpt;
+    p.redo = nullptr;
     const int sms = sm_count();
     const int grid = p.num_items < sms ? p.num_items : sms;
     p.a_ctas = grid;
@@ -1358,6 +1314,7 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, 
     TcParams p;
     if (!init_params(a, p)) return cudaErrorInvalidValue;
     const int M = L.M, N = a.num_seqs;
+    p.redo = nullptr;   // the segments' results feed the scan: a fast decay is reported
     cudaError_t err = launch_split_plan(a, L, ws, stream);
     if (err != cudaSuccess) return err;
     p.vt0 = reinterpret_cast<const int64_t*>(ws + L.vt0);

@@ -229,7 +229,7 @@ kda_status kda_check_wait_timeout(void* workspace, size_t workspace_bytes, uint6
  * the segment buffers): a batch with few long chains, such as one sequence
  * of 128K tokens with 32 heads, runs slower here than through kda_prefill
  * with a full workspace.  The scratch it needs lives in a device array built
- * into the library (about 256 KB on every GPU that loads it, held until the
+ * into the library (about 512 KB on every GPU that loads it, held until the
  * process exits).  Every call looks up that array's address in the CUDA
  * context current at the call (cudaGetSymbolAddress, which allocates
  * nothing), so switching driver contexts or resetting the device between
@@ -241,6 +241,10 @@ kda_status kda_check_wait_timeout(void* workspace, size_t workspace_bytes, uint6
  * clears what it needs cleared, but calls that overlap on the GPU (issued on
  * different streams with no ordering between them) race on it and must not
  * be made.  num_seqs > KDA_NOALLOC_MAX_SEQS returns KDA_ERR_UNSUPPORTED.
+ * Channels whose decay is too fast for the tensor-core kernel's one-pass
+ * chunks are redone by the portable kernel for batches of up to 16384
+ * (sequence, head, 128-channel block) units; larger batches report such
+ * channels as KDA_ERR_DEVICE_RANGE instead.
  * Device-detected input errors leave the outputs unwritten; they cannot be
  * queried afterwards, because kda_prefill_device_status needs a workspace.
  */
