@@ -222,6 +222,29 @@ kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream)
     return KDA_ERR_DEVICE_INPUT;
 }
 
+kda_status kda_segment_combine(const float* S_in, const float* g, const float* P, const float* R,
+                               int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
+                               float* S_out, kda_stream_t stream) {
+    if (num_seqs < 0 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+    if (d_k > 128) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    if (!S_in || !g || !P || !R || !S_out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {S_in, g, P, R, S_out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_INVALID_ARG;
+    const size_t ns = (size_t)num_seqs * H * d_v * d_k * sizeof(float);
+    const void* ins[] = {g, P, R};
+    const size_t in_n[] = {(size_t)num_seqs * H * d_v * sizeof(float),
+                           (size_t)num_seqs * H * d_k * d_k * sizeof(float), ns};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(S_out, ns, ins[i], in_n[i])) return KDA_ERR_INVALID_ARG;
+    if (S_out != S_in && overlaps(S_out, ns, S_in, ns)) return KDA_ERR_INVALID_ARG;
+    return kda::launch_segment_combine(S_in, g, P, R, num_seqs, H, d_k, d_v, S_out,
+                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
 kda_status kda_check_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t timeout_ns,
                                   kda_stream_t stream) {
     if (!workspace || !aligned16(workspace) || workspace_bytes < kda::WorkspaceLayout::bytes(0))

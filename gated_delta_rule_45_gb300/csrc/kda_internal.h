@@ -141,6 +141,10 @@ cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, char* 
                               cudaStream_t stream);
 cudaError_t launch_split_combine(const PrefillArgs& a, const SplitLayout& L, char* ws,
                                  cudaStream_t stream);
+// S_out = diag(g) S_in P + R per (sequence, head) (kda_segment_combine).
+cudaError_t launch_segment_combine(const float* S_in, const float* g, const float* P,
+                                   const float* R, int32_t N, int32_t H, int32_t d_k,
+                                   int32_t d_v, float* S_out, cudaStream_t stream);
 bool prefill_tc_supports(const PrefillArgs& a);
 // One CTA that runs the prefill kernel's wait-timeout path with nothing to
 // wait for (status: the workspace's status word, cleared first).

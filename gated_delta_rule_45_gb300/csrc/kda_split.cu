@@ -150,7 +150,62 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
     }
 }
 
+// S_out = diag(g) S_in P + R for every (sequence, head): one CTA per
+// (sequence, head, 32-row block); P (d_k x d_k) and the block's rows of S_in
+// in shared memory, fp32, each thread 4 rows x up to 4 columns of the product.
+// The rows of a block are read before any is written, so S_out may be S_in.
+constexpr int kCombRows = 32;
+__global__ void __launch_bounds__(256) segment_combine_kernel(
+    const float* __restrict__ S_in, const float* __restrict__ g, const float* __restrict__ P,
+    const float* __restrict__ R, int H, int d_k, int d_v, float* S_out) {
+    extern __shared__ float sh[];
+    const int ld = d_k + 1;
+    float* sP = sh;                    // [d_k][ld]
+    float* sS = sh + (size_t)d_k * ld;   // [kCombRows][ld]
+    const int nrb = (d_v + kCombRows - 1) / kCombRows;
+    const int nh = blockIdx.x / nrb, rb = blockIdx.x % nrb;
+    const int r0 = rb * kCombRows, rows = min(kCombRows, d_v - r0);
+    const size_t soff = ((size_t)nh * d_v + r0) * d_k;
+    const float* Pm = P + (size_t)nh * d_k * d_k;
+    for (int e = threadIdx.x; e < d_k * d_k; e += blockDim.x) sP[(e / d_k) * ld + e % d_k] = Pm[e];
+    for (int e = threadIdx.x; e < rows * d_k; e += blockDim.x)
+        sS[(e / d_k) * ld + e % d_k] = S_in[soff + e];
+    __syncthreads();
+    // thread (ty, tx): rows ty, ty + 8, ty + 16, ty + 24; columns tx + 32 c
+    const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
+    for (int c0 = tx; c0 < d_k; c0 += 32) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < d_k; ++k) {
+            const float pk = sP[k * ld + c0];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(sS[(ty + 8 * i) * ld + k], pk, acc[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = ty + 8 * i;
+            if (r < rows) {
+                const size_t e = soff + (size_t)r * d_k + c0;
+                S_out[e] = fmaf(g[(size_t)nh * d_v + r0 + r], acc[i], R[e]);
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_segment_combine(const float* S_in, const float* g, const float* P,
+                                   const float* R, int32_t N, int32_t H, int32_t d_k,
+                                   int32_t d_v, float* S_out, cudaStream_t stream) {
+    const int smem = (d_k + kCombRows) * (d_k + 1) * (int)sizeof(float);
+    cudaError_t err = cudaFuncSetAttribute(segment_combine_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    const int64_t blocks = (int64_t)N * H * ((d_v + kCombRows - 1) / kCombRows);
+    if (blocks == 0) return cudaSuccess;
+    segment_combine_kernel<<<(unsigned)blocks, 256, smem, stream>>>(S_in, g, P, R, H, d_k, d_v,
+                                                                    S_out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, char* ws,
                               cudaStream_t stream) {

@@ -71,6 +71,8 @@ def load(path: str | None = None):
                                         ctypes.c_int, i32, vp, vp, vp]
     lib.kda_prefill_supported.restype = ctypes.c_int
     lib.kda_prefill_supported.argtypes = [ctypes.c_int, i32, i32, i32, ctypes.c_int, i32]
+    lib.kda_segment_combine.restype = ctypes.c_int
+    lib.kda_segment_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp]
     lib.kda_check_wait_timeout.restype = ctypes.c_int
     lib.kda_check_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
     lib.kda_prefill_device_status.restype = ctypes.c_int
@@ -276,6 +278,21 @@ def prefill_noalloc_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, *, chunk:
                                     _stream_ptr(stream))
     if st != OK:
         raise KdaError(st, "kda_prefill_noalloc")
+
+
+def segment_combine(S_in, g, P, R, S_out=None, *, stream=None):
+    """Enqueue kda_segment_combine: S_out = diag(g) S_in P + R per (sequence, head);
+    S_in, R [N, H, d_v, d_k], g [N, H, d_v], P [N, H, d_k, d_k], fp32.  Returns S_out."""
+    _check_f32("segment maps", S_in, g, P, R)
+    _check_cuda(S_in, g, P, R)
+    N, H, d_v, d_k = S_in.shape
+    if S_out is None:
+        S_out = torch.empty_like(S_in)
+    st = load().kda_segment_combine(_ptr(S_in), _ptr(g), _ptr(P), _ptr(R), N, H, d_k, d_v,
+                                    _ptr(S_out), _stream_ptr(stream))
+    if st != OK:
+        raise KdaError(st, "kda_segment_combine")
+    return S_out
 
 
 def check_wait_timeout(workspace, timeout_ns: int, *, stream=None) -> None:

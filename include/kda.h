@@ -32,8 +32,9 @@
  *   kda_prefill_device_status, which says so.
  * - Errors: argument errors are returned synchronously and enqueue nothing.
  *   A failed kernel launch returns KDA_ERR_CUDA.  Errors that depend on device
- *   data (a malformed cu_seqlens) are detected on the device: the kernels then
- *   write no output, and kda_prefill_device_status reports the error.
+ *   data are detected on the device and reported by kda_prefill_device_status:
+ *   a malformed cu_seqlens (the kernels then write no output), or a decay too
+ *   fast for the chunk form (see kda_prefill).
  *   No C++ exception crosses this interface.
  * - Alias rules: outputs must not overlap inputs, except that S_T may equal
  *   S0 exactly (in-place state update).
@@ -102,12 +103,15 @@ typedef enum {
 /*
  * Bytes of device workspace kda_prefill needs for `num_seqs` sequences of H
  * heads with these sizes.  Returns 0 for num_seqs < 0.  The workspace holds
- * the varlen schedule (sequence order, work counter, device error word) and,
- * for batches with few (sequence, head, 128-channel block) chains on the
- * current device, the buffers of the sequence-axis split: at most
- * 8 x num_seqs x H x d_v x d_k x 12 bytes.  A smaller workspace of at least
- * the schedule's size is accepted and never splits.  Its contents need no
- * initialisation and are overwritten by every call.
+ * the varlen schedule (sequence order, work counter, device error word), a
+ * bitmap of the channels the tensor-core kernel hands to the portable one
+ * (16 bytes per (sequence, head, 128-channel block); see "Fast decay" at
+ * kda_prefill) and, for batches with few (sequence, head, 128-channel block)
+ * chains on the current device, the buffers of the sequence-axis split in
+ * the bitmap's place: at most 8 x num_seqs x H x d_v x d_k x 12 bytes.  A
+ * smaller workspace of at least the schedule's size is accepted; it never
+ * splits and reports fast-decaying channels instead of recomputing them.
+ * Its contents need no initialisation and are overwritten by every call.
  */
 size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
                                   int32_t chunk);
@@ -136,9 +140,21 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int3
  *                         may run concurrently
  *
  * Supported: 1 <= H, 16 <= d_k <= 128 and d_k % 16 == 0, 1 <= d_v <= 1024
- * and d_v % 16 == 0, alpha in (0, 1] with every product of alpha over one
- * chunk of one channel >= 1e-30 (the chunk form divides by it).
+ * and d_v % 16 == 0, alpha in (0, 1].
  * num_seqs == 0 or total_tokens == 0 is a valid no-op apart from S_T = S0.
+ *
+ * Fast decay.  The chunk form divides by the running product of alpha within
+ * a chunk, so it needs that product to stay above 1e-30.  The tensor-core
+ * kernel hands every channel whose product over one of its 64-token chunks
+ * falls below that to the portable kernel, which runs the channel again from
+ * S0 (its S_T is left unwritten until then, so an in-place S0 survives) and
+ * takes such chunks 16 tokens at a time.  This needs the workspace size
+ * kda_prefill_workspace_size returns; with a smaller workspace, or when the
+ * sequence axis is split, such a channel is reported instead.  A channel
+ * whose alpha multiplies to less than 1e-30 over 16 tokens (a decay of more
+ * than a factor 1e30 in 16 steps) is beyond the chunk form:
+ * kda_prefill_device_status then returns KDA_ERR_DEVICE_RANGE, and o and S_T
+ * of that sequence and head are not valid (all others are).
  */
 kda_status kda_prefill(const void* q, const void* k, const void* v,
                        const float* alpha, const float* beta, const float* S0,
@@ -187,11 +203,37 @@ kda_status kda_prefill_supported(kda_prefill_kernel kernel, int32_t H, int32_t d
 /*
  * Blocks until `stream` has finished the work enqueued so far, then returns
  * the device-side status a kda_prefill call on `workspace` recorded
- * (KDA_OK, KDA_ERR_DEVICE_INPUT or KDA_ERR_DEVICE_TIMEOUT), or KDA_ERR_CUDA
- * if the copy fails.
+ * (KDA_OK, KDA_ERR_DEVICE_INPUT, KDA_ERR_DEVICE_TIMEOUT or
+ * KDA_ERR_DEVICE_RANGE), or KDA_ERR_CUDA if the copy fails.
  * This is the only call that synchronises the host.
  */
 kda_status kda_prefill_device_status(const void* workspace, kda_stream_t stream);
+
+/*
+ * One step of the exchange that splits the sequence axis across devices (or
+ * across calls).  Over a segment of tokens the recurrence is affine in the
+ * state it starts from: S_end = diag(g) S_start P + R, with g the product of
+ * alpha over the segment (per value channel), P the product of the segment's
+ * (I - beta_t k_t k_t^T) factors in token order (d_k x d_k; the two commute
+ * with the decay, which acts on the rows) and R the state the segment
+ * reaches from zero ("Kimi (AI)", section "Kimi Delta Attention (KDA)": the
+ * forget gating and memory updating lines, composed over the segment).  This
+ * call applies such maps:
+ *
+ *     S_out[n][h] = diag(g[n][h]) S_in[n][h] P[n][h] + R[n][h]
+ *
+ *   S_in, R, S_out   [N][H][d_v][d_k] fp32; S_out may equal S_in
+ *   g                [N][H][d_v] fp32
+ *   P                [N][H][d_k][d_k] fp32
+ *
+ * kda_prefill itself gives each part of a segment's map: R is its S_T from
+ * S0 = NULL; P is its S_T with v = 0, alpha = 1 and S0 = the identity (d_v =
+ * d_k); g is any column of its S_T with k = 0 and S0 = all ones.  Supported:
+ * d_k <= 128; arithmetic in fp32.
+ */
+kda_status kda_segment_combine(const float* S_in, const float* g, const float* P, const float* R,
+                               int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
+                               float* S_out, kda_stream_t stream);
 
 /*
  * Runs the device-side timeout path of the prefill kernels, so that a user can
@@ -318,7 +360,10 @@ size_t kda_backward_workspace_size(int32_t num_seqs, int64_t total_tokens, int32
  * every output unwritten.  The result is deterministic (no atomics).
  *
  * Supported: dtype KDA_BF16, d_k == 128, d_v a multiple of 64 up to 1024,
- * chunk == 64; alpha as for kda_prefill.  Arithmetic is fp32.
+ * chunk == 64; alpha in (0, 1] with every product of alpha over one 64-token
+ * chunk of one channel >= 1e-30 (the chunkwise reverse mode divides by it and
+ * has no 16-token fallback; for d_v a multiple of 128 a chunk below it is
+ * reported as KDA_ERR_DEVICE_RANGE).  Arithmetic is fp32.
  */
 kda_status kda_backward(const void* q, const void* k, const void* v, const float* alpha,
                         const float* beta, const float* S0, const int32_t* cu_seqlens,
