@@ -249,8 +249,8 @@ def time_oracle_sample(d, steps, pairs_wanted: int, budget_s: float, seed: int =
     chosen = []
     token_heads = 0
     # pick pairs until about the budget's worth of work (≈ 8 d_k d_v flop per token-head,
-    # ~2 Gflop/s per core fp64 for this loop nest)
-    per_core_rate = 2.0e9
+    # ~3.5 Gflop/s per core fp64 for this loop nest)
+    per_core_rate = 3.5e9
     target = budget_s * per_core_rate * cores / (8.0 * spec.d_k * spec.d_v)
     for idx in order[:pairs_wanted]:
         n, h = divmod(int(idx), spec.H)
@@ -512,7 +512,10 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16 in/out; bf16 hi/lo MMA + fp32 accumulate; fp32 state",
+            "dtype": "bf16",
+            "precision": "bf16 inputs and output; tensor-core products on bf16 operands "
+                         "(non-input operands as hi + lo bf16 pairs) with fp32 accumulation; "
+                         "fp32 state and CUDA-core arithmetic",
             "data": "synthetic (seeded: torch.Generator seed 0 + rank)",
             "config": {"workload": "varlen: 64 seqs, lengths U[128,8192], H=16, d_k=128, "
                                    "d_v=256, chunk=64, S0~N(0,0.1^2), then 32 decode steps",
@@ -542,11 +545,13 @@ def run_ours(args):
             "e2e": e2e,
         }
         if not args.no_cpu_baseline:
-            v, cores, desc, _ = time_oracle_sample(d, steps, pairs_wanted=64,
-                                                   budget_s=args.ref_budget)
+            every = spec.num_seqs * spec.H
+            v, cores, desc, _ = time_oracle_sample(d, steps, pairs_wanted=every,
+                                                   budget_s=args.cpu_baseline_budget)
             # the same oracle on one thread, over a quarter of the budget
-            v1, _, desc1, _ = time_oracle_sample(d, steps, pairs_wanted=64,
-                                                 budget_s=args.ref_budget / 4, seed=1, threads=1)
+            v1, _, desc1, _ = time_oracle_sample(d, steps, pairs_wanted=every,
+                                                 budget_s=args.cpu_baseline_budget / 4, seed=1,
+                                                 threads=1)
             line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                     "sample": desc,
                                     "single_core": {"value": v1, "unit": UNIT, "cores": 1,
@@ -961,6 +966,9 @@ def main(argv=None):
     p.add_argument("--ref-budget", type=float, default=None,
                    help="seconds of CPU work per reference step / cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-baseline-budget", type=float, default=12.0,
+                   help="seconds of CPU work for the cpu_baseline sample on every core "
+                        "(a quarter of it again on one thread)")
     p.add_argument("--no-components", action="store_true",
                    help="skip timing the other workloads' kernels alone after the step")
     p.add_argument("--workload",
