@@ -127,9 +127,8 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     if (use_tc && split.M < 3 && redo_n > 0 && workspace_bytes >= redo_at + redo_n && d_v % 128 == 0)
         a.redo = reinterpret_cast<uint32_t*>(ws + redo_at);
 
-    if (kda::launch_planner(a, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_planner(a, stream, redo_n) != cudaSuccess) return KDA_ERR_CUDA;
     if (num_seqs == 0) return KDA_OK;
-    if (a.redo && cudaMemsetAsync(a.redo, 0, redo_n, stream) != cudaSuccess) return KDA_ERR_CUDA;
     cudaError_t err;
     if (use_tc && split.M >= 3) {
         err = kda::launch_prefill_tc_split(a, split, ws, stream);

@@ -123,7 +123,7 @@ struct BackwardArgs {
 };
 
 // Launchers; each returns the CUDA error of its launch.
-cudaError_t launch_planner(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_planner(const PrefillArgs& a, cudaStream_t stream, size_t redo_bytes = 0);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 // The portable kernel over the channels the tensor-core kernel handed back in
