@@ -419,7 +419,7 @@ def run_ours(args):
     o = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev)
     S = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
     o_dec = [torch.empty((N, H, d_v), dtype=torch.bfloat16, device=dev) for _ in range(n_dec)]
-    wsp = torch.empty(kda.workspace_size(N, H, d_k, d_v, spec.chunk), dtype=torch.uint8,
+    wsp = torch.empty(kda.workspace_size(N, H, d_k, d_v, spec.chunk, T), dtype=torch.uint8,
                       device=dev)
     torch.cuda.synchronize()
 
@@ -592,7 +592,8 @@ def run_e2e(args, kda, d, steps, spec, dev, stream):
     o = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev)
     S = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
     o_dec = torch.empty((len(steps), N, H, d_v), dtype=torch.bfloat16, device=dev)
-    wsp = torch.empty(kda.workspace_size(N), dtype=torch.uint8, device=dev)
+    wsp = torch.empty(kda.workspace_size(N, H, d_k, d_v, spec.chunk, T), dtype=torch.uint8,
+                      device=dev)
     o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     S_h = torch.empty(S.shape, dtype=S.dtype).pin_memory()
     od_h = torch.empty(o_dec.shape, dtype=o_dec.dtype).pin_memory()
@@ -688,8 +689,8 @@ def prefill_case(name, kda, dev, stream, gen_device="cpu"):
     T = int(g["cu_seqlens"][-1])
     o = torch.empty((T, spec.H, spec.d_v), dtype=torch.bfloat16, device=dev)
     S = torch.empty((spec.num_seqs, spec.H, spec.d_v, spec.d_k), device=dev)
-    wsp = torch.empty(kda.workspace_size(spec.num_seqs, spec.H, spec.d_k, spec.d_v, spec.chunk),
-                      dtype=torch.uint8, device=dev)
+    wsp = torch.empty(kda.workspace_size(spec.num_seqs, spec.H, spec.d_k, spec.d_v, spec.chunk,
+                                         T), dtype=torch.uint8, device=dev)
     alpha_bytes = None
     if additive:   # the additive update of linear attention on the same inputs
         def launch():

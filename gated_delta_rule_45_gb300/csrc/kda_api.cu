@@ -110,10 +110,10 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
         !additive) {
         const int M = kda::split_segments(num_seqs, H, d_k, d_v, chunk);
         const bool forced = kernel == KDA_KERNEL_CHUNK_TC_SPLIT;
-        if (forced && M < 3) return KDA_ERR_UNSUPPORTED;
+        if (forced && M < 2) return KDA_ERR_UNSUPPORTED;
         const bool long_enough = total_tokens >= (int64_t)num_seqs * M * 2048;
-        if (M >= 3 && (long_enough || forced)) {
-            split = kda::split_layout(num_seqs, H, d_k, d_v, M);
+        if (M >= 2 && (long_enough || forced)) {
+            split = kda::split_layout(num_seqs, total_tokens, H, d_k, d_v, M);
             if (workspace_bytes < split.end) {
                 if (forced) return KDA_ERR_INVALID_ARG;
                 split.M = 1;
@@ -124,13 +124,13 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const void*
     // room for the channels the tensor-core kernel may hand back to the portable one
     const size_t redo_at = kda::WorkspaceLayout::bytes(num_seqs);
     const size_t redo_n = kda::WorkspaceLayout::redo_bytes(num_seqs, H, d_v);
-    if (use_tc && split.M < 3 && redo_n > 0 && workspace_bytes >= redo_at + redo_n && d_v % 128 == 0)
+    if (use_tc && split.M < 2 && redo_n > 0 && workspace_bytes >= redo_at + redo_n && d_v % 128 == 0)
         a.redo = reinterpret_cast<uint32_t*>(ws + redo_at);
 
     if (kda::launch_planner(a, stream, redo_n) != cudaSuccess) return KDA_ERR_CUDA;
     if (num_seqs == 0) return KDA_OK;
     cudaError_t err;
-    if (use_tc && split.M >= 3) {
+    if (use_tc && split.M >= 2) {
         err = kda::launch_prefill_tc_split(a, split, ws, stream);
     } else if (use_tc) {
         err = kda::launch_prefill_tc(a, stream);
@@ -148,16 +148,24 @@ extern "C" {
 
 size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
                                   int32_t chunk) {
+    (void)chunk;
     if (num_seqs < 0) return 0;
     const size_t base = kda::WorkspaceLayout::bytes(num_seqs);
     if (H < 1 || d_k < 1 || d_v < 1) return base;
-    // the channels handed back by the tensor-core kernel, in the place the
-    // split's buffers take when it splits
-    const size_t with_redo = base + kda::WorkspaceLayout::redo_bytes(num_seqs, H, d_v);
+    // the channels handed back by the tensor-core kernel
+    return base + kda::WorkspaceLayout::redo_bytes(num_seqs, H, d_v);
+}
+
+size_t kda_prefill_workspace_size_tokens(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                         int32_t d_k, int32_t d_v, int32_t chunk) {
+    if (num_seqs < 0 || total_tokens < 0) return 0;
+    const size_t plain = kda_prefill_workspace_size(num_seqs, H, d_k, d_v, chunk);
+    if (H < 1 || d_k < 1 || d_v < 1) return plain;
+    // the sequence-axis split's buffers, in the bitmap's place, when it splits
     const int M = kda::split_segments(num_seqs, H, d_k, d_v, chunk);
-    if (M < 3) return with_redo;
-    const size_t split = kda::split_layout(num_seqs, H, d_k, d_v, M).end;
-    return split > with_redo ? split : with_redo;
+    if (M < 2) return plain;
+    const size_t split = kda::split_layout(num_seqs, total_tokens, H, d_k, d_v, M).end;
+    return split > plain ? split : plain;
 }
 
 kda_status kda_prefill(const void* q, const void* k, const void* v, const float* alpha,

@@ -14,6 +14,9 @@ namespace kda {
 // range's end.  A chunk below it on some channel is taken again in passes of
 // 16 tokens; a pass of 16 below it is reported as KDA_ERR_DEVICE_RANGE.
 constexpr float kDecayFloor = 1e-30f;
+// Sequence-axis split: a later segment's zero-start output is kept in fp32
+// for the chunks whose decay from the segment start is at least this.
+constexpr float kOresFloor = 0x1p-10f;
 
 // Layout of the prefill workspace (all offsets in bytes from its start).
 //   [0, 4)    int32 device status (0 = ok, or a KDA_ERR_DEVICE_* code)
@@ -42,20 +45,36 @@ struct WorkspaceLayout {
 // Sequence-axis split of the tensor-core prefill (few long chains): each
 // sequence is cut into M segments of whole chunks.  Virtual sequence
 // v = j * N + n is segment j of sequence n.  Buffers appended to the workspace:
-//   vt0   int64 [M N]           first token of each segment
-//   vlen  int32 [M N]           its length
-//   sfin  fp32 [(M-1) N][H][d_v][d_k]   final state of segments 0..M-2
-//             (segment 0 from the true S0, the others from zero)
-//   pbuf  fp32 [(M-2) N][H][d_k][d_k]   transition P of segments 1..M-2
-//   gbuf  fp32 [(M-1) N][H][d_v]        prod alpha over segments 0..M-2
-//   sst   fp32 [(M-1) N][H][d_v][d_k]   true initial state of segments 1..M-1
+//   vt0    int64 [M N]                  first token of each segment
+//   vlen   int32 [M N]                  its length
+//   sfin   fp32 [M N][H][d_v][d_k]      final state of each segment (segment 0
+//                                       from the true S0, the others from zero)
+//   pbuf   fp32 [(M-1) N][H][d_k][d_k]  transition P of segments 1..M-1
+//   gbuf   fp32 [M N][H][d_v]           prod alpha over each segment
+//   sst    fp32 [(M-1) N][H][d_v][d_k]  true initial state of segments 1..M-1
+//   rnorm  fp32 [(M-1) N][H][d_v]       norms of the rows of sst
+//   gstart fp32 [T / 64 + N + 1][H][d_v] per chunk of segments 1..M-1: prod
+//                                       alpha from the segment start to the
+//                                       chunk start (slot cu[n] / 64 + n + c)
+//   qtil   fp32 [T][H][d_k]             P_{<=t} q_t for the tokens of
+//                                       segments 1..M-1 (P_{<=t}: the product
+//                                       of (I - beta k k^T) from the segment
+//                                       start through token t)
+//   ores   fp32 [T][H][d_v]             o of segments 1..M-1 from a zero start,
+//                                       for the chunks (and channels) whose
+//                                       gstart is at least kOresFloor
+//   clist  int32 count (16 bytes), then int32 [slots H d_v/128][4]: the
+//          (chunk slot, head x 128-channel block, sequence, segment) of the
+//          chunks whose output the initial state can still change
 struct SplitLayout {
     int M = 1;
-    size_t vt0 = 0, vlen = 0, sfin = 0, pbuf = 0, gbuf = 0, sst = 0, end = 0;
+    size_t vt0 = 0, vlen = 0, sfin = 0, pbuf = 0, gbuf = 0, sst = 0, rnorm = 0, gstart = 0,
+           qtil = 0, ores = 0, clist = 0, end = 0;
 };
 // Segments for this shape on the current device (1: no split).
 int split_segments(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int32_t chunk);
-SplitLayout split_layout(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int M);
+SplitLayout split_layout(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                         int32_t d_v, int M);
 
 struct PrefillArgs {
     const void* q;
@@ -140,6 +159,9 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, 
 cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, char* ws,
                               cudaStream_t stream);
 cudaError_t launch_split_combine(const PrefillArgs& a, const SplitLayout& L, char* ws,
+                                 cudaStream_t stream);
+// o of segments 1..M-1 += diag(decay from the segment start) S_start P_{<=t} q_t.
+cudaError_t launch_split_correct(const PrefillArgs& a, const SplitLayout& L, char* ws,
                                  cudaStream_t stream);
 // S_out = diag(g) S_in P + R per (sequence, head) (kda_segment_combine).
 cudaError_t launch_segment_combine(const float* S_in, const float* g, const float* P,

@@ -135,6 +135,19 @@ struct TcParams {
     // channels whose chunks decayed too fast for the one-pass chunk form, one
     // bit per channel of [N][H][d_v / 128] blocks (null: reported instead)
     uint32_t* redo;
+    // Split launches: plain items of virtual sequences v >= gstart_lo write,
+    // for each chunk, prod alpha from the segment's start to the chunk's start
+    // per channel, to gstart [slot][H][d_v] with slot = cu[n] / C + n + (the
+    // chunk's index within sequence n = v % gstart_lo); transition items write
+    // their outputs P_{<=t} q_t in fp32 to qtil [T][H][DK] (null: none).
+    // Plain items of v >= gstart_lo also keep their o in fp32 in ores
+    // [T][H][d_v] for the chunks whose decay from the segment start is at
+    // least kOresFloor, for the correction that adds the initial state's
+    // share (elsewhere that share is small beside the bf16 rounding).
+    float* gstart;
+    float* qtil;
+    float* ores;
+    int32_t gstart_lo;
     const float* alpha_s;   // GATE_SCALAR: alpha [T][H]
     // GATE_F32_CKPT: fp32 [slots][H][d_v][DK]; chunk c of sequence n starting
     // at token t0 in slot t0 / C + n + c
@@ -716,6 +729,30 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
 // No register carries this across the chunk loop: the bit is set after the
 // chunk's state is handed back, and read back (a global load of the bit this
 // same thread set) before the item's final state is written.
+// Split outputs, out of line so that the chunk loop's code stays small:
+// 32 token rows of one channel in fp32, from TMEM (the transition items'
+// P_{<=t} q_t) or from registers (a later segment's o from a zero start).
+__device__ __noinline__ void store_tmem_column_f32(uint32_t taddr, float* dst, int64_t stride,
+                                                   int lim) {
+#pragma unroll 1
+    for (int q2 = 0; q2 < 2; ++q2) {
+        uint32_t v[16];
+        tmem_ld16(taddr + 16 * q2, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (16 * q2 + j < lim) dst[(16 * q2 + j) * stride] = __uint_as_float(v[j]);
+    }
+}
+struct Column32 {
+    uint32_t v[32];
+};
+__device__ __noinline__ void store_column_f32(Column32 x, float* dst, int64_t stride, int lim) {
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j)
+        if (j < lim) dst[j * stride] = __uint_as_float(x.v[j]);
+}
+
 template <bool SPLIT>
 __device__ __noinline__ void report_fast_decay(const TcParams& p, const ItemInfo& it, int r) {
     if (!SPLIT && p.redo)
@@ -811,6 +848,14 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
             stage_state_piece(lane_addr, h, q, x);
         }
         float gtot = 1.f;   // prod alpha over the item, for g_out
+        // where this item's per-chunk decay from the segment start goes (split only)
+        float* gs_row = nullptr;
+        if (SPLIT && p.gstart && !rg.pk && h == 0 && it.n >= p.gstart_lo) {
+            const int n0 = it.n % p.gstart_lo;
+            const int64_t c0 = p.cu[n0];
+            const int64_t slot = c0 / C + n0 + (it.t0 - c0) / C;
+            gs_row = p.gstart + ((size_t)slot * p.H + it.h) * p.d_v + ch;
+        }
 
         tmem_st_wait();
         tc_fence_before();
@@ -907,6 +952,8 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&cx.bars[B_V_EMPTY + (g & 1)]);   // V consumed
             }
+            if (SPLIT && gs_row) gs_row[(size_t)c * p.H * p.d_v] = gtot;
+            const bool keep_fp32 = SPLIT && gtot >= kOresFloor;   // see TcParams::ores
             gtot *= gC;
 
             // X = vg - beta (S K^T), split and staged as the A operand of U^T = X^T T^T
@@ -1015,9 +1062,20 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                 p.g_out[((size_t)it.n * p.H + it.h) * p.d_v + ch] = gtot;
             // O = Gamma * (Q S^T + P U); leaves after the state has been handed back
             if (!(ok = warp_wait(cx, B_O_DONE, g & 1))) break;
-            if (rg.pk) {   // transition items have no output
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
+            if (rg.pk) {   // transition items: o_t = P_{<=t} q_t, kept in fp32 if asked
+                if (SPLIT && p.qtil) {
+                    tc_fence_after();
+                    const int64_t qstride = (int64_t)p.H * DK;
+                    store_tmem_column_f32(lane_addr + TM_SKQ + 64 + 32 * h,
+                                          p.qtil + (tok0 + 32 * h) * qstride + (int64_t)it.h * DK + ch,
+                                          qstride, nvalid - 32 * h);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
+                } else {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
+                }
                 continue;
             }
             tc_fence_after();
@@ -1031,7 +1089,19 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                     const float2 oo = __fmul2_rn(make_float2(gam[2 * j], gam[2 * j + 1]),
                                                  make_float2(__uint_as_float(ov[2 * j]),
                                                              __uint_as_float(ov[2 * j + 1])));
+                    if (SPLIT) {   // a later segment's o, kept in fp32 (ov no longer needed)
+                        ov[2 * j] = __float_as_uint(oo.x);
+                        ov[2 * j + 1] = __float_as_uint(oo.y);
+                    }
                     opk[j] = pack_bf16x2(oo.x, oo.y);
+                }
+                if (SPLIT && keep_fp32 && p.ores && it.n >= p.gstart_lo) {
+                    const int64_t rs = (int64_t)p.H * p.d_v;
+                    Column32 col;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) col.v[j] = ov[j];
+                    store_column_f32(col, p.ores + (tok0 + 32 * h) * rs + (int64_t)it.h * p.d_v + ch,
+                                     rs, nvalid - 32 * h);
                 }
             }
             tc_fence_before();
@@ -1238,6 +1308,10 @@ bool init_params(const PrefillArgs& a, TcParams& p) {
     p.P_out = nullptr;
     p.ckpt = nullptr;
     p.redo = a.redo;
+    p.gstart = nullptr;
+    p.qtil = nullptr;
+    p.ores = nullptr;
+    p.gstart_lo = 0;
     return true;
 }
 
@@ -1309,7 +1383,7 @@ cudaError_t launch_prefill_tc_ckpt(const PrefillArgs& a, float* ckpt, cudaStream
 
 cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, char* ws,
                                     cudaStream_t stream) {
-    if (!prefill_tc_supports(a) || L.M < 3 || a.gate != GATE_F32) return cudaErrorInvalidValue;
+    if (!prefill_tc_supports(a) || L.M < 2 || a.gate != GATE_F32) return cudaErrorInvalidValue;
     if (a.total_tokens == 0 || a.num_seqs == 0) return launch_prefill_tc(a, stream);
     TcParams p;
     if (!init_params(a, p)) return cudaErrorInvalidValue;
@@ -1320,47 +1394,45 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, 
     p.vt0 = reinterpret_cast<const int64_t*>(ws + L.vt0);
     p.vlen = reinterpret_cast<const int32_t*>(ws + L.vlen);
     const int sms = sm_count();
-    // pass 1: segment 0 from S0 and segments 1..M-2 from zero (final states
-    // and prod alpha kept), and the transitions P of segments 1..M-2
-    TcParams p1 = p;
-    p1.num_items = (M - 1) * N * a.H * p.nvb;
-    p1.S_T = reinterpret_cast<float*>(ws + L.sfin);
-    p1.st_hi = (M - 1) * N;
-    p1.g_out = reinterpret_cast<float*>(ws + L.gbuf);
-    p1.n_base_p = N;
-    p1.num_items_p = (M - 2) * N * a.H;
-    p1.P_out = reinterpret_cast<float*>(ws + L.pbuf);
+    // One pass over every segment: segment 0 from S0 (its o is final),
+    // segments 1..M-1 from zero (o from a zero start, final state R, prod
+    // alpha, and the decay from the segment start at each chunk), and the
+    // transitions P of segments 1..M-1 with their outputs P_{<=t} q_t.
+    p.num_items = M * N * a.H * p.nvb;
+    p.S_T = reinterpret_cast<float*>(ws + L.sfin);
+    p.s0_lo = 0;
+    p.s0_hi = N;
+    p.st_lo = 0;
+    p.st_hi = M * N;
+    p.g_out = reinterpret_cast<float*>(ws + L.gbuf);
+    p.gstart = reinterpret_cast<float*>(ws + L.gstart);
+    p.gstart_lo = N;
+    p.n_base_p = N;
+    p.num_items_p = (M - 1) * N * a.H;
+    p.P_out = reinterpret_cast<float*>(ws + L.pbuf);
+    p.qtil = reinterpret_cast<float*>(ws + L.qtil);
+    p.ores = reinterpret_cast<float*>(ws + L.ores);
     // one CTA per item when they all fit; otherwise the SMs are divided in
     // proportion to the two kinds of items, so that both take the same number
     // of waves
     int a_ctas, p_ctas;
-    const int64_t all = (int64_t)p1.num_items + p1.num_items_p;
+    const int64_t all = (int64_t)p.num_items + p.num_items_p;
     if (all <= sms) {
-        a_ctas = p1.num_items;
-        p_ctas = p1.num_items_p;
+        a_ctas = p.num_items;
+        p_ctas = p.num_items_p;
     } else {
-        a_ctas = (int)(((int64_t)sms * p1.num_items + all / 2) / all);
+        a_ctas = (int)(((int64_t)sms * p.num_items + all / 2) / all);
         if (a_ctas < 1) a_ctas = 1;
         if (a_ctas > sms - 1) a_ctas = sms - 1;
         p_ctas = sms - a_ctas;
     }
-    p1.a_ctas = a_ctas;
-    if ((err = launch<true>(p1, a_ctas + p_ctas, stream)) != cudaSuccess) return err;
+    p.a_ctas = a_ctas;
+    if ((err = launch<true>(p, a_ctas + p_ctas, stream)) != cudaSuccess) return err;
     // the scan of the segment maps: true initial states of segments 1..M-1
+    // (and their row norms), the last map's image is S_T
     if ((err = launch_split_combine(a, L, ws, stream)) != cudaSuccess) return err;
-    // pass 2: segments 1..M-1 from their true initial states; the last one
-    // writes S_T
-    TcParams p2 = p;
-    p2.n_base = N;
-    p2.num_items = (M - 1) * N * a.H * p.nvb;
-    p2.S0 = reinterpret_cast<const float*>(ws + L.sst);
-    p2.s0_lo = N;
-    p2.s0_hi = M * N;
-    p2.st_lo = (M - 1) * N;
-    p2.st_hi = M * N;
-    const int grid2 = p2.num_items < sms ? p2.num_items : sms;
-    p2.a_ctas = grid2;
-    return launch<true>(p2, grid2, stream);
+    // each later segment's output gets its initial state's share
+    return launch_split_correct(a, L, ws, stream);
 }
 
 }  // namespace kda

@@ -8,29 +8,40 @@
 // rows and the projector on the columns):
 //   S_end = diag(g) S_start P + R,
 // g = prod alpha (per value channel), P = prod (I - beta k k^T) (d_k x d_k),
-// R = the state reached from S_start = 0.  The first pass runs segment 0 from
-// the true S0 and, for segments 1..M-2, R (from zero) and P (alpha = 1, v = 0,
-// S_start = I); this scan then chains the maps; the second pass reruns
-// segments 1..M-1 from their true initial states.
+// R = the state reached from S_start = 0.  The same holds for every token t
+// of the segment: the output is affine in S_start,
+//   o_t = o_t(from zero) + G_t * (S_start P_{<=t} q_t),
+// with G_t = prod alpha from the segment start through t (per channel) and
+// P_{<=t} the product of the segment's (I - beta k k^T) through t.
+//
+// One pass of the chunk kernel runs segment 0 from the true S0 (its o is
+// final) and, for segments 1..M-1, the segment from zero (o from zero, R,
+// g, G at each chunk start) and the transition from S_start = I with
+// alpha = 1 and v = 0 (P, and its outputs P_{<=t} q_t).  The scan below
+// chains the maps into each segment's true initial state and S_T; the
+// correction kernels then add each segment's G_t * S_start P_{<=t} q_t to o,
+// only where it can change the stored value.
 #include "kda_internal.h"
+
+#include <cfloat>
 
 namespace kda {
 
 int split_segments(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int32_t chunk) {
     if (num_seqs <= 0 || H <= 0 || d_k != 128 || d_v % 128 != 0 || chunk != 64) return 1;
     const int64_t chains = (int64_t)num_seqs * H * (d_v / 128);
+    const int64_t trans = (int64_t)num_seqs * H;
     const int64_t sms = sm_count();
-    if (sms <= 0 || 2 * chains + (int64_t)num_seqs * H > sms) return 1;
-    // a pass takes (waves of its items) x (chunks per segment) chunk times: the
-    // first pass has (M-1) items per chain plus (M-2) transition items per
-    // (sequence, head), the second (M-1) per chain; pick the M in [3, 8] with
-    // the fewest waves per segment of the sequence (ties: the smaller M)
+    if (sms <= 0 || 2 * chains + trans > sms) return 1;
+    // the pass has M items per chain and M - 1 transition items per (sequence,
+    // head); it takes (waves of its items) x (chunks per segment) chunk
+    // times: pick the M in [2, 16] with the fewest waves per segment of the
+    // sequence (ties: the smaller M)
     int M = 1;
     double best = 0.0;
-    for (int m = 3; m <= 8; ++m) {
-        const int64_t p1 = (m - 1) * chains + (int64_t)(m - 2) * num_seqs * H;
-        const int64_t p2 = (m - 1) * chains;
-        const double cost = (double)((p1 + sms - 1) / sms + (p2 + sms - 1) / sms) / m;
+    for (int m = 2; m <= 16; ++m) {
+        const int64_t items = m * chains + (m - 1) * trans;
+        const double cost = (double)((items + sms - 1) / sms) / m;
         if (M == 1 || cost < best - 1e-9) {
             M = m;
             best = cost;
@@ -39,7 +50,8 @@ int split_segments(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int32_
     return M;
 }
 
-SplitLayout split_layout(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int M) {
+SplitLayout split_layout(int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                         int32_t d_v, int M) {
     SplitLayout L;
     L.M = M;
     if (M <= 1 || num_seqs <= 0) return L;
@@ -50,12 +62,20 @@ SplitLayout split_layout(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, 
         return at;
     };
     const size_t N = (size_t)num_seqs, st = (size_t)H * d_v * d_k * sizeof(float);
+    const size_t T = total_tokens > 0 ? (size_t)total_tokens : 0;
+    const size_t slots = T / 64 + N + 1;
     L.vt0 = take(sizeof(int64_t) * M * N);
     L.vlen = take(sizeof(int32_t) * M * N);
-    L.sfin = take((M - 1) * N * st);
-    L.pbuf = take((M - 2) * N * (size_t)H * d_k * d_k * sizeof(float));
-    L.gbuf = take((M - 1) * N * (size_t)H * d_v * sizeof(float));
+    L.sfin = take(M * N * st);
+    L.pbuf = take((M - 1) * N * (size_t)H * d_k * d_k * sizeof(float));
+    L.gbuf = take(M * N * (size_t)H * d_v * sizeof(float));
     L.sst = take((M - 1) * N * st);
+    L.rnorm = take((M - 1) * N * (size_t)H * d_v * sizeof(float));
+    L.gstart = take(slots * (size_t)H * d_v * sizeof(float));
+    L.qtil = take(T * (size_t)H * d_k * sizeof(float));
+    L.ores = take(T * (size_t)H * d_v * sizeof(float));
+    // the correction's work list: a count, then (slot, head-block) pairs
+    L.clist = take(16 + sizeof(int32_t) * 4 * slots * (size_t)H * (d_v / 128));
     L.end = off;
     return L;
 }
@@ -65,7 +85,9 @@ namespace {
 // Segment j of sequence n = whole chunks [j nc / M, (j + 1) nc / M) of its nc.
 __global__ void split_plan_kernel(const int32_t* __restrict__ cu, int N, int M,
                                   int64_t* __restrict__ vt0, int32_t* __restrict__ vlen,
+                                  int32_t* __restrict__ ccount,
                                   const int32_t* __restrict__ status) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ccount = 0;   // the correction list
     if (*status == KDA_ERR_DEVICE_INPUT) return;
     for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
         const int64_t t0 = cu[n];
@@ -84,11 +106,13 @@ constexpr int kB = 128;        // rows and columns of a state block
 constexpr int kLd = kB + 4;    // padded row stride in shared memory
 
 // One CTA per (sequence, head, 128-row block): S_1 = S_fin(0);
-// S_{j+1} = diag(g_j) S_j P_j + R_j for j = 1..M-2, R_j = S_fin(j).  fp32,
-// S and P in shared memory, each thread an 8 x 8 tile of the product.
+// S_{j+1} = diag(g_j) S_j P_j + R_j for j = 1..M-1, R_j = S_fin(j); S_M is the
+// sequence's S_T.  fp32, S and P in shared memory, each thread an 8 x 8 tile
+// of the product.  S_1..S_{M-1} go to sst with the norms of their rows.
 __global__ void __launch_bounds__(256) split_combine_kernel(
     int N, int H, int d_v, int M, const float* __restrict__ sfin, const float* __restrict__ pbuf,
-    const float* __restrict__ gbuf, float* __restrict__ sst, const int32_t* __restrict__ status) {
+    const float* __restrict__ gbuf, float* __restrict__ sst, float* __restrict__ rnorm,
+    float* __restrict__ S_T, const int32_t* __restrict__ status) {
     if (*status == KDA_ERR_DEVICE_INPUT) return;
     extern __shared__ float sh[];
     float* sS = sh;              // [128][kLd]
@@ -109,7 +133,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
             d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
         }
     }
-    for (int j = 1; j <= M - 2; ++j) {
+    for (int j = 1; j <= M - 1; ++j) {
         const size_t v = (size_t)j * N + n;
         const float* P = pbuf + (((v - N) * H + h) * (size_t)kB) * kB;
         for (int e = tid * 4; e < kB * kB; e += 256 * 4) {
@@ -118,6 +142,11 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
             d[0] = x.x; d[1] = x.y; d[2] = x.z; d[3] = x.w;
         }
         __syncthreads();
+        if (tid < kB) {   // norms of the rows of S_j, the initial state of segment j
+            float acc = 0.f;
+            for (int k = 0; k < kB; ++k) acc = fmaf(sS[tid * kLd + k], sS[tid * kLd + k], acc);
+            rnorm[((v - N) * H + h) * (size_t)d_v + (size_t)vb * kB + tid] = sqrtf(acc);
+        }
         float acc[8][8] = {};
         for (int k = 0; k < kB; ++k) {
             float a[8], b[8];
@@ -133,7 +162,8 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
         __syncthreads();   // every thread is done reading S_j
         const float* R = sfin + state(v);
         const float* gv = gbuf + (v * H + h) * (size_t)d_v + (size_t)vb * kB;
-        float* dst = sst + state(v);   // S_{j+1}: row (j + 1) N + n - N of sst
+        // S_{j+1}: row j N + n of sst, or S_T after the last segment
+        float* dst = j < M - 1 ? sst + state(v) : S_T + state((size_t)n);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = 8 * ty + i;
@@ -147,6 +177,178 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
             }
         }
         __syncthreads();
+    }
+}
+
+// Chunk slot s (as laid out in SplitLayout::gstart) -> sequence n, chunk c
+// within it and its segment j; false if s holds no chunk of a segment j >= 1.
+__device__ bool slot_chunk(const int32_t* __restrict__ cu, int N, int M,
+                           const int64_t* __restrict__ vt0, const int32_t* __restrict__ vlen,
+                           int64_t s, int& n, int& c, int& j) {
+    int lo = 0, hi = N - 1;   // the largest n with cu[n] / 64 + n <= s (increasing in n)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)cu[mid] / 64 + mid <= s) lo = mid;
+        else hi = mid - 1;
+    }
+    n = lo;
+    const int64_t cc = s - ((int64_t)cu[n] / 64 + n);
+    const int len = cu[n + 1] - cu[n];
+    if (cc < 0 || cc >= (len + 63) / 64) return false;
+    c = (int)cc;
+    const int64_t t0 = cu[n] + 64 * cc;
+    for (j = 1; j < M; ++j) {
+        const int64_t a = vt0[(size_t)j * N + n];
+        if (t0 >= a && t0 < a + vlen[(size_t)j * N + n]) return true;
+    }
+    return false;   // segment 0: its o is exact
+}
+
+// One warp per (chunk slot, head, 128-channel block): the chunk is listed for
+// the correction unless, in every row, the decay from the segment start is
+// below the smallest normal float or the state's row is zero.  (A product of
+// alphas that reached the denormals can stay at the smallest one for good.)
+__global__ void __launch_bounds__(256) split_select_kernel(
+    const int32_t* __restrict__ cu, int N, int M, int H, int d_v, int64_t slots,
+    const int64_t* __restrict__ vt0, const int32_t* __restrict__ vlen,
+    const float* __restrict__ gstart, const float* __restrict__ rnorm,
+    int32_t* __restrict__ ccount, int4* __restrict__ clist, const int32_t* __restrict__ status) {
+    if (*status == KDA_ERR_DEVICE_INPUT) return;
+    const int lane = threadIdx.x & 31;
+    const int nvb = d_v / kB;
+    const int64_t items = slots * H * nvb;
+    for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < items;
+         w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const int64_t s = w / (H * nvb);
+        const int hv = (int)(w % (H * nvb)), h = hv / nvb, vb = hv % nvb;
+        int n, c, j;
+        if (!slot_chunk(cu, N, M, vt0, vlen, s, n, c, j)) continue;   // uniform over the warp
+        const float* gs = gstart + ((size_t)s * H + h) * d_v + (size_t)vb * kB;
+        const float* rn = rnorm + ((((size_t)(j - 1) * N + n) * H + h) * d_v) + (size_t)vb * kB;
+        bool live = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            live |= !(gs[lane + 32 * i] < FLT_MIN) && !(rn[lane + 32 * i] == 0.f);
+        if (__any_sync(0xffffffffu, live) && lane == 0) {
+            const int at = atomicAdd(ccount, 1);
+            clist[at] = make_int4((int)s, hv, n, j);
+        }
+    }
+}
+
+constexpr int kQld = kB + 4;   // row stride of the q~ tile (16-byte rows)
+constexpr int kCorrThreads = 512;
+
+// Persistent: each CTA takes listed chunks in turn.  Thread (r, quarter):
+// value channel r of the block, tokens 16 quarter .. 16 quarter + 15.
+//   G_t,r   = gstart_r * prod_{i <= t} alpha_i,r
+//   bound   = G_t,r * |S_start row r| * |q~_t|  >= |G_t,r (S_start q~_t)_r|
+// o holds bf16(o from zero) already.  If bound <= 2^-20 |o_t,r| for every
+// element, the share is below 2^-12 of half a bf16 ulp of the value, so the
+// stored value is the rounding of the exact one except in the rare case of
+// a value within that distance of a rounding boundary; the chunk is left as
+// it is.  Otherwise o_t,r = bf16(o from zero + G_t,r (S_start q~_t)_r), with
+// o from zero in fp32 (ores) where the chunk kernel kept it (gstart_r >=
+// kOresFloor), else the bf16 value (where the decay is below kOresFloor the
+// share is small beside it, so the second rounding is rare and one ulp).
+__global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
+    int N, int H, int d_v, const float* __restrict__ alpha, const float* __restrict__ qtil,
+    const float* __restrict__ gstart, const float* __restrict__ sst,
+    const float* __restrict__ rnorm, const int32_t* __restrict__ cu,
+    const int32_t* __restrict__ ccount, const int4* __restrict__ clist,
+    const float* __restrict__ ores, __nv_bfloat16* __restrict__ o,
+    const int32_t* __restrict__ status) {
+    if (*status == KDA_ERR_DEVICE_INPUT) return;
+    extern __shared__ float sh[];
+    float* sQ = sh;                  // [64][kQld]
+    float* sN = sQ + 64 * kQld;      // [64] norms of the q~ rows
+    float* sTot = sN + 64;           // [4][128] products of alpha over each token quarter
+    float* sS = sTot + 4 * kB;       // [128][kB + 1] rows of the initial state
+    const int tid = threadIdx.x, r = tid & (kB - 1), qt = tid >> 7;
+    const int nvb = d_v / kB;
+    const int count = *ccount;
+    const int64_t ostride = (int64_t)H * d_v, qstride = (int64_t)H * kB;
+    for (int it = blockIdx.x; it < count; it += gridDim.x) {
+        const int4 e = clist[it];
+        const int h = e.y / nvb, vb = e.y % nvb, n = e.z, j = e.w;
+        const int64_t base = cu[n];
+        const int c = e.x - (int)(base / 64) - n;
+        const int64_t t0 = base + 64 * (int64_t)c;
+        const int nvalid = min(64, cu[n + 1] - (int)base - 64 * c);
+        const int ch = vb * kB + r;
+        const size_t srow = (((size_t)(j - 1) * N + n) * H + h) * d_v + ch;   // row of sst / rnorm
+        __syncthreads();   // the previous item's tiles are no longer read
+        for (int x = tid; x < 64 * (kB / 4); x += kCorrThreads) {
+            const int t = x / (kB / 4), k4 = x % (kB / 4);
+            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < nvalid)
+                q = *reinterpret_cast<const float4*>(qtil + (t0 + t) * qstride + (int64_t)h * kB + 4 * k4);
+            *reinterpret_cast<float4*>(sQ + t * kQld + 4 * k4) = q;
+        }
+        const float* arow = alpha + t0 * ostride + (int64_t)h * d_v + ch;
+        __nv_bfloat16* orow = o + t0 * ostride + (int64_t)h * d_v + ch;
+        float a[16], om[16];   // alpha, then its running product; |o from zero| (bf16)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int t = 16 * qt + i;
+            a[i] = t < nvalid ? arow[t * ostride] : 1.f;
+            om[i] = t < nvalid ? fabsf(__bfloat162float(orow[t * ostride])) : INFINITY;
+        }
+        const float g0 = gstart[((size_t)e.x * H + h) * d_v + ch];
+        const float rn = rnorm[srow];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) a[i] *= a[i - 1];   // running product within the quarter
+        sTot[qt * kB + r] = a[15];
+        __syncthreads();
+        {   // norms of the q~ rows: 8 threads per token
+            const int t = tid >> 3, part = tid & 7;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc = fmaf(sQ[t * kQld + 16 * part + k], sQ[t * kQld + 16 * part + k], acc);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            if (part == 0) sN[t] = sqrtf(acc);
+        }
+        float pre = g0;   // decay from the segment start to this quarter's first token
+        for (int q = 0; q < qt; ++q) pre *= sTot[q * kB + r];
+        __syncthreads();   // sN
+        bool need = false;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) need |= !(pre * a[i] * rn * sN[16 * qt + i] <= 0x1p-20f * om[i]);
+        if (!__syncthreads_or(need)) continue;
+        {   // the block's rows of S_start, coalesced
+            const float4* Sg = reinterpret_cast<const float4*>(sst + (srow - r) * kB);
+            for (int x = tid; x < kB * kB / 4; x += kCorrThreads) {
+                const float4 v = Sg[x];
+                float* d = sS + (x / (kB / 4)) * (kB + 1) + 4 * (x % (kB / 4));
+                d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+            }
+        }
+        __syncthreads();
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = 0.f;
+#pragma unroll 2
+        for (int k4 = 0; k4 < kB / 4; ++k4) {
+            const float* sr = sS + r * (kB + 1) + 4 * k4;
+            const float s0 = sr[0], s1 = sr[1], s2 = sr[2], s3 = sr[3];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 q = *reinterpret_cast<const float4*>(sQ + (16 * qt + i) * kQld + 4 * k4);
+                y[i] = fmaf(q.x, s0, fmaf(q.y, s1, fmaf(q.z, s2, fmaf(q.w, s3, y[i]))));
+            }
+        }
+        const float* orr = ores + t0 * ostride + (int64_t)h * d_v + ch;
+        const bool exact = g0 >= kOresFloor;   // the zero-start o was kept in fp32
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int t = 16 * qt + i;
+            if (t < nvalid) {
+                const float base = exact ? orr[t * ostride] : __bfloat162float(orow[t * ostride]);
+                orow[t * ostride] = __float2bfloat16_rn(fmaf(pre * a[i], y[i], base));
+            }
+        }
     }
 }
 
@@ -212,7 +414,8 @@ cudaError_t launch_split_plan(const PrefillArgs& a, const SplitLayout& L, char* 
     const int threads = 256, blocks = (a.num_seqs + threads - 1) / threads;
     split_plan_kernel<<<blocks, threads, 0, stream>>>(
         a.cu_seqlens, a.num_seqs, L.M, reinterpret_cast<int64_t*>(ws + L.vt0),
-        reinterpret_cast<int32_t*>(ws + L.vlen), a.status);
+        reinterpret_cast<int32_t*>(ws + L.vlen), reinterpret_cast<int32_t*>(ws + L.clist),
+        a.status);
     return cudaGetLastError();
 }
 
@@ -226,7 +429,38 @@ cudaError_t launch_split_combine(const PrefillArgs& a, const SplitLayout& L, cha
     split_combine_kernel<<<blocks, 256, smem, stream>>>(
         a.num_seqs, a.H, a.d_v, L.M, reinterpret_cast<const float*>(ws + L.sfin),
         reinterpret_cast<const float*>(ws + L.pbuf), reinterpret_cast<const float*>(ws + L.gbuf),
-        reinterpret_cast<float*>(ws + L.sst), a.status);
+        reinterpret_cast<float*>(ws + L.sst), reinterpret_cast<float*>(ws + L.rnorm), a.S_T,
+        a.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_correct(const PrefillArgs& a, const SplitLayout& L, char* ws,
+                                 cudaStream_t stream) {
+    const int64_t slots = a.total_tokens / 64 + a.num_seqs + 1;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidValue;
+    int32_t* ccount = reinterpret_cast<int32_t*>(ws + L.clist);
+    int4* clist = reinterpret_cast<int4*>(ws + L.clist + 16);
+    const int64_t warps = slots * a.H * (a.d_v / kB);
+    const int64_t want = (warps + 7) / 8;
+    const int sel_blocks = (int)(want < 16 * sms ? want : 16 * sms);
+    split_select_kernel<<<sel_blocks, 256, 0, stream>>>(
+        a.cu_seqlens, a.num_seqs, L.M, a.H, a.d_v, slots,
+        reinterpret_cast<const int64_t*>(ws + L.vt0), reinterpret_cast<const int32_t*>(ws + L.vlen),
+        reinterpret_cast<const float*>(ws + L.gstart), reinterpret_cast<const float*>(ws + L.rnorm),
+        ccount, clist, a.status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const int smem = (64 * kQld + 64 + 4 * kB + kB * (kB + 1)) * (int)sizeof(float);
+    err = cudaFuncSetAttribute(split_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem);
+    if (err != cudaSuccess) return err;
+    split_correct_kernel<<<2 * sms, kCorrThreads, smem, stream>>>(
+        a.num_seqs, a.H, a.d_v, static_cast<const float*>(a.alpha),
+        reinterpret_cast<const float*>(ws + L.qtil), reinterpret_cast<const float*>(ws + L.gstart),
+        reinterpret_cast<const float*>(ws + L.sst), reinterpret_cast<const float*>(ws + L.rnorm),
+        a.cu_seqlens, ccount, clist, reinterpret_cast<const float*>(ws + L.ores),
+        static_cast<__nv_bfloat16*>(a.o), a.status);
     return cudaGetLastError();
 }
 

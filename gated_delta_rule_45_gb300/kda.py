@@ -57,6 +57,8 @@ def load(path: str | None = None):
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     lib.kda_prefill_workspace_size.restype = sz
     lib.kda_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.kda_prefill_workspace_size_tokens.restype = sz
+    lib.kda_prefill_workspace_size_tokens.argtypes = [i32, i64, i32, i32, i32, i32]
     prefill_args = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, ctypes.c_int, i32,
                     vp, vp, vp, sz]
     lib.kda_prefill.restype = ctypes.c_int
@@ -167,8 +169,14 @@ def supported(kernel: str, H: int, d_k: int, d_v: int, dtype: torch.dtype, chunk
 
 
 def workspace_size(num_seqs: int, H: int = 1, d_k: int = 128, d_v: int = 128,
-                   chunk: int = 64) -> int:
-    return int(load().kda_prefill_workspace_size(num_seqs, H, d_k, d_v, chunk))
+                   chunk: int = 64, total_tokens: int | None = None) -> int:
+    """Prefill workspace bytes: kda_prefill_workspace_size_tokens when the
+    token count is given (room for the sequence-axis split where it applies),
+    else kda_prefill_workspace_size (no split)."""
+    if total_tokens is None:
+        return int(load().kda_prefill_workspace_size(num_seqs, H, d_k, d_v, chunk))
+    return int(load().kda_prefill_workspace_size_tokens(num_seqs, total_tokens, H, d_k, d_v,
+                                                        chunk))
 
 
 def prefill_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, workspace, *, chunk: int = 64,
@@ -230,7 +238,8 @@ def prefill_gates(q, k, v, alpha, beta, S0, cu_seqlens, *, gate: str = "channel"
     N = cu_seqlens.numel() - 1
     o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
     S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=q.device)
-    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk), dtype=torch.uint8, device=q.device)
+    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk, T), dtype=torch.uint8,
+                     device=q.device)
     prefill_gates_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, ws, gate=gate, chunk=chunk,
                        kernel=kernel, stream=stream)
     if check_device_status:
@@ -246,7 +255,8 @@ def prefill(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64, kernel: st
     N = cu_seqlens.numel() - 1
     o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
     S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=q.device)
-    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk), dtype=torch.uint8, device=q.device)
+    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk, T), dtype=torch.uint8,
+                     device=q.device)
     prefill_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, ws, chunk=chunk, kernel=kernel,
                  stream=stream)
     if check_device_status:
@@ -379,7 +389,8 @@ def prefill_additive(q, k, v, alpha, beta, S0, cu_seqlens, *, chunk: int = 64,
     N = cu_seqlens.numel() - 1
     o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
     S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=q.device)
-    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk), dtype=torch.uint8, device=q.device)
+    ws = torch.empty(workspace_size(N, H, d_k, d_v, chunk, T), dtype=torch.uint8,
+                     device=q.device)
     prefill_additive_into(q, k, v, alpha, beta, S0, cu_seqlens, o, S_T, ws, chunk=chunk,
                           kernel=kernel, stream=stream)
     if check_device_status:

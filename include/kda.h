@@ -76,15 +76,17 @@ typedef enum {
     KDA_KERNEL_AUTO = 0,
     KDA_KERNEL_CHUNK_SIMT = 1,   /* fp32 CUDA-core chunk kernel: any supported shape */
     KDA_KERNEL_CHUNK_TC = 2,     /* tcgen05 / TMEM / TMA chunk kernel */
-    /* the tensor-core kernel with the sequence axis split into M >= 3
-     * segments of whole chunks: a first pass runs segment 0 of every sequence
-     * from S0 and, for segments 1..M-2, the state reached from zero, the
-     * product of alpha and the transition prod (I - beta k k^T); a scan
-     * chains these affine maps into each segment's initial state; a second
-     * pass runs segments 1..M-1 from those states.  Same results as
-     * KDA_KERNEL_CHUNK_TC up to rounding.  Only for batches with few chains
-     * (those for which kda_prefill_workspace_size includes the segment
-     * buffers), whatever the sequence lengths. */
+    /* the tensor-core kernel with the sequence axis split into M >= 2
+     * segments of whole chunks: one pass runs segment 0 of every sequence
+     * from S0 and, for segments 1..M-1, the segment from a zero state (its
+     * output, final state and product of alpha) and its transition
+     * prod (I - beta k k^T) applied to each token's q; a scan chains these
+     * affine maps into each segment's initial state and S_T; a correction
+     * adds each later segment's initial-state share to its output where it
+     * can change the stored value.  Same results as KDA_KERNEL_CHUNK_TC up
+     * to rounding.  Only for batches with few chains (those for which
+     * kda_prefill_workspace_size_tokens exceeds kda_prefill_workspace_size),
+     * whatever the sequence lengths. */
     KDA_KERNEL_CHUNK_TC_SPLIT = 3
 } kda_prefill_kernel;
 
@@ -102,19 +104,31 @@ typedef enum {
 
 /*
  * Bytes of device workspace kda_prefill needs for `num_seqs` sequences of H
- * heads with these sizes.  Returns 0 for num_seqs < 0.  The workspace holds
- * the varlen schedule (sequence order, work counter, device error word), a
- * bitmap of the channels the tensor-core kernel hands to the portable one
- * (16 bytes per (sequence, head, 128-channel block); see "Fast decay" at
- * kda_prefill) and, for batches with few (sequence, head, 128-channel block)
- * chains on the current device, the buffers of the sequence-axis split in
- * the bitmap's place: at most 8 x num_seqs x H x d_v x d_k x 12 bytes.  A
- * smaller workspace of at least the schedule's size is accepted; it never
- * splits and reports fast-decaying channels instead of recomputing them.
- * Its contents need no initialisation and are overwritten by every call.
+ * heads with these sizes, without the sequence-axis split.  Returns 0 for
+ * num_seqs < 0.  The workspace holds the varlen schedule (sequence order,
+ * work counter, device error word) and a bitmap of the channels the
+ * tensor-core kernel hands to the portable one (16 bytes per (sequence,
+ * head, 128-channel block); see "Fast decay" at kda_prefill).  A smaller
+ * workspace of at least the schedule's size is accepted; it reports
+ * fast-decaying channels instead of recomputing them.  Its contents need no
+ * initialisation and are overwritten by every call.
  */
 size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
                                   int32_t chunk);
+
+/*
+ * kda_prefill_workspace_size for a batch of `total_tokens` tokens, with room
+ * for the sequence-axis split where the kernel choice may take it (batches
+ * with few (sequence, head, 128-channel block) chains on the current
+ * device): its buffers, in the bitmap's place, hold each segment's states,
+ * fp32 q-transforms of every token (total_tokens x H x d_k x 4 bytes) and
+ * the zero-start outputs of later segments in fp32 (total_tokens x H x d_v x 4
+ * bytes) and per-chunk decay factors (about total_tokens / 64 x H x d_v x 4 bytes).
+ * Returns 0 for num_seqs < 0 or total_tokens < 0.  With a workspace of
+ * kda_prefill_workspace_size bytes the split is not taken.
+ */
+size_t kda_prefill_workspace_size_tokens(int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                         int32_t d_k, int32_t d_v, int32_t chunk);
 
 /*
  * Chunkwise-parallel prefill over a packed (varlen) batch.  Runs the
@@ -135,9 +149,10 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t H, int32_t d_k, int3
  *   o                     output [T][H][d_v] (dtype)
  *   S_T                   output [N][H][d_v][d_k] fp32; may equal S0; may be
  *                         NULL only when num_seqs == 0
- *   workspace             device memory of kda_prefill_workspace_size bytes,
- *                         16-byte aligned; must not be shared by calls that
- *                         may run concurrently
+ *   workspace             device memory of kda_prefill_workspace_size_tokens
+ *                         bytes (kda_prefill_workspace_size: no
+ *                         sequence-axis split), 16-byte aligned; must not be
+ *                         shared by calls that may run concurrently
  *
  * Supported: 1 <= H, 16 <= d_k <= 128 and d_k % 16 == 0, 1 <= d_v <= 1024
  * and d_v % 16 == 0, alpha in (0, 1].
@@ -167,7 +182,7 @@ kda_status kda_prefill(const void* q, const void* k, const void* v,
  * shape).  Requesting KDA_KERNEL_CHUNK_TC or KDA_KERNEL_CHUNK_TC_SPLIT for a
  * shape the tensor-core kernel does not cover returns KDA_ERR_UNSUPPORTED;
  * KDA_KERNEL_CHUNK_TC_SPLIT with a workspace smaller than
- * kda_prefill_workspace_size returns KDA_ERR_INVALID_ARG. */
+ * kda_prefill_workspace_size_tokens returns KDA_ERR_INVALID_ARG. */
 kda_status kda_prefill_ex(const void* q, const void* k, const void* v,
                           const float* alpha, const float* beta, const float* S0,
                           const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,

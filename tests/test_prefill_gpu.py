@@ -155,15 +155,15 @@ def test_bad_cu_seqlens_reported_and_nothing_written(bad):
         assert torch.all(o == 5.0) and torch.all(S_T == 5.0)
 
 
-def _split_case(lengths, H, d_v, s0_std, seed):
+def _split_case(lengths, H, d_v, s0_std, seed, alpha_mu=3.0):
     spec = synth.PrefillSpec(num_seqs=len(lengths), len_lo=1, len_hi=1, H=H, d_k=128, d_v=d_v,
-                             chunk=64, s0_std=s0_std, seed=seed)
+                             chunk=64, s0_std=s0_std, alpha_mu=alpha_mu, seed=seed)
     d = synth.prefill_inputs(spec)
     # replace the drawn lengths with the given ones (inputs are per token, so
     # a longer draw is cut to size)
     T = int(sum(lengths))
     big = synth.PrefillSpec(num_seqs=1, len_lo=T, len_hi=T, H=H, d_k=128, d_v=d_v, chunk=64,
-                            s0_std=0.0, seed=seed)
+                            s0_std=0.0, alpha_mu=alpha_mu, seed=seed)
     db = synth.prefill_inputs(big)
     for key in ("q", "k", "v", "alpha", "beta"):
         d[key] = db[key]
@@ -172,22 +172,26 @@ def _split_case(lengths, H, d_v, s0_std, seed):
     return spec, d
 
 
-@pytest.mark.parametrize("lengths,H,d_v,s0_std", [
-    ([1000, 60, 2500], 2, 128, 0.1),     # one single-chunk sequence: mostly empty segments
-    ([4096, 0, 3000], 1, 256, 0.1),      # an empty sequence, two value blocks
-    ([5000], 3, 128, 0.0),               # no initial state
+@pytest.mark.parametrize("lengths,H,d_v,s0_std,alpha_mu", [
+    ([1000, 60, 2500], 2, 128, 0.1, 3.0),   # one single-chunk sequence: mostly empty segments
+    ([4096, 0, 3000], 1, 256, 0.1, 3.0),    # an empty sequence, two value blocks
+    ([5000], 3, 128, 0.0, 3.0),             # no initial state
+    ([6000, 3000], 2, 128, 0.5, 7.0),       # long memory: every chunk takes a correction
+    ([4000, 130], 2, 256, 0.5, 1.0),        # quick decay: corrections die out in a few chunks
 ])
-def test_sequence_split_matches_oracle(lengths, H, d_v, s0_std):
-    """The split form (segment 0 from S0, segment maps from zero / identity,
-    their scan, then the other segments from their true initial states)
+def test_sequence_split_matches_oracle(lengths, H, d_v, s0_std, alpha_mu):
+    """The split form (one pass: segment 0 from S0, every other segment from
+    zero and as a transition from the identity; the scan of the segment maps;
+    each later segment's output corrected by its initial state's share)
     against the oracle, on every (sequence, head)."""
-    spec, d = _split_case(lengths, H, d_v, s0_std, seed=11)
+    spec, d = _split_case(lengths, H, d_v, s0_std, seed=11, alpha_mu=alpha_mu)
     if not kda.supported("tc_split", H, 128, d_v, torch.bfloat16, 64):
         pytest.skip("tensor-core kernel not available for this shape")
     dev = parity.to_device(d)
     N = len(lengths)
-    ws_bytes = kda.workspace_size(N, H, 128, d_v, 64)
-    assert ws_bytes > kda.workspace_size(N, 1, 16, 16, 16)   # room for the segments
+    T = int(sum(lengths))
+    ws_bytes = kda.workspace_size(N, H, 128, d_v, 64, T)
+    assert ws_bytes > kda.workspace_size(N, H, 128, d_v, 64)   # room for the segments
     o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
                          dev["cu_seqlens"], chunk=64, kernel="tc_split",
                          check_device_status=True)
@@ -208,7 +212,7 @@ def test_sequence_split_in_place_state():
     S = dev["S0"].clone()
     T = int(d["cu_seqlens"][-1])
     o = torch.empty((T, 2, 128), dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(kda.workspace_size(2, 2, 128, 128, 64), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(kda.workspace_size(2, 2, 128, 128, 64, T), dtype=torch.uint8, device="cuda")
     kda.prefill_into(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], S,
                      dev["cu_seqlens"], o, S, ws, kernel="tc_split")
     kda.device_status(ws)
