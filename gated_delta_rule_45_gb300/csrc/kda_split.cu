@@ -241,16 +241,17 @@ constexpr int kCorrThreads = 512;
 
 // Persistent: each CTA takes listed chunks in turn.  Thread (r, quarter):
 // value channel r of the block, tokens 16 quarter .. 16 quarter + 15.
-//   G_t,r   = gstart_r * prod_{i <= t} alpha_i,r
-//   bound   = G_t,r * |S_start row r| * |q~_t|  >= |G_t,r (S_start q~_t)_r|
+//   G_t,r   = gstart_r * prod_{i <= t} alpha_i,r  <= gstart_r  (alpha <= 1)
+//   bound   = gstart_r * |S_start row r| * |q~_t|  >= |G_t,r (S_start q~_t)_r|
 // o holds bf16(o from zero) already.  If bound <= 2^-20 |o_t,r| for every
 // element, the share is below 2^-12 of half a bf16 ulp of the value, so the
 // stored value is the rounding of the exact one except in the rare case of
 // a value within that distance of a rounding boundary; the chunk is left as
-// it is.  Otherwise o_t,r = bf16(o from zero + G_t,r (S_start q~_t)_r), with
-// o from zero in fp32 (ores) where the chunk kernel kept it (gstart_r >=
-// kOresFloor), else the bf16 value (where the decay is below kOresFloor the
-// share is small beside it, so the second rounding is rare and one ulp).
+// it is (having read only q~ and o).  Otherwise alpha is read and
+// o_t,r = bf16(o from zero + G_t,r (S_start q~_t)_r), with o from zero in
+// fp32 (ores) where the chunk kernel kept it (gstart_r >= kOresFloor), else
+// the bf16 value (where the decay is below kOresFloor the share is small
+// beside it, so the second rounding is rare and one ulp).
 __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
     int N, int H, int d_v, const float* __restrict__ alpha, const float* __restrict__ qtil,
     const float* __restrict__ gstart, const float* __restrict__ sst,
@@ -278,27 +279,32 @@ __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
         const int ch = vb * kB + r;
         const size_t srow = (((size_t)(j - 1) * N + n) * H + h) * d_v + ch;   // row of sst / rnorm
         __syncthreads();   // the previous item's tiles are no longer read
-        for (int x = tid; x < 64 * (kB / 4); x += kCorrThreads) {
-            const int t = x / (kB / 4), k4 = x % (kB / 4);
-            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < nvalid)
-                q = *reinterpret_cast<const float4*>(qtil + (t0 + t) * qstride + (int64_t)h * kB + 4 * k4);
-            *reinterpret_cast<float4*>(sQ + t * kQld + 4 * k4) = q;
+        {   // the q~ tile: all four loads of a thread in flight together
+            float4 q[64 * (kB / 4) / kCorrThreads];
+#pragma unroll
+            for (int u = 0; u < 64 * (kB / 4) / kCorrThreads; ++u) {
+                const int x = tid + u * kCorrThreads, t = x / (kB / 4), k4 = x % (kB / 4);
+                q[u] = t < nvalid ? *reinterpret_cast<const float4*>(qtil + (t0 + t) * qstride +
+                                                                     (int64_t)h * kB + 4 * k4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 64 * (kB / 4) / kCorrThreads; ++u) {
+                const int x = tid + u * kCorrThreads, t = x / (kB / 4), k4 = x % (kB / 4);
+                *reinterpret_cast<float4*>(sQ + t * kQld + 4 * k4) = q[u];
+            }
         }
         const float* arow = alpha + t0 * ostride + (int64_t)h * d_v + ch;
         __nv_bfloat16* orow = o + t0 * ostride + (int64_t)h * d_v + ch;
-        float a[16], om[16];   // alpha, then its running product; |o from zero| (bf16)
+        // |o from zero| of this quarter, kept in the state tile's space for the test
+        float* sO = sS;   // [64][128]
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int t = 16 * qt + i;
-            a[i] = t < nvalid ? arow[t * ostride] : 1.f;
-            om[i] = t < nvalid ? fabsf(__bfloat162float(orow[t * ostride])) : INFINITY;
+            sO[t * kB + r] = t < nvalid ? fabsf(__bfloat162float(orow[t * ostride])) : INFINITY;
         }
         const float g0 = gstart[((size_t)e.x * H + h) * d_v + ch];
         const float rn = rnorm[srow];
-#pragma unroll
-        for (int i = 1; i < 16; ++i) a[i] *= a[i - 1];   // running product within the quarter
-        sTot[qt * kB + r] = a[15];
         __syncthreads();
         {   // norms of the q~ rows: 8 threads per token
             const int t = tid >> 3, part = tid & 7;
@@ -310,19 +316,26 @@ __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
             acc += __shfl_xor_sync(0xffffffffu, acc, 4);
             if (part == 0) sN[t] = sqrtf(acc);
         }
-        float pre = g0;   // decay from the segment start to this quarter's first token
-        for (int q = 0; q < qt; ++q) pre *= sTot[q * kB + r];
         __syncthreads();   // sN
+        // alpha <= 1, so the decay at every token of the chunk is at most g0
         bool need = false;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) need |= !(pre * a[i] * rn * sN[16 * qt + i] <= 0x1p-20f * om[i]);
+        const float b0 = g0 * rn;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const int t = 16 * qt + i;
+            need |= !(b0 * sN[t] <= 0x1p-20f * sO[t * kB + r]);
+        }
         if (!__syncthreads_or(need)) continue;
-        {   // the block's rows of S_start, coalesced
+        {   // the block's rows of S_start, coalesced, all loads in flight together
             const float4* Sg = reinterpret_cast<const float4*>(sst + (srow - r) * kB);
-            for (int x = tid; x < kB * kB / 4; x += kCorrThreads) {
-                const float4 v = Sg[x];
+            float4 v[kB * kB / 4 / kCorrThreads];
+#pragma unroll
+            for (int u = 0; u < kB * kB / 4 / kCorrThreads; ++u) v[u] = Sg[tid + u * kCorrThreads];
+#pragma unroll
+            for (int u = 0; u < kB * kB / 4 / kCorrThreads; ++u) {
+                const int x = tid + u * kCorrThreads;
                 float* d = sS + (x / (kB / 4)) * (kB + 1) + 4 * (x % (kB / 4));
-                d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+                d[0] = v[u].x; d[1] = v[u].y; d[2] = v[u].z; d[3] = v[u].w;
             }
         }
         __syncthreads();
@@ -339,14 +352,29 @@ __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
                 y[i] = fmaf(q.x, s0, fmaf(q.y, s1, fmaf(q.z, s2, fmaf(q.w, s3, y[i]))));
             }
         }
+        // the decay: this quarter's running product of alpha after the earlier quarters'
+        float a16[16], run = 1.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int t = 16 * qt + i;
+            a16[i] = t < nvalid ? arow[t * ostride] : 1.f;
+            run *= a16[i];
+        }
+        __syncthreads();   // every thread is done with the state tile
+        sTot[qt * kB + r] = run;
+        __syncthreads();
+        float pre = g0;
+        for (int q = 0; q < qt; ++q) pre *= sTot[q * kB + r];
         const float* orr = ores + t0 * ostride + (int64_t)h * d_v + ch;
         const bool exact = g0 >= kOresFloor;   // the zero-start o was kept in fp32
+        float G = pre;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int t = 16 * qt + i;
             if (t < nvalid) {
+                G *= a16[i];
                 const float base = exact ? orr[t * ostride] : __bfloat162float(orow[t * ostride]);
-                orow[t * ostride] = __float2bfloat16_rn(fmaf(pre * a[i], y[i], base));
+                orow[t * ostride] = __float2bfloat16_rn(fmaf(G, y[i], base));
             }
         }
     }
