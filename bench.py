@@ -42,9 +42,9 @@ UNIT = "tokens/s"
 # kernel's source is the one the capture was taken on (its sha256 below);
 # after any change to the kernel it is null until captured again.
 TRAFFIC_CAPTURE = {
-    "bytes_per_launch": 10.31e9,
-    "date": "2026-12-02",
-    "sources_sha256": None,
+    "bytes_per_launch": 10.33e9,
+    "date": "2026-12-03",
+    "sources_sha256": "107181fee4102a317e47876189eaa2f8b6e99d9e18a7ac1ce9b0107e6edab1b4",
 }
 TRAFFIC_SOURCES = ("gated_delta_rule_45_gb300/csrc/kda_prefill_tc.cu",
                    "gated_delta_rule_45_gb300/csrc/kda_tc.cuh")
@@ -973,7 +973,7 @@ def main(argv=None):
     p.add_argument("--no-components", action="store_true",
                    help="skip timing the other workloads' kernels alone after the step")
     p.add_argument("--workload",
-                   choices=["varlen", "varlen_prefill", "prefill", "long", "decode",
+                   choices=["varlen", "varlen_prefill", "prefill", "long", "long_small", "decode",
                             "l2_resident", "prefill_head_gate", "prefill_log_gate",
                             "backward", "backward_small", "attnres", "attnres_small",
                             "prefill_additive"],
@@ -983,6 +983,8 @@ def main(argv=None):
                         "l2_resident: the chunk kernel with its inputs in L2, against the "
                         "tensor-core peak; prefill_head_gate / prefill_log_gate: the prefill "
                         "workload with a per-head fp32 gate / a bf16 log-alpha gate; "
+                        "long_small: the long workload at 32768 tokens, for profiling the "
+                        "sequence-axis split; "
                         "backward: kda_backward on the prefill workload; backward_small: "
                         "the same with 512 tokens per sequence, for profiling; attnres: "
                         "Blocked Attention Residuals over a 64-layer network; attnres_small: "

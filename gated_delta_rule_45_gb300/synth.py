@@ -75,8 +75,12 @@ VARLEN_DECODE_STEPS = 32
 # ~110 MB of inputs and states, so that back-to-back launches are served from L2.
 L2_RESIDENT = PrefillSpec(num_seqs=152, len_lo=384, len_hi=384, H=1, d_k=128, d_v=128,
                           chunk=64, s0_std=0.1)
+# The long workload at a quarter of the length (32768 tokens), small enough for
+# multi-pass profiler captures of the sequence-axis split's kernels.
+LONG_SMALL = PrefillSpec(num_seqs=1, len_lo=32768, len_hi=32768, H=32, d_k=128, d_v=128,
+                         chunk=64, alpha_mu=5.0, s0_std=0.1)
 WORKLOADS = {"tiny": TINY, "decode": DECODE, "prefill": PREFILL, "long": LONG, "varlen": VARLEN,
-             "l2_resident": L2_RESIDENT}
+             "l2_resident": L2_RESIDENT, "long_small": LONG_SMALL}
 
 
 def _normal(gen: torch.Generator, shape, mean: float = 0.0, std: float = 1.0) -> torch.Tensor:
