@@ -21,7 +21,9 @@ constexpr float kOresFloor = 0x1p-10f;
 // Layout of the prefill workspace (all offsets in bytes from its start).
 //   [0, 4)    int32 device status (0 = ok, or a KDA_ERR_DEVICE_* code)
 //   [4, 8)    int32 work counter of the persistent tensor-core kernel
-//   [16, ...) int32 order[num_seqs]: sequence indices, longest first
+//   [16, ...) int32 order[num_seqs]: sequence indices, longest first, then
+//             int32 [num_seqs]: the planner's sorted runs (batches of more
+//             than 1024 sequences)
 //   then, for the tensor-core kernel without the sequence-axis split (whose
 //   buffers take the same place), when the workspace has room: uint32
 //   [num_seqs][H][d_v / 128][4], for each 128-channel block the channels whose
@@ -31,8 +33,9 @@ struct WorkspaceLayout {
     static constexpr size_t kStatus = 0;
     static constexpr size_t kCounter = 4;
     static constexpr size_t kOrder = 16;
+    // order[num_seqs], then the planner's sorted runs (num_seqs more)
     static size_t bytes(int32_t num_seqs) {
-        size_t b = kOrder + sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 0);
+        size_t b = kOrder + 2 * sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 0);
         return (b + 255) & ~(size_t)255;
     }
     static size_t redo_bytes(int32_t num_seqs, int32_t H, int32_t d_v) {

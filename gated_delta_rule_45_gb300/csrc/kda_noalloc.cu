@@ -2,7 +2,7 @@
 // caller-provided workspace, for callers that cannot allocate device memory.
 //
 // The scratch is a file-scope __device__ array, so every GPU that loads this
-// library holds it (about 512 KB) until
+// library holds it (about 768 KB) until
 // the process exits.  Host code must not pass the array's name to a kernel:
 // on the host that name is only a stand-in for the symbol.  Its device
 // address is looked up on every call, with the caller's device and context
@@ -27,7 +27,7 @@ namespace {
 // the tensor-core kernel may hand back to the portable one (16 bytes per
 // (sequence, head, 128-channel block): up to 16384 such blocks)
 constexpr size_t kScheduleBytes =
-    (kda::WorkspaceLayout::kOrder + sizeof(int32_t) * (size_t)KDA_NOALLOC_MAX_SEQS + 255) &
+    (kda::WorkspaceLayout::kOrder + 2 * sizeof(int32_t) * (size_t)KDA_NOALLOC_MAX_SEQS + 255) &
     ~(size_t)255;
 constexpr size_t kScratchBytes = kScheduleBytes + 16 * 16384;
 

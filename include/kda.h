@@ -286,7 +286,7 @@ kda_status kda_check_wait_timeout(void* workspace, size_t workspace_bytes, uint6
  * the segment buffers): a batch with few long chains, such as one sequence
  * of 128K tokens with 32 heads, runs slower here than through kda_prefill
  * with a full workspace.  The scratch it needs lives in a device array built
- * into the library (about 512 KB on every GPU that loads it, held until the
+ * into the library (about 768 KB on every GPU that loads it, held until the
  * process exits).  Every call looks up that array's address in the CUDA
  * context current at the call (cudaGetSymbolAddress, which allocates
  * nothing), so switching driver contexts or resetting the device between

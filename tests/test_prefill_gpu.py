@@ -384,3 +384,62 @@ def test_decay_beyond_the_chunk_forms_range_is_reported(kernel):
     ref = parity.oracle_pairs(d, [(0, 0), (0, 1), (1, 0)])
     wo, ws = parity.compare_pairs(d, o, S_T, ref)
     assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
+
+
+def _lengths_case(lengths, H, d, seed, dtype="bf16"):
+    """A batch with the given sequence lengths (inputs drawn for the total)."""
+    T = int(sum(lengths))
+    big = synth.PrefillSpec(num_seqs=1, len_lo=max(T, 1), len_hi=max(T, 1), H=H, d_k=d, d_v=d,
+                            chunk=64, dtype=dtype, s0_std=0.0, seed=seed)
+    d_ = synth.prefill_inputs(big)
+    spec = synth.PrefillSpec(num_seqs=len(lengths), len_lo=1, len_hi=1, H=H, d_k=d, d_v=d,
+                             chunk=64, dtype=dtype, s0_std=0.1, seed=seed)
+    d_["S0"] = synth.prefill_inputs(spec)["S0"]
+    d_["spec"] = spec
+    for key in ("q", "k", "v", "alpha", "beta"):
+        d_[key] = d_[key][:T]
+    d_["cu_seqlens"] = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    d_["lengths"] = list(lengths)
+    return d_
+
+
+@pytest.mark.parametrize("N", [1, 7, 1024, 1025, 3000, 5000])
+def test_planner_order_is_longest_first(N):
+    """The planner's order (in the workspace after a prefill) is exactly the
+    sequences sorted by (-length, index): one sorted run up to 1024
+    sequences, several runs merged by rank beyond; lengths with many ties."""
+    rng = np.random.default_rng(N)
+    lengths = rng.integers(0, 40, size=N).tolist()
+    d = _lengths_case(lengths, 1, 16, seed=N, dtype="fp32")
+    dev = parity.to_device(d)
+    T = int(sum(lengths))
+    o = torch.empty((T, 1, 16), dtype=torch.float32, device="cuda")
+    S_T = torch.empty((N, 1, 16, 16), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.workspace_size(N, 1, 16, 16, 16, T), dtype=torch.uint8, device="cuda")
+    kda.prefill_into(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                     dev["cu_seqlens"], o, S_T, ws, chunk=16)
+    kda.device_status(ws)
+    order = ws[16:16 + 4 * N].cpu().view(torch.int32).tolist()
+    assert order == sorted(range(N), key=lambda i: (-lengths[i], i))
+
+
+def test_many_short_sequences_tensor_core():
+    """1500 sequences (several planner runs) through the tensor-core kernel:
+    sampled (sequence, head) pairs against the oracle, and every final state
+    against the portable kernel."""
+    rng = np.random.default_rng(77)
+    lengths = rng.integers(1, 150, size=1500).tolist()
+    d = _lengths_case(lengths, 1, 128, seed=77)
+    if not kda.supported("tc", 1, 128, 128, torch.bfloat16, 64):
+        pytest.skip("tensor-core kernel not available for this shape")
+    dev = parity.to_device(d)
+    o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], chunk=64, kernel="tc", check_device_status=True)
+    pairs = [(int(n), 0) for n in rng.choice(1500, size=40, replace=False)]
+    pairs += [(int(np.argmax(lengths)), 0), (int(np.argmin(lengths)), 0)]
+    ref = parity.oracle_pairs(d, sorted(set(pairs)))
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
+    o2, S2 = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], chunk=64, kernel="simt", check_device_status=True)
+    assert parity.rel(S_T.cpu().numpy(), S2.cpu().numpy()) < 1e-3
