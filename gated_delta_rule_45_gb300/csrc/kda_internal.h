@@ -63,6 +63,8 @@ struct WorkspaceLayout {
 //                                       segments 1..M-1 (P_{<=t}: the product
 //                                       of (I - beta k k^T) from the segment
 //                                       start through token t)
+//   qfro   fp32 [T / 64 + N + 1][H]     per chunk of segments 1..M-1: the sum of
+//                                       squares of P_{<=t} q_t over its tokens
 //   ores   fp32 [T][H][d_v]             o of segments 1..M-1 from a zero start,
 //                                       for the chunks (and channels) whose
 //                                       gstart is at least kOresFloor
@@ -72,7 +74,7 @@ struct WorkspaceLayout {
 struct SplitLayout {
     int M = 1;
     size_t vt0 = 0, vlen = 0, sfin = 0, pbuf = 0, gbuf = 0, sst = 0, rnorm = 0, gstart = 0,
-           qtil = 0, ores = 0, clist = 0, end = 0;
+           qtil = 0, qfro = 0, qfro_bytes = 0, ores = 0, clist = 0, end = 0;
 };
 // Segments for this shape on the current device (1: no split).
 int split_segments(int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v, int32_t chunk);

@@ -147,6 +147,9 @@ struct TcParams {
     float* gstart;
     float* qtil;
     float* ores;
+    // transition items also add each chunk's sum of squares of P_{<=t} q_t
+    // (over its tokens and rows) to qfro [slot][H], zeroed beforehand
+    float* qfro;
     int32_t gstart_lo;
     const float* alpha_s;   // GATE_SCALAR: alpha [T][H]
     // GATE_F32_CKPT: fp32 [slots][H][d_v][DK]; chunk c of sequence n starting
@@ -732,8 +735,11 @@ __device__ void run_token_group(const TcParams& p, const Ctx& cx, int t, int war
 // Split outputs, out of line so that the chunk loop's code stays small:
 // 32 token rows of one channel in fp32, from TMEM (the transition items'
 // P_{<=t} q_t) or from registers (a later segment's o from a zero start).
+// The TMEM version also adds the warp's sum of squares of the stored values
+// to *fro (one atomic per warp) when fro is not null.
 __device__ __noinline__ void store_tmem_column_f32(uint32_t taddr, float* dst, int64_t stride,
-                                                   int lim) {
+                                                   int lim, float* fro) {
+    float acc = 0.f;
 #pragma unroll 1
     for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t v[16];
@@ -741,7 +747,16 @@ __device__ __noinline__ void store_tmem_column_f32(uint32_t taddr, float* dst, i
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            if (16 * q2 + j < lim) dst[(16 * q2 + j) * stride] = __uint_as_float(v[j]);
+            if (16 * q2 + j < lim) {
+                const float x = __uint_as_float(v[j]);
+                dst[(16 * q2 + j) * stride] = x;
+                acc = fmaf(x, x, acc);
+            }
+    }
+    if (fro) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if ((threadIdx.x & 31) == 0) atomicAdd(fro, acc);
     }
 }
 struct Column32 {
@@ -850,11 +865,15 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
         float gtot = 1.f;   // prod alpha over the item, for g_out
         // where this item's per-chunk decay from the segment start goes (split only)
         float* gs_row = nullptr;
-        if (SPLIT && p.gstart && !rg.pk && h == 0 && it.n >= p.gstart_lo) {
+        float* qf_row = nullptr;   // transition items: the chunk sums of squares of their outputs
+        if (SPLIT && p.gstart && (rg.pk || h == 0) && it.n >= p.gstart_lo) {
             const int n0 = it.n % p.gstart_lo;
             const int64_t c0 = p.cu[n0];
             const int64_t slot = c0 / C + n0 + (it.t0 - c0) / C;
-            gs_row = p.gstart + ((size_t)slot * p.H + it.h) * p.d_v + ch;
+            if (rg.pk)
+                qf_row = p.qfro ? p.qfro + (size_t)slot * p.H + it.h : nullptr;
+            else
+                gs_row = p.gstart + ((size_t)slot * p.H + it.h) * p.d_v + ch;
         }
 
         tmem_st_wait();
@@ -1068,7 +1087,8 @@ __device__ void run_row_group(const TcParams& p, const Ctx& cx, int rt, int warp
                     const int64_t qstride = (int64_t)p.H * DK;
                     store_tmem_column_f32(lane_addr + TM_SKQ + 64 + 32 * h,
                                           p.qtil + (tok0 + 32 * h) * qstride + (int64_t)it.h * DK + ch,
-                                          qstride, nvalid - 32 * h);
+                                          qstride, nvalid - 32 * h,
+                                          qf_row ? qf_row + (size_t)c * p.H : nullptr);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&cx.bars[B_O_READ]);
@@ -1311,6 +1331,7 @@ bool init_params(const PrefillArgs& a, TcParams& p) {
     p.gstart = nullptr;
     p.qtil = nullptr;
     p.ores = nullptr;
+    p.qfro = nullptr;
     p.gstart_lo = 0;
     return true;
 }
@@ -1412,6 +1433,8 @@ cudaError_t launch_prefill_tc_split(const PrefillArgs& a, const SplitLayout& L, 
     p.P_out = reinterpret_cast<float*>(ws + L.pbuf);
     p.qtil = reinterpret_cast<float*>(ws + L.qtil);
     p.ores = reinterpret_cast<float*>(ws + L.ores);
+    p.qfro = reinterpret_cast<float*>(ws + L.qfro);
+    if ((err = cudaMemsetAsync(p.qfro, 0, L.qfro_bytes, stream)) != cudaSuccess) return err;
     // one CTA per item when they all fit; otherwise the SMs are divided in
     // proportion to the two kinds of items, so that both take the same number
     // of waves

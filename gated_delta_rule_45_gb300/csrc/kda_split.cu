@@ -73,6 +73,8 @@ SplitLayout split_layout(int32_t num_seqs, int64_t total_tokens, int32_t H, int3
     L.rnorm = take((M - 1) * N * (size_t)H * d_v * sizeof(float));
     L.gstart = take(slots * (size_t)H * d_v * sizeof(float));
     L.qtil = take(T * (size_t)H * d_k * sizeof(float));
+    L.qfro_bytes = slots * (size_t)H * sizeof(float);
+    L.qfro = take(L.qfro_bytes);
     L.ores = take(T * (size_t)H * d_v * sizeof(float));
     // the correction's work list: a count, then (slot, head-block) pairs
     L.clist = take(16 + sizeof(int32_t) * 4 * slots * (size_t)H * (d_v / 128));
@@ -242,12 +244,15 @@ constexpr int kCorrThreads = 512;
 // Persistent: each CTA takes listed chunks in turn.  Thread (r, quarter):
 // value channel r of the block, tokens 16 quarter .. 16 quarter + 15.
 //   G_t,r   = gstart_r * prod_{i <= t} alpha_i,r  <= gstart_r  (alpha <= 1)
-//   bound   = gstart_r * |S_start row r| * |q~_t|  >= |G_t,r (S_start q~_t)_r|
+//   bound   = gstart_r * |S_start row r| * |Q~|_F >= |G_t,r (S_start q~_t)_r|,
+// |Q~|_F the Frobenius norm of the chunk's q~ (accumulated by the transition
+// items), so this first test reads only o; a chunk it keeps is tested again
+// with each token's own |q~_t| (reading q~) before anything is computed.
 // o holds bf16(o from zero) already.  If bound <= 2^-20 |o_t,r| for every
 // element, the share is below 2^-12 of half a bf16 ulp of the value, so the
 // stored value is the rounding of the exact one except in the rare case of
 // a value within that distance of a rounding boundary; the chunk is left as
-// it is (having read only q~ and o).  Otherwise alpha is read and
+// it is.  Otherwise alpha is read and
 // o_t,r = bf16(o from zero + G_t,r (S_start q~_t)_r), with o from zero in
 // fp32 (ores) where the chunk kernel kept it (gstart_r >= kOresFloor), else
 // the bf16 value (where the decay is below kOresFloor the share is small
@@ -255,8 +260,9 @@ constexpr int kCorrThreads = 512;
 __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
     int N, int H, int d_v, const float* __restrict__ alpha, const float* __restrict__ qtil,
     const float* __restrict__ gstart, const float* __restrict__ sst,
-    const float* __restrict__ rnorm, const int32_t* __restrict__ cu,
-    const int32_t* __restrict__ ccount, const int4* __restrict__ clist,
+    const float* __restrict__ rnorm, const float* __restrict__ qfro,
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ ccount,
+    const int4* __restrict__ clist,
     const float* __restrict__ ores, __nv_bfloat16* __restrict__ o,
     const int32_t* __restrict__ status) {
     if (*status == KDA_ERR_DEVICE_INPUT) return;
@@ -279,6 +285,20 @@ __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
         const int ch = vb * kB + r;
         const size_t srow = (((size_t)(j - 1) * N + n) * H + h) * d_v + ch;   // row of sst / rnorm
         __syncthreads();   // the previous item's tiles are no longer read
+        const float* arow = alpha + t0 * ostride + (int64_t)h * d_v + ch;
+        __nv_bfloat16* orow = o + t0 * ostride + (int64_t)h * d_v + ch;
+        const float g0 = gstart[((size_t)e.x * H + h) * d_v + ch];
+        // |q~_t| <= the chunk's Frobenius norm of q~; alpha <= 1, so the decay
+        // at every token of the chunk is at most g0
+        const float b0 = g0 * rnorm[srow] * sqrtf(qfro[(size_t)e.x * H + h]);
+        bool need = false;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int t = 16 * qt + i;
+            if (t < nvalid)
+                need |= !(b0 <= 0x1p-20f * fabsf(__bfloat162float(orow[t * ostride])));
+        }
+        if (!__syncthreads_or(need)) continue;
         {   // the q~ tile: all four loads of a thread in flight together
             float4 q[64 * (kB / 4) / kCorrThreads];
 #pragma unroll
@@ -294,17 +314,6 @@ __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
                 *reinterpret_cast<float4*>(sQ + t * kQld + 4 * k4) = q[u];
             }
         }
-        const float* arow = alpha + t0 * ostride + (int64_t)h * d_v + ch;
-        __nv_bfloat16* orow = o + t0 * ostride + (int64_t)h * d_v + ch;
-        // |o from zero| of this quarter, kept in the state tile's space for the test
-        float* sO = sS;   // [64][128]
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int t = 16 * qt + i;
-            sO[t * kB + r] = t < nvalid ? fabsf(__bfloat162float(orow[t * ostride])) : INFINITY;
-        }
-        const float g0 = gstart[((size_t)e.x * H + h) * d_v + ch];
-        const float rn = rnorm[srow];
         __syncthreads();
         {   // norms of the q~ rows: 8 threads per token
             const int t = tid >> 3, part = tid & 7;
@@ -316,26 +325,32 @@ __global__ void __launch_bounds__(kCorrThreads, 2) split_correct_kernel(
             acc += __shfl_xor_sync(0xffffffffu, acc, 4);
             if (part == 0) sN[t] = sqrtf(acc);
         }
-        __syncthreads();   // sN
-        // alpha <= 1, so the decay at every token of the chunk is at most g0
-        bool need = false;
-        const float b0 = g0 * rn;
+        __syncthreads();
+        {   // the same test with each token's own |q~_t|
+            const float b1 = g0 * rnorm[srow];
+            need = false;
 #pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-            const int t = 16 * qt + i;
-            need |= !(b0 * sN[t] <= 0x1p-20f * sO[t * kB + r]);
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * qt + i;
+                if (t < nvalid)
+                    need |= !(b1 * sN[t] <= 0x1p-20f * fabsf(__bfloat162float(orow[t * ostride])));
+            }
         }
         if (!__syncthreads_or(need)) continue;
         {   // the block's rows of S_start, coalesced, all loads in flight together
             const float4* Sg = reinterpret_cast<const float4*>(sst + (srow - r) * kB);
-            float4 v[kB * kB / 4 / kCorrThreads];
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {   // two rounds of four loads
+                float4 v[kB * kB / 8 / kCorrThreads];
 #pragma unroll
-            for (int u = 0; u < kB * kB / 4 / kCorrThreads; ++u) v[u] = Sg[tid + u * kCorrThreads];
+                for (int u = 0; u < kB * kB / 8 / kCorrThreads; ++u)
+                    v[u] = Sg[tid + (u + h2 * (kB * kB / 8 / kCorrThreads)) * kCorrThreads];
 #pragma unroll
-            for (int u = 0; u < kB * kB / 4 / kCorrThreads; ++u) {
-                const int x = tid + u * kCorrThreads;
-                float* d = sS + (x / (kB / 4)) * (kB + 1) + 4 * (x % (kB / 4));
-                d[0] = v[u].x; d[1] = v[u].y; d[2] = v[u].z; d[3] = v[u].w;
+                for (int u = 0; u < kB * kB / 8 / kCorrThreads; ++u) {
+                    const int x = tid + (u + h2 * (kB * kB / 8 / kCorrThreads)) * kCorrThreads;
+                    float* d = sS + (x / (kB / 4)) * (kB + 1) + 4 * (x % (kB / 4));
+                    d[0] = v[u].x; d[1] = v[u].y; d[2] = v[u].z; d[3] = v[u].w;
+                }
             }
         }
         __syncthreads();
@@ -487,7 +502,8 @@ cudaError_t launch_split_correct(const PrefillArgs& a, const SplitLayout& L, cha
         a.num_seqs, a.H, a.d_v, static_cast<const float*>(a.alpha),
         reinterpret_cast<const float*>(ws + L.qtil), reinterpret_cast<const float*>(ws + L.gstart),
         reinterpret_cast<const float*>(ws + L.sst), reinterpret_cast<const float*>(ws + L.rnorm),
-        a.cu_seqlens, ccount, clist, reinterpret_cast<const float*>(ws + L.ores),
+        reinterpret_cast<const float*>(ws + L.qfro), a.cu_seqlens, ccount, clist,
+        reinterpret_cast<const float*>(ws + L.ores),
         static_cast<__nv_bfloat16*>(a.o), a.status);
     return cudaGetLastError();
 }
