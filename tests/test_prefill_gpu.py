@@ -178,6 +178,7 @@ def _split_case(lengths, H, d_v, s0_std, seed, alpha_mu=3.0):
     ([5000], 3, 128, 0.0, 3.0),             # no initial state
     ([6000, 3000], 2, 128, 0.5, 7.0),       # long memory: every chunk takes a correction
     ([4000, 130], 2, 256, 0.5, 1.0),        # quick decay: corrections die out in a few chunks
+    ([3000], 48, 128, 0.5, 5.0),            # 48 chains: the rule takes two segments
 ])
 def test_sequence_split_matches_oracle(lengths, H, d_v, s0_std, alpha_mu):
     """The split form (one pass: segment 0 from S0, every other segment from
