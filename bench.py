@@ -44,7 +44,7 @@ UNIT = "tokens/s"
 TRAFFIC_CAPTURE = {
     "bytes_per_launch": 10.33e9,
     "date": "2026-12-03",
-    "sources_sha256": "107181fee4102a317e47876189eaa2f8b6e99d9e18a7ac1ce9b0107e6edab1b4",
+    "sources_sha256": "653da9a9b41098d5e235e629e375cb1736a2786ef3cbbd276fed685b1654a904",
 }
 TRAFFIC_SOURCES = ("gated_delta_rule_45_gb300/csrc/kda_prefill_tc.cu",
                    "gated_delta_rule_45_gb300/csrc/kda_tc.cuh")
