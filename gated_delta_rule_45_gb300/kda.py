@@ -7,7 +7,8 @@ library is missing or a call fails, an exception is raised.
 
 The names follow the C ABI: ``prefill`` / ``prefill_into`` wrap
 ``kda_prefill`` / ``kda_prefill_ex``, ``decode_step`` wraps
-``kda_decode_step``, ``workspace_size`` wraps ``kda_prefill_workspace_size``,
+``kda_decode_step``, ``workspace_size`` wraps ``kda_prefill_workspace_size``
+(``kda_prefill_workspace_size_tokens`` when given the token count),
 ``device_status`` wraps ``kda_prefill_device_status`` and ``backward`` /
 ``backward_into`` / ``backward_workspace_size`` wrap ``kda_backward`` and
 ``kda_backward_workspace_size``; ``attnres_layer`` wraps the Blocked Attention

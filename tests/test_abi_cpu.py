@@ -52,6 +52,14 @@ def test_workspace_size(lib):
     assert kda.workspace_size(1000) >= 16 + 4 * 1000
     assert kda.workspace_size(1000) % 256 == 0
     assert lib.kda_prefill_workspace_size(-1, 1, 128, 128, 64) == 0
+    # with the token count: never less than without it (the split's buffers,
+    # where the device would take the split, replace the hand-back bitmap)
+    for N, T, H, dv in ((1, 131072, 32, 128), (8, 32768, 32, 128), (64, 4096, 16, 256)):
+        plain = kda.workspace_size(N, H, 128, dv, 64)
+        tok = kda.workspace_size(N, H, 128, dv, 64, T)
+        assert tok >= plain and tok % 256 == 0
+    assert lib.kda_prefill_workspace_size_tokens(-1, 64, 1, 128, 128, 64) == 0
+    assert lib.kda_prefill_workspace_size_tokens(1, -1, 1, 128, 128, 64) == 0
 
 
 P = ctypes.c_void_p
