@@ -444,3 +444,27 @@ def test_many_short_sequences_tensor_core():
     o2, S2 = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
                          dev["cu_seqlens"], chunk=64, kernel="simt", check_device_status=True)
     assert parity.rel(S_T.cpu().numpy(), S2.cpu().numpy()) < 1e-3
+
+
+def test_split_reports_decay_beyond_the_chunk_forms_range():
+    """Under the sequence-axis split a chunk whose alpha product falls below the
+    chunk form's range is reported (KDA_ERR_DEVICE_RANGE), not handed to the
+    portable kernel; here it lies inside a later segment of one channel.  The
+    other (sequence, head) pairs are still right: rows of the state, and so
+    the segment maps' rows, do not mix."""
+    spec, d = _split_case([2000, 1500], 2, 128, 0.1, seed=45)
+    if not kda.supported("tc_split", 2, 128, 128, torch.bfloat16, 64):
+        pytest.skip("tensor-core kernel not available for this shape")
+    a = int(d["cu_seqlens"][1]) + 800
+    d["alpha"][a:a + 16, 1, 5] = 10.0 ** -2.5     # sequence 1, head 1, channel 5
+    dev = parity.to_device(d)
+    with pytest.raises(kda.KdaError) as e:
+        kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                    dev["cu_seqlens"], chunk=64, kernel="tc_split", check_device_status=True)
+    assert e.value.status == kda.ERR_DEVICE_RANGE
+    o, S_T = kda.prefill(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["beta"], dev["S0"],
+                         dev["cu_seqlens"], chunk=64, kernel="tc_split")
+    torch.cuda.synchronize()
+    ref = parity.oracle_pairs(d, [(0, 0), (0, 1), (1, 0)])
+    wo, ws = parity.compare_pairs(d, o, S_T, ref)
+    assert wo <= parity.TOL_BF16 and ws <= parity.TOL_BF16, (wo, ws)
