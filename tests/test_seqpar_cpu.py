@@ -8,6 +8,7 @@ import os
 import socket
 
 import numpy as np
+import pytest
 import torch
 import torch.multiprocessing as mp
 
@@ -42,8 +43,9 @@ def _worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
-def test_two_ranks_match_the_whole_sequence():
-    world = 2
+@pytest.mark.parametrize("world", [2, 3])
+def test_ranks_match_the_whole_sequence(world):
+    """With 3 ranks the last one chains two earlier segments' maps."""
     port = _free_port()
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
