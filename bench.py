@@ -967,7 +967,7 @@ def main(argv=None):
     p.add_argument("--ref-budget", type=float, default=None,
                    help="seconds of CPU work per reference step / cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-baseline-budget", type=float, default=12.0,
+    p.add_argument("--cpu-baseline-budget", type=float, default=15.0,
                    help="seconds of CPU work for the cpu_baseline sample on every core "
                         "(a quarter of it again on one thread)")
     p.add_argument("--no-components", action="store_true",
