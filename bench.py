@@ -507,7 +507,8 @@ def run_ours(args):
     traffic, traffic_src = stored_traffic()
 
     if rank == 0:
-        ours_launches = 2 + n_dec  # planner + prefill kernel + one kernel per decode step
+        # planner + chunk kernel + fast-decay hand-back kernel + one kernel per decode step
+        ours_launches = 3 + n_dec
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps,
